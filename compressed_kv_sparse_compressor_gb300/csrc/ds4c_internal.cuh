@@ -1,0 +1,138 @@
+// Internal declarations of libds4c: kernel argument blocks and launchers.
+// Every translation unit of the library includes this header; nothing outside
+// the library does.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ds4c.h"
+
+namespace ds4c {
+
+constexpr int kMaxRot = 128;
+constexpr int kMaxDecodeSeq = 1024;
+constexpr uint32_t kMaxIdxCap = 53248;
+
+inline int lane_width(const ds4c_layer_cfg &c, bool attn) { return attn ? (int)c.head_dim : (int)c.idx_head_dim; }
+inline int coff_of(const ds4c_layer_cfg &c) { return c.ratio == 4 ? 2 : 1; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Opt a kernel into `bytes` of dynamic shared memory.  The default limit of
+// 48 KiB covers static and dynamic shared memory together, so the opt-in is
+// made for any request above 16 KiB (every kernel here has less than 16 KiB
+// of static shared memory).  On failure the error is also taken out of the
+// runtime's last-error slot, so it is reported once, by the caller.
+template <typename F>
+inline cudaError_t ensure_dyn_smem(F *func, size_t bytes) {
+    if (bytes <= 16 * 1024) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) cudaGetLastError();
+    return e;
+}
+
+// ----------------------------------------------------------------------------
+// Projection GEMM: C[g][m][n] = sum_k A[m][k] * B[g][n][k], fp32 out.
+// ----------------------------------------------------------------------------
+struct GemmGroup {
+    const void *B;      // [N][K] row-major, dtype
+    float *C;           // [M][ldc]
+    int64_t ldc;
+    int N;
+};
+struct GemmArgs {
+    const void *A;      // [M][K] row-major, dtype
+    int M, K;
+    int dtype;          // DS4C_F32 / DS4C_BF16
+    int n_groups;
+    GemmGroup g[4];
+};
+cudaError_t launch_gemm_simt(const GemmArgs &a, cudaStream_t s);
+// tcgen05 path for bf16 operands; returns cudaErrorNotSupported when the
+// shape is outside what it handles (the caller then uses the SIMT kernel).
+cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s);
+unsigned int gemm_tc_read_clear_error();
+
+// ----------------------------------------------------------------------------
+// Compressor (store + APE, pool, RMSNorm, tail RoPE, FP8, append, frontier).
+// ----------------------------------------------------------------------------
+struct RopeTable { float inv_freq[kMaxRot / 2]; };
+
+struct LaneArgs {
+    const float *kv;  int64_t kv_ld;   // projection output rows (kv part), [rows][ld]
+    const float *sc;  int64_t sc_ld;   // projection output rows (score part)
+    const float *ape;                  // [ratio][W]
+    const float *gain;                 // [Dl] or null
+    float *comp;                       // [n_seq][cap][Dl]
+    float *prequant;                   // same or null
+    float *skv, *ssc;                  // [n_seq][coff*ratio][W]
+    int Dl, cap, is_attn;
+};
+struct CompressArgs {
+    LaneArgs lane[2];
+    int n_lanes;
+    int ratio, n_rot;
+    float eps;
+    RopeTable rope;
+    // segments: prefill = one segment (seq 0); decode = one token per sequence
+    int n_seg;
+    uint64_t pos0;        // prefill
+    uint32_t T;           // prefill tokens
+    const uint64_t *pos_d; // unused
+};
+struct DecodePos { uint64_t pos[kMaxDecodeSeq]; };
+
+cudaError_t launch_compress_prefill(const CompressArgs &a, cudaStream_t s);
+cudaError_t launch_compress_decode(const CompressArgs &a, const DecodePos &p, int n_seq, cudaStream_t s);
+
+// ----------------------------------------------------------------------------
+// Indexer score + top-k
+// ----------------------------------------------------------------------------
+struct IndexerArgs {
+    const float *q;          // [n][d]
+    const float *rows;       // [n_seq][idx_cap][d]
+    int64_t seq_stride;      // idx_cap * d
+    float *scores;           // [n][lds]
+    int64_t lds;
+    int32_t *topk;           // [n][k]
+    int d, k;
+    int n_seq, n_tok;
+    uint64_t pos0;           // prefill
+};
+cudaError_t launch_indexer_prefill(const IndexerArgs &a, cudaStream_t s);
+cudaError_t launch_indexer_decode(const IndexerArgs &a, const DecodePos &p, cudaStream_t s);
+
+// ----------------------------------------------------------------------------
+// Sparse SWA attention + ring commit
+// ----------------------------------------------------------------------------
+struct AttnArgs {
+    const float *q;          // [n][H][D]
+    const float *raw_new;    // [n][D]
+    const float *ring;       // [n_seq][S][D]
+    const float *comp;       // [n_seq][comp_cap][D]
+    const int32_t *topk;     // [n][k] or null
+    float *out;              // [n][H][D]
+    int D, H, S, ratio, k, comp_cap;
+    float scale;
+    int n_seq, n_tok;
+    uint64_t pos0;
+};
+cudaError_t launch_attention(const AttnArgs &a, const DecodePos *p, cudaStream_t s);
+cudaError_t launch_ring_commit(float *ring, const float *raw_new, int D, int S, int n_seq, int n_tok,
+                               uint64_t pos0, const DecodePos *p, cudaStream_t s);
+
+// ----------------------------------------------------------------------------
+// State init, checkpoint gather
+// ----------------------------------------------------------------------------
+cudaError_t launch_fill(float *p, size_t n, float v, cudaStream_t s);
+
+struct GatherSeg { const float *src; int64_t dst_off; int64_t n; };
+struct GatherArgs {
+    float *dst;
+    const float *ring; int64_t D; int64_t S; uint64_t pos; int64_t n_live;
+    int n_seg;
+    GatherSeg seg[8];
+};
+cudaError_t launch_gather(const GatherArgs &a, cudaStream_t s);
+
+}  // namespace ds4c

@@ -1,0 +1,375 @@
+// Projection GEMM on the 5th-generation tensor cores (K1):
+//   C[g][m][n] = sum_k A[m][k] * B_g[n][k]   (bf16 operands, fp32 accumulate)
+// for the wkv / wgate matrices of the attention and indexer lanes
+// ("Metal グラフと圧縮 KV の実装を読む" §4-§5: both projections are coff*head_dim
+// wide; all four share the hidden rows A, so one persistent launch covers them).
+//
+// Design (sm_103a):
+//   - 128 x 256 output tile per CTA, K consumed in 64-element (128-byte) slices;
+//     A and B slices arrive by TMA (cp.async.bulk.tensor, 128-byte swizzle) into
+//     a 4-stage shared-memory ring guarded by mbarriers.
+//   - One elected thread issues tcgen05.mma (kind::f16, M=128, N=256, K=16) with
+//     the accumulator in tensor memory; two 256-column accumulators let the
+//     epilogue of one tile overlap the main loop of the next.
+//   - Warp roles: warp 0 TMA producer, warp 1 MMA issuer (and TMEM owner),
+//     warps 2-5 epilogue (tcgen05.ld 32x32b -> registers -> global fp32).
+//   - Persistent grid of one CTA per SM over (group, n-tile, m-tile).
+//   - Every mbarrier wait is bounded (4 s of %globaltimer); a wait that gives up
+//     raises the library's device error word and the CTA winds down, freeing
+//     its tensor memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "ds4c_internal.cuh"
+
+namespace ds4c {
+
+__device__ unsigned int g_gemm_tc_err;
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 512;
+constexpr int THREADS = 192;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr unsigned long long WAIT_NS = 4000000000ull;
+
+struct TcParams {
+    int M, K;
+    int m_tiles;
+    int n_groups;
+    int tile_start[5];     // prefix sums of tiles per group
+    int n_tiles[4];
+    int N[4];
+    float *C[4];
+    int64_t ldc[4];
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Bounded wait for the completion of the phase with the given parity.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((i & 255u) == 255u) {
+            if (*abort) return false;
+            const uint64_t now = globaltimer();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > WAIT_NS) {
+                *abort = 1;
+                atomicOr(&g_gemm_tc_err, 1u);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle
+// layout TMA writes (8-row atoms of 1024 bytes, stride-byte-offset 1024).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);          // start address
+    d |= (uint64_t)1 << 16;                           // leading-byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;                 // stride-byte offset
+    d |= (uint64_t)1 << 46;                           // descriptor version (tcgen05)
+    d |= (uint64_t)2 << 61;                           // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: kind::f16, A = B = bf16, D = f32, both K-major.
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(IDESC), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tile_coords(const TcParams &p, int tile, int &g, int &mt, int &nt) {
+    g = 0;
+    while (g + 1 < p.n_groups && tile >= p.tile_start[g + 1]) g++;
+    const int local = tile - p.tile_start[g];
+    nt = local / p.m_tiles;
+    mt = local % p.m_tiles;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
+               const __grid_constant__ CUtensorMap mapB1, const __grid_constant__ CUtensorMap mapB2,
+               const __grid_constant__ CUtensorMap mapB3, TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    uint64_t *full = bars, *empty = bars + STAGES, *acc_full = bars + 2 * STAGES, *acc_empty = bars + 2 * STAGES + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4);
+    volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int total = p.tile_start[p.n_groups];
+    const int kb_count = (p.K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; s++) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int a = 0; a < 2; a++) {
+            mbar_init(smem_u32(&acc_full[a]), 1);
+            mbar_init(smem_u32(&acc_empty[a]), 128);
+        }
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapA)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        fence_before();
+    }
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // TMA producer
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                int g, mt, nt;
+                tile_coords(p, tile, g, mt, nt);
+                const CUtensorMap *mb = g == 0 ? &mapB0 : g == 1 ? &mapB1 : g == 2 ? &mapB2 : &mapB3;
+                for (int kb = 0; kb < kb_count; kb++, it++) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort)) { ok = false; break; }
+                    uint8_t *sa = smem + s * STAGE_BYTES;
+                    uint8_t *sb = sa + A_BYTES;
+                    const uint32_t bar = smem_u32(&full[s]);
+                    mbar_expect_tx(bar, STAGE_BYTES);
+                    tma_load_2d(smem_u32(sa), &mapA, kb * BK, mt * BM, bar);
+                    tma_load_2d(smem_u32(sb), mb, kb * BK, nt * BN, bar);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // MMA issuer
+            uint32_t it = 0, local = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, local++) {
+                const int acc = local & 1;
+                const uint32_t aph = (local >> 1) & 1;
+                if (!mbar_wait(smem_u32(&acc_empty[acc]), aph ^ 1, abort)) break;
+                fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < kb_count; kb++, it++) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (!mbar_wait(smem_u32(&full[s]), ph, abort)) { ok = false; break; }
+                    fence_after();
+                    const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; k++)
+                        mma_bf16(d_tmem, sw128_desc(sa + k * 32), sw128_desc(sb + k * 32), (kb > 0 || k > 0) ? 1u : 0u);
+                    mma_commit(smem_u32(&empty[s]));
+                }
+                if (ok) mma_commit(smem_u32(&acc_full[acc]));
+            }
+            // drain: wait (bounded) for every issued MMA before the TMEM is freed
+            if (it > 0) {
+                const uint32_t last = it - 1;
+                mbar_wait(smem_u32(&empty[last % STAGES]), (last / STAGES) & 1, abort);
+            }
+        }
+    } else {
+        // epilogue: warps 2..5 -> TMEM lane quarter (warp % 4)
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        uint32_t local = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, local++) {
+            int g, mt, nt;
+            tile_coords(p, tile, g, mt, nt);
+            const int acc = local & 1;
+            const uint32_t aph = (local >> 1) & 1;
+            if (!mbar_wait(smem_u32(&acc_full[acc]), aph, abort)) break;
+            fence_after();
+            const int m = mt * BM + row;
+            const int n0 = nt * BN;
+            float *crow = p.C[g] + (size_t)m * p.ldc[g];
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; c++) {
+                uint32_t r[32];
+                tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c * 32), r);
+                const int n = n0 + c * 32;
+                if (m < p.M && n < p.N[g]) {
+                    if (n + 32 <= p.N[g]) {
+#pragma unroll
+                        for (int v = 0; v < 8; v++)
+                            *reinterpret_cast<float4 *>(crow + n + 4 * v) =
+                                make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                            __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                    } else {
+                        for (int v = 0; v < 32 && n + v < p.N[g]; v++) crow[n + v] = __uint_as_float(r[v]);
+                    }
+                }
+            }
+            fence_before();
+            mbar_arrive(smem_u32(&acc_empty[acc]));
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+bool make_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t K, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
+    if (a.dtype != DS4C_BF16 || a.M < 64 || a.K % 8 != 0 || a.n_groups < 1 || a.n_groups > 4)
+        return cudaErrorNotSupported;
+    if (((uintptr_t)a.A & 15) != 0) return cudaErrorNotSupported;
+    TcParams p{};
+    p.M = a.M;
+    p.K = a.K;
+    p.m_tiles = (a.M + BM - 1) / BM;
+    p.n_groups = a.n_groups;
+    CUtensorMap mA, mB[4];
+    if (!make_map(&mA, a.A, (uint64_t)a.M, (uint64_t)a.K, BM)) return cudaErrorNotSupported;
+    int start = 0;
+    for (int g = 0; g < 4; g++) {
+        const int gi = g < a.n_groups ? g : a.n_groups - 1;
+        if (g < a.n_groups) {
+            const GemmGroup &G = a.g[g];
+            if (((uintptr_t)G.B & 15) != 0 || (G.ldc % 4) != 0 || ((uintptr_t)G.C & 15) != 0) return cudaErrorNotSupported;
+            if (!make_map(&mB[g], G.B, (uint64_t)G.N, (uint64_t)a.K, BN)) return cudaErrorNotSupported;
+            p.N[g] = G.N;
+            p.C[g] = G.C;
+            p.ldc[g] = G.ldc;
+            p.n_tiles[g] = (G.N + BN - 1) / BN;
+            p.tile_start[g] = start;
+            start += p.n_tiles[g] * p.m_tiles;
+        } else {
+            mB[g] = mB[gi];
+        }
+    }
+    p.tile_start[a.n_groups] = start;
+    cudaError_t e = ensure_dyn_smem(gemm_tc_kernel, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int grid = start < sm_count() ? start : sm_count();
+    gemm_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(mA, mB[0], mB[1], mB[2], mB[3], p);
+    return cudaGetLastError();
+}
+
+unsigned int gemm_tc_read_clear_error() {
+    unsigned int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_gemm_tc_err, sizeof v) != cudaSuccess) return 0;
+    if (v) cudaMemcpyToSymbol(g_gemm_tc_err, &z, sizeof z);
+    return v;
+}
+
+}  // namespace ds4c

@@ -1,0 +1,216 @@
+/*
+ * ds4c — compressed-KV sparse attention path of a DeepSeek-V4-style engine,
+ * as hand-written CUDA for sm_103a (GB300), behind a plain C ABI.
+ *
+ * The method is the one described in "Metal グラフと圧縮 KV の実装を読む"
+ * (DwarfStar/ds4 series part 3; cited below as [P2] with its section) and the
+ * checkpoint layout of "【#4】ds4.c を読み解く" ([P1]).  Per layer and token a
+ * learned compressor projects the hidden state (wkv, wgate), adds a learned
+ * position bias (APE) to the score, stores both into a recurrent frontier and,
+ * at every ratio boundary, softmax-pools the frontier into one row that goes
+ * through RMSNorm, a RoPE on its last n_rot dims and (attention lane) an FP8
+ * E4M3 round trip before it is appended to the compressed KV.  Ratio-4 layers
+ * run a second (indexer) lane; a top-k over the indexer rows selects which
+ * compressed rows the attention sees next to a 128-row raw sliding window.
+ *
+ * Conventions shared by every call
+ *   - Tensor pointers are DEVICE pointers owned by the caller, unless a name
+ *     ends in _h (host pointer).  The library allocates no device memory; its
+ *     scratch is the caller's workspace, sized by ds4c_workspace_bytes.
+ *   - Calls are asynchronous on `stream`.  Arguments are validated on the host
+ *     before anything is launched, so a call that returns an error has no
+ *     side effect.  Calls on one layer state must be ordered on one stream.
+ *   - A position `pos` counts tokens already processed by a sequence; token
+ *     `pos` is the next one.  Compressed row c of a ratio-r layer pools the
+ *     window of tokens c*r .. c*r+r-1 and exists once pos >= (c+1)*r.
+ *   - Row-major layouts; "[a][b]" lists the slowest dimension first.
+ *   - Kernel-side problems (an exhausted bounded wait) raise a sticky device
+ *     error word that ds4c_sync_status reports and clears.
+ */
+#ifndef DS4C_H
+#define DS4C_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define DS4C_API __attribute__((visibility("default")))
+#else
+#define DS4C_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DS4C_OK = 0,
+    DS4C_ERR_NULL = 1,         /* a required pointer is NULL */
+    DS4C_ERR_SHAPE = 2,        /* a configuration value outside the supported set */
+    DS4C_ERR_CAPACITY = 3,     /* positions past comp_cap*ratio, or an output buffer too small */
+    DS4C_ERR_UNSUPPORTED = 4,  /* n_seq > 1 together with n_tok > 1, or a batch above the limit */
+    DS4C_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed */
+    DS4C_ERR_DEVICE = 6,       /* a kernel reported a failure through the device error word */
+    DS4C_ERR_WORKSPACE = 7     /* workspace NULL or smaller than ds4c_workspace_bytes */
+} ds4c_status;
+
+enum { DS4C_F32 = 0, DS4C_BF16 = 1 };
+
+/* One layer's shape.  [P2] §1 (ratio 0, 4 or 128 per layer), §2 (swa: raw
+ * ring rows, 128 on Flash), §6 (indexer head_dim 128, top-k 512), §8
+ * (head_dim 512 with the last n_rot = 64 dims rotated; compressed layers use
+ * their own RoPE base).
+ * Supported: ratio in {0,4,128}; head_dim and idx_head_dim in {64,128,256,512};
+ * n_rot a multiple of 4, 4 <= n_rot <= min(head_dim, idx_head_dim), at most 128;
+ * d_model a multiple of 8; n_heads a multiple of 8, at most 128;
+ * 1 <= swa <= 1024; 1 <= top_k <= 2048; idx_cap <= 53248. */
+typedef struct {
+    uint32_t d_model;       /* hidden width fed to the projections */
+    uint32_t head_dim;      /* D: width of a raw / compressed attention row (K = V = the row) */
+    uint32_t n_rot;         /* R: RoPE tail width */
+    uint32_t idx_head_dim;  /* d: indexer row width (ratio-4 layers) */
+    uint32_t n_heads;       /* H: query heads sharing the single KV row */
+    uint32_t ratio;         /* 0, 4 or 128 */
+    uint32_t swa;           /* raw ring rows S */
+    uint32_t top_k;         /* k: compressed rows an attention query keeps (ratio 4) */
+    uint32_t comp_cap;      /* attention compressed rows per sequence */
+    uint32_t idx_cap;       /* indexer compressed rows per sequence (ratio 4) */
+    uint32_t dtype;         /* DS4C_F32 or DS4C_BF16: element type of weights and hidden */
+    float rms_eps;          /* RMSNorm epsilon */
+    float attn_scale;       /* logit scale, 1/sqrt(head_dim) in the shipped configs */
+    float rope_base;        /* compressed-layer RoPE base; theta_i = base^(-2i/n_rot) */
+} ds4c_layer_cfg;
+
+/* One compressor lane's weights ([P2] §4, §6: the attention lane and, on
+ * ratio-4 layers, the indexer lane with its own ape/kv/gate/norm tensors).
+ * With Dl = head_dim (attention lane) or idx_head_dim (indexer lane) and
+ * coff = 2 on ratio-4 layers, 1 otherwise:
+ *   wkv, wgate: [coff*Dl][d_model] of cfg->dtype;
+ *   ape:        [ratio][coff*Dl] float, row pos % ratio is added to the score;
+ *   norm:       [Dl] float RMSNorm gain, or NULL for ones. */
+typedef struct {
+    const void *wkv;
+    const void *wgate;
+    const float *ape;
+    const float *norm;
+} ds4c_lane_weights;
+
+/* One lane's state for n_seq sequences ([P2] §2 ds4_layer_cache: compressed
+ * rows plus the frontier state_kv / state_score):
+ *   comp:        [n_seq][cap][Dl]  appended compressed rows (cap = comp_cap or idx_cap);
+ *   state_kv:    [n_seq][coff*ratio][coff*Dl]  frontier (ratio 4: rows 0..3 previous
+ *                window, rows 4..7 current window, [P2] §5);
+ *   state_score: same shape, scores with the APE already added;
+ *   prequant:    optional [n_seq][cap][Dl]: each compressed row as it was before the
+ *                FP8 round trip (inspection output), NULL = not written. */
+typedef struct {
+    float *comp;
+    float *state_kv;
+    float *state_score;
+    float *prequant;
+} ds4c_lane_state;
+
+/* A layer's state: raw: [n_seq][swa][head_dim] ring, slot p % swa holds the raw
+ * row of position p ([P2] §2 raw_kv).  idx is unused unless ratio == 4.
+ * Calls with n_seq == 1 treat the pointers as the one sequence they address. */
+typedef struct {
+    float *raw;
+    ds4c_lane_state attn;
+    ds4c_lane_state idx;
+} ds4c_layer_state;
+
+/* Bytes of workspace a call on `cfg` needs when it processes at most
+ * `max_rows` rows (n_tok of a prefill chunk, or n_seq of a decode step).
+ * Returns 0 for an invalid cfg. */
+DS4C_API size_t ds4c_workspace_bytes(const ds4c_layer_cfg *cfg, uint32_t max_rows);
+
+/* Fresh state for n_seq sequences: frontier kv = 0 and score = -inf (so rows
+ * no token wrote carry no pooling weight), raw ring zeroed.  Compressed rows
+ * are left as they are. */
+DS4C_API ds4c_status ds4c_state_init(const ds4c_layer_cfg *cfg, const ds4c_layer_state *state,
+                            uint32_t n_seq, cudaStream_t stream);
+
+/* Compressor over n_tok tokens of one sequence at absolute positions
+ * pos0 .. pos0+n_tok-1 ([P2] §3 chunked prefill with absolute-position
+ * boundaries; §4 compressor_decode_one; §5 ratio-4 frontier and shift; §8
+ * tail RoPE; §9 FP8 round trip).  hidden: [n_tok][d_model] of cfg->dtype.
+ * idx must be non-NULL exactly when ratio == 4.  Appends rows
+ * pos0/ratio .. (pos0+n_tok)/ratio - 1 of each lane and leaves the frontier as
+ * the token-by-token recurrence would.  Ratio 0: nothing to do, returns OK.
+ * Errors: DS4C_ERR_CAPACITY when (pos0+n_tok)/ratio exceeds a lane's cap. */
+DS4C_API ds4c_status ds4c_compress_prefill(const ds4c_layer_cfg *cfg, const ds4c_lane_weights *attn,
+                                  const ds4c_lane_weights *idx, const ds4c_layer_state *state,
+                                  const void *hidden, uint32_t n_tok, uint64_t pos0,
+                                  void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Compressor for one token of each of n_seq independent sequences, sequence b
+ * at position pos_h[b] (host array).  hidden: [n_seq][d_model].  n_seq <= 1024. */
+DS4C_API ds4c_status ds4c_compress_decode_step(const ds4c_layer_cfg *cfg, const ds4c_lane_weights *attn,
+                                      const ds4c_lane_weights *idx, const ds4c_layer_state *state,
+                                      const void *hidden, const uint64_t *pos_h, uint32_t n_seq,
+                                      void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Indexer top-k of a ratio-4 layer ([P2] §6, §7).  Queries: either n_tok
+ * tokens of one sequence at pos_h[0] .. pos_h[0]+n_tok-1 (n_seq == 1), or one
+ * token per sequence at pos_h[b] (n_tok == 1).  q_idx: [n][idx_head_dim]
+ * float, n = n_seq*n_tok.  A query at position t scores rows c < (t+1)/4 of
+ * its sequence's index_comp_kv with s = fmaf chain over i = 0..d-1 of
+ * q[i]*row[i] (float, in order) and keeps the top_k largest (ties: lower
+ * index), written to topk [n][top_k] in ascending index order, padded with -1.
+ * scores (optional, NULL = not written): [n][score_stride] floats, column c
+ * valid for c < (t+1)/4; score_stride >= max over queries of (t+1)/4. */
+DS4C_API ds4c_status ds4c_indexer_topk(const ds4c_layer_cfg *cfg, const ds4c_layer_state *state,
+                              const float *q_idx, const uint64_t *pos_h, uint32_t n_seq,
+                              uint32_t n_tok, int32_t *topk, float *scores, size_t score_stride,
+                              void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Sparse sliding-window attention ([P2] §7 indexed mixed attention): for each
+ * query at position t and head h, one softmax over the raw rows of positions
+ * max(0, t+1-swa) .. t and the compressed rows: ratio 4 the topk list (entries
+ * < 0 skipped, the first entry >= (t+1)/4 ends the list), ratio 128 every row
+ * c < (t+1)/128, ratio 0 none.  logit = (q . row) * attn_scale; out = sum p*row.
+ * Query layout as ds4c_indexer_topk; q: [n][n_heads][head_dim] float (already
+ * rotated); raw_new: [n][head_dim] float, the raw rows of the queries' own
+ * positions; positions before pos_h[.] come from the ring.  out: [n][n_heads]
+ * [head_dim] float.  commit_ring != 0 then writes raw_new into the ring (the
+ * last min(n_tok, swa) rows of a chunk; one row per sequence in a decode
+ * step), after the attention has read it.  topk may be NULL unless ratio == 4. */
+DS4C_API ds4c_status ds4c_sparse_swa_attn(const ds4c_layer_cfg *cfg, const ds4c_layer_state *state,
+                                 const float *q, const float *raw_new, const int32_t *topk,
+                                 const uint64_t *pos_h, uint32_t n_seq, uint32_t n_tok,
+                                 float *out, int commit_ring, void *ws, size_t ws_bytes,
+                                 cudaStream_t stream);
+
+/* Floats of one sequence's checkpoint after pos tokens:
+ *   min(pos, swa)*D + [ratio != 0] ((pos/ratio)*D + 2*(coff*ratio)*(coff*D))
+ *   + [ratio == 4] ((pos/4)*d + 2*8*(2d)). */
+DS4C_API size_t ds4c_checkpoint_floats(const ds4c_layer_cfg *cfg, uint64_t pos);
+
+/* Logical-order checkpoint of sequence `seq` after pos tokens into dst ([P1]
+ * §5 payload body order, §6 the raw ring written in logical position order,
+ * §7 frontier tensors): raw rows of positions pos-n_live .. pos-1 (n_live =
+ * min(pos, swa)), attn comp rows 0 .. pos/ratio-1, attn state_kv, attn
+ * state_score, then on ratio-4 layers idx comp rows 0 .. pos/4-1, idx
+ * state_kv, idx state_score.  Bit copy.  dst_floats < ds4c_checkpoint_floats
+ * -> DS4C_ERR_CAPACITY.  *written_h (host, optional) receives the count. */
+DS4C_API ds4c_status ds4c_checkpoint_gather(const ds4c_layer_cfg *cfg, const ds4c_layer_state *state,
+                                   uint32_t seq, uint64_t pos, float *dst, size_t dst_floats,
+                                   size_t *written_h, cudaStream_t stream);
+
+/* Synchronises `stream`, then reports (and clears) the device error word:
+ * DS4C_ERR_DEVICE if a kernel raised it, DS4C_ERR_CUDA if the stream failed. */
+DS4C_API ds4c_status ds4c_sync_status(cudaStream_t stream);
+
+/* Static description of a status code. */
+DS4C_API const char *ds4c_status_string(ds4c_status status);
+
+/* Name of the CUDA runtime error behind the calling thread's most recent
+ * DS4C_ERR_CUDA ("cudaSuccess" if there was none), for diagnostics. */
+DS4C_API const char *ds4c_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS4C_H */

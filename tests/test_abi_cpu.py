@@ -1,0 +1,114 @@
+"""Host-side checks of libds4c that need no GPU: the library loads, exports every
+symbol include/ds4c.h declares, sizes its buffers as the oracle does, and
+rejects bad arguments on the host before anything is launched."""
+
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from compressed_kv_sparse_compressor_gb300 import abi, configs
+from compressed_kv_sparse_compressor_gb300 import build as build_mod
+from helpers import orc_layer
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_mod.build()
+    return abi.lib()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "ds4c.h")).read()
+    return sorted(set(re.findall(r"\b(ds4c_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    syms = declared_symbols()
+    assert set(syms) == set(abi.EXPORTS)
+    for s in syms:
+        assert hasattr(L, s), s
+
+
+def _cfg(shape, comp_cap=64, idx_cap=64):
+    return abi.LayerCfg(d_model=shape.d_model, head_dim=shape.head_dim, n_rot=shape.n_rot,
+                        idx_head_dim=shape.idx_head_dim, n_heads=shape.n_heads, ratio=shape.ratio, swa=shape.swa,
+                        top_k=shape.top_k, comp_cap=comp_cap, idx_cap=idx_cap,
+                        dtype=abi.DS4C_F32 if shape.dtype == "f32" else abi.DS4C_BF16, rms_eps=shape.rms_eps,
+                        attn_scale=shape.attn_scale, rope_base=shape.rope_base)
+
+
+def test_checkpoint_floats_matches_oracle(L, orc):
+    for w in (configs.C1, configs.C2, configs.C5):
+        for ratio in (0, 4, 128):
+            shape = configs.LayerShape(**{**w.layer.__dict__, "ratio": ratio})
+            cap = 40000
+            cfg = _cfg(shape, cap, cap)
+            for pos in (0, 3, 127, 128, 1000, 131072):
+                assert abi.ds4c_checkpoint_floats(cfg, pos) == orc.checkpoint_floats(orc_layer(shape, cap, cap), pos)
+
+
+def test_invalid_configs_are_rejected(L):
+    base = configs.C1.layer
+    assert abi.ds4c_workspace_bytes(_cfg(base), 64) > 0
+    for bad in (dict(ratio=3), dict(head_dim=96), dict(n_heads=12), dict(n_rot=6), dict(d_model=100),
+                dict(idx_head_dim=48), dict(swa=0), dict(top_k=0)):
+        shape = configs.LayerShape(**{**base.__dict__, **bad})
+        assert abi.ds4c_workspace_bytes(_cfg(shape), 64) == 0, bad
+
+
+FAKE = 1 << 20          # an aligned non-NULL address that is never dereferenced
+
+
+def _state():
+    lane = abi.LaneState(FAKE, FAKE, FAKE, None)
+    return abi.LayerState(FAKE, lane, lane)
+
+
+def _weights():
+    return abi.LaneWeights(FAKE, FAKE, FAKE, None)
+
+
+def test_host_validation_errors(L):
+    shape = configs.C1.layer
+    cfg = _cfg(shape, comp_cap=16, idx_cap=16)
+    st, w = _state(), _weights()
+    ws_need = abi.ds4c_workspace_bytes(cfg, 64)
+    pos1 = abi.u64_array([0])
+    # NULL hidden / weights
+    assert abi.ds4c_compress_prefill(cfg, w, w, st, None, 64, 0, FAKE, ws_need, None) == abi.DS4C_ERR_NULL
+    assert abi.ds4c_compress_prefill(cfg, None, w, st, FAKE, 64, 0, FAKE, ws_need, None) == abi.DS4C_ERR_NULL
+    # ratio-4 needs the indexer lane
+    assert abi.ds4c_compress_prefill(cfg, w, None, st, FAKE, 64, 0, FAKE, ws_need, None) == abi.DS4C_ERR_NULL
+    # capacity: 68 tokens make 17 rows > comp_cap 16
+    assert abi.ds4c_compress_prefill(cfg, w, w, st, FAKE, 68, 0, FAKE, ws_need, None) == abi.DS4C_ERR_CAPACITY
+    # workspace
+    assert abi.ds4c_compress_prefill(cfg, w, w, st, FAKE, 64, 0, FAKE, ws_need - 1, None) == abi.DS4C_ERR_WORKSPACE
+    assert abi.ds4c_compress_prefill(cfg, w, w, st, FAKE, 64, 0, None, ws_need, None) == abi.DS4C_ERR_WORKSPACE
+    # misaligned pointer
+    assert abi.ds4c_compress_prefill(cfg, w, w, st, FAKE + 4, 64, 0, FAKE, ws_need, None) == abi.DS4C_ERR_SHAPE
+    # n_seq > 1 with n_tok > 1
+    pos2 = abi.u64_array([0, 0])
+    assert abi.ds4c_indexer_topk(cfg, st, FAKE, pos2, 2, 4, FAKE, None, 0, FAKE, ws_need, None) == abi.DS4C_ERR_UNSUPPORTED
+    assert abi.ds4c_sparse_swa_attn(cfg, st, FAKE, FAKE, FAKE, pos2, 2, 4, FAKE, 1, FAKE, ws_need, None) == \
+        abi.DS4C_ERR_UNSUPPORTED
+    # indexer on a non-ratio-4 layer
+    cfg128 = _cfg(configs.LayerShape(**{**shape.__dict__, "ratio": 128}), comp_cap=16)
+    assert abi.ds4c_indexer_topk(cfg128, st, FAKE, pos1, 1, 4, FAKE, None, 0, FAKE, ws_need, None) == abi.DS4C_ERR_SHAPE
+    # scores buffer too narrow: 64 queries from 0 see up to 16 rows
+    assert abi.ds4c_indexer_topk(cfg, st, FAKE, pos1, 1, 64, FAKE, FAKE, 15, FAKE, ws_need, None) == abi.DS4C_ERR_CAPACITY
+    # ratio-4 attention needs a top-k list
+    assert abi.ds4c_sparse_swa_attn(cfg, st, FAKE, FAKE, None, pos1, 1, 4, FAKE, 1, FAKE, ws_need, None) == \
+        abi.DS4C_ERR_NULL
+    # decode batch above the limit
+    big = abi.u64_array([0] * 1025)
+    assert abi.ds4c_compress_decode_step(cfg, w, w, st, FAKE, big, 1025, FAKE, ws_need, None) == \
+        abi.DS4C_ERR_UNSUPPORTED
+    # checkpoint buffer too small
+    n = abi.ds4c_checkpoint_floats(cfg, 40)
+    written = C.c_size_t(0)
+    assert abi.ds4c_checkpoint_gather(cfg, st, 0, 40, FAKE, n - 1, C.byref(written), None) == abi.DS4C_ERR_CAPACITY
+    assert abi.status_string(abi.DS4C_ERR_CAPACITY).startswith("positions")

@@ -1,0 +1,206 @@
+"""GPU parity of every call of the C ABI against the oracle (-m gpu).
+
+Protocol: each call is compared with the oracle run on that call's own inputs
+(the GPU state before the call, downloaded): compressed rows and frontier
+within rel 2e-3 / abs 1e-4 (the FP8 round trip bit-exact on the GPU's own
+pre-quantisation row), indexer scores and top-k bit-exact, attention within
+the tolerance, ring commit and checkpoint gather bit-exact.  Sizes span several
+tiles with ragged tails; the full-size workloads are checked on sampled outputs.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from compressed_kv_sparse_compressor_gb300 import configs
+from gpu_util import (ATOL, RTOL, check_attention_sampled, check_compress, check_indexer_sampled, device_layer,
+                      download, require_gpu)
+from helpers import lane_np, np_in, orc_layer
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+    orc.build()
+
+
+def _run_chunk(dl, wa, wi, shape, seed, pos0, T, report, sample=None, check=True, layer=0):
+    """One prefill chunk through all four calls, each checked stage-wise."""
+    dev = "cuda"
+    h = configs.hidden(shape, seed, T, offset_tok=pos0, layer=layer).to(dev)
+    q, q_idx, raw = (x.to(dev) for x in configs.queries(shape, seed, T, offset_tok=pos0, layer=layer))
+    before = download(dl) if check else None
+    dl.compress_prefill(h, pos0)
+    after = download(dl) if check else None
+    if check and shape.ratio:
+        check_compress(before, after, wa, wi, h.cpu(), pos0, report)
+    topk = None
+    n = np.arange(T) if sample is None else np.asarray(sample)
+    if shape.ratio == 4:
+        V = (pos0 + T) // 4
+        topk = torch.empty(T, shape.top_k, dtype=torch.int32, device=dev)
+        scores = torch.full((T, max(V, 4)), float("nan"), device=dev)
+        dl.indexer_topk(q_idx, [pos0], 1, T, topk, scores, scores.shape[1])
+        if check:
+            check_indexer_sampled(after, q_idx.cpu().numpy(), [pos0 + j for j in range(T)], topk.cpu().numpy(),
+                                  scores.cpu().numpy(), n)
+    out = torch.empty(T, shape.n_heads, shape.head_dim, device=dev)
+    dl.attention(q, raw, topk, [pos0], 1, T, out, commit_ring=True)
+    dl.sync()
+    if check:
+        check_attention_sampled(after, q.cpu().numpy(), raw.cpu().numpy(),
+                                None if topk is None else topk.cpu().numpy(), out.cpu().numpy(), pos0, n)
+        # ring commit: slot p % S holds raw row p for the chunk's last min(T, S) positions
+        ring = dl.raw[0].cpu().numpy()
+        rawc = raw.cpu().numpy()
+        for p in range(max(pos0, pos0 + T - shape.swa), pos0 + T):
+            np.testing.assert_array_equal(ring[p % shape.swa], rawc[p - pos0])
+    return topk, out
+
+
+def _gather_check(dl, pos):
+    n = dl.checkpoint_floats(pos)
+    dst = torch.full((n + 8,), float("nan"), device="cuda")
+    w = dl.checkpoint_gather(0, pos, dst)
+    dl.sync()
+    assert w == n
+    st = download(dl)
+    np.testing.assert_array_equal(dst[:n].cpu().numpy(), orc.checkpoint_gather(st, pos))
+    assert torch.isnan(dst[n:]).all()
+
+
+# ---------------------------------------------------------------------------
+# "One ratio-4 layer, 64-token prefill, fp32 throughout, seed 0"
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("splits", [[64], [16, 48], [37, 27]])
+def test_c1(splits):
+    w = configs.C1
+    shape = w.layer
+    dl, wa, wi = device_layer(shape, comp_cap=16, idx_cap=16, seed=w.seed)
+    report = {}
+    pos = 0
+    for T in splits:
+        _run_chunk(dl, wa, wi, shape, w.seed, pos, T, report)
+        pos += T
+    _gather_check(dl, pos)
+    # the chunk split does not change the state beyond fp32 rounding
+    ref, _, _ = device_layer(shape, comp_cap=16, idx_cap=16, seed=w.seed)
+    ref.compress_prefill(configs.hidden(shape, w.seed, 64).cuda(), 0)
+    torch.cuda.synchronize()
+    torch.testing.assert_close(dl.attn_comp, ref.attn_comp, rtol=RTOL, atol=ATOL)
+    torch.testing.assert_close(dl.idx_comp, ref.idx_comp, rtol=RTOL, atol=ATOL)
+
+
+def test_c1_chain_against_oracle_end_to_end():
+    """Chain report: the oracle's own end-to-end run (its own state and top-k)."""
+    w = configs.C1
+    shape = w.layer
+    dl, wa, wi = device_layer(shape, comp_cap=16, idx_cap=16, seed=w.seed)
+    topk, out = _run_chunk(dl, wa, wi, shape, w.seed, 0, 64, {}, check=False)
+    st = orc.State(orc_layer(shape, 16, 16))
+    orc.state_init(st)
+    orc.compress(st, lane_np(wa), lane_np(wi), np_in(configs.hidden(shape, w.seed, 64)), 0)
+    q, q_idx, raw = configs.queries(shape, w.seed, 64)
+    tk = orc.indexer_topk(st, q_idx.numpy(), np.arange(64))
+    o = orc.attention(st, q.numpy(), raw.numpy(), tk, 0)
+    gt = topk.cpu().numpy()
+    overlap = np.mean([len(set(a[a >= 0]) & set(b[b >= 0])) / max(1, len(set(b[b >= 0]))) for a, b in zip(gt, tk)])
+    assert overlap > 0.95
+    same = np.all(gt == tk, axis=1)
+    np.testing.assert_allclose(out.cpu().numpy()[same], o[same], rtol=RTOL, atol=ATOL)
+
+
+# ---------------------------------------------------------------------------
+# Multi-tile shapes with ragged tails (D=512, d=128, 64 heads)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("ratio", [0, 4, 128])
+def test_ragged_chunks(ratio):
+    shape = configs.LayerShape(d_model=512, head_dim=512, n_rot=64, idx_head_dim=128, n_heads=64, ratio=ratio,
+                               top_k=16, dtype="bf16", w_std=0.04)
+    seed = 21
+    T_total = 300 if ratio != 128 else 700
+    cap = T_total // max(ratio, 1) + 1
+    dl, wa, wi = device_layer(shape, comp_cap=cap, idx_cap=T_total // 4 + 1, seed=seed, gamma_std=0.1)
+    report = {}
+    pos = 0
+    for T in ([131, 169] if ratio != 128 else [131, 300, 269]):
+        sample = sorted(set([0, 1, 2, 3, T // 2, T - 2, T - 1] + list(range(0, T, 37))))
+        _run_chunk(dl, wa, wi, shape, seed, pos, T, report, sample=sample)
+        pos += T
+    _gather_check(dl, pos)
+
+
+# ---------------------------------------------------------------------------
+# Decode: B sequences, one token each at staggered positions
+# ---------------------------------------------------------------------------
+
+def test_decode_small():
+    shape = configs.LayerShape(d_model=512, head_dim=512, n_rot=64, idx_head_dim=128, n_heads=64, ratio=4,
+                               top_k=16, dtype="bf16", w_std=0.04)
+    seed, B = 31, 8
+    lens = [60 + b for b in range(B)]                    # every stagger class, some emit this step
+    cap = max(lens) // 4 + 2
+    dl, wa, wi = device_layer(shape, comp_cap=cap, idx_cap=cap, n_seq=B, seed=seed, max_rows=128)
+    for b in range(B):
+        view = dl.seq_view(b)
+        saved = dl.state
+        dl.state = view
+        h = configs.hidden(shape, seed, lens[b], layer=b).cuda()
+        _, _, raw = configs.queries(shape, seed, lens[b], layer=b)
+        dl.compress_prefill(h, 0)
+        dl.state = saved
+        for p in range(max(0, lens[b] - shape.swa), lens[b]):
+            dl.raw[b, p % shape.swa] = raw[p].cuda()
+    torch.cuda.synchronize()
+    befores = [download(dl, b) for b in range(B)]
+    hid = torch.stack([configs.hidden(shape, seed, 1, offset_tok=lens[b], layer=b)[0] for b in range(B)]).cuda()
+    qs = [configs.queries(shape, seed, 1, offset_tok=lens[b], layer=b) for b in range(B)]
+    q = torch.cat([x[0] for x in qs]).cuda()
+    q_idx = torch.cat([x[1] for x in qs]).cuda()
+    raw = torch.cat([x[2] for x in qs]).cuda()
+    dl.compress_decode(hid, lens)
+    topk = torch.empty(B, shape.top_k, dtype=torch.int32, device="cuda")
+    vmax = (max(lens) + 1) // 4
+    scores = torch.full((B, vmax), float("nan"), device="cuda")
+    dl.indexer_topk(q_idx, lens, B, 1, topk, scores, vmax)
+    out = torch.empty(B, shape.n_heads, shape.head_dim, device="cuda")
+    after_compress = [None] * B
+    torch.cuda.synchronize()
+    after_compress = [download(dl, b) for b in range(B)]
+    dl.attention(q, raw, topk, lens, B, 1, out, commit_ring=True)
+    dl.sync()
+    for b in range(B):
+        check_compress(befores[b], after_compress[b], wa, wi, hid[b:b + 1].cpu(), lens[b])
+        check_indexer_sampled(after_compress[b], q_idx[b:b + 1].cpu().numpy(), [lens[b]],
+                              topk[b:b + 1].cpu().numpy(), scores[b:b + 1].cpu().numpy(), [0])
+        check_attention_sampled(after_compress[b], q[b:b + 1].cpu().numpy(), raw[b:b + 1].cpu().numpy(),
+                                topk[b:b + 1].cpu().numpy(), out[b:b + 1].cpu().numpy(), lens[b], [0])
+        np.testing.assert_array_equal(dl.raw[b, lens[b] % shape.swa].cpu().numpy(), raw[b].cpu().numpy())
+    # decode(t) equals prefill's t-th step: a fresh one-shot prefill of len+1 tokens
+    for b in (0, 3):
+        ref, _, _ = device_layer(shape, comp_cap=cap, idx_cap=cap, seed=seed)
+        ref.compress_prefill(configs.hidden(shape, seed, lens[b] + 1, layer=b).cuda(), 0)
+        torch.cuda.synchronize()
+        torch.testing.assert_close(dl.attn_comp[b], ref.attn_comp[0], rtol=RTOL, atol=ATOL)
+        torch.testing.assert_close(dl.attn_kv[b], ref.attn_kv[0], rtol=RTOL, atol=ATOL)
+        torch.testing.assert_close(dl.idx_comp[b], ref.idx_comp[0], rtol=RTOL, atol=ATOL)
+
+
+# ---------------------------------------------------------------------------
+# "One ratio-128 layer, 8192-token prefill in two 4096-token chunks" (full size)
+# ---------------------------------------------------------------------------
+
+def test_c2_full():
+    w = configs.C2
+    shape = w.layer
+    dl, wa, wi = device_layer(shape, comp_cap=w.n_tok // 128, seed=w.seed)
+    report = {}
+    for c in range(w.n_tok // w.chunk):
+        sample = [0, 1, 127, 128, 1000, 2047, 4094, 4095]
+        _run_chunk(dl, wa, wi, shape, w.seed, c * w.chunk, w.chunk, report, sample=sample)
+    _gather_check(dl, w.n_tok)
