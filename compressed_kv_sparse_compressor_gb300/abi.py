@@ -25,7 +25,7 @@ DS4C_BF16 = 1
 EXPORTS = (
     "ds4c_workspace_bytes", "ds4c_state_init", "ds4c_compress_prefill", "ds4c_compress_decode_step",
     "ds4c_indexer_topk", "ds4c_sparse_swa_attn", "ds4c_checkpoint_floats", "ds4c_checkpoint_gather",
-    "ds4c_sync_status", "ds4c_status_string", "ds4c_last_cuda_error",
+    "ds4c_sync_status", "ds4c_status_string", "ds4c_last_cuda_error", "ds4c_attn_uses_tensor_cores",
 )
 
 
@@ -52,7 +52,7 @@ class LaneWeights(C.Structure):
 
 class LaneState(C.Structure):
     _fields_ = [("comp", C.c_void_p), ("state_kv", C.c_void_p), ("state_score", C.c_void_p),
-                ("prequant", C.c_void_p)]
+                ("prequant", C.c_void_p), ("comp_split", C.c_void_p)]
 
 
 class LayerState(C.Structure):
@@ -74,7 +74,8 @@ def lib() -> C.CDLL:
     cfgp, lwp, lsp = C.POINTER(LayerCfg), C.POINTER(LaneWeights), C.POINTER(LayerState)
     st = C.c_int
     sig = {
-        "ds4c_workspace_bytes": (SZ, [cfgp, U32]),
+        "ds4c_workspace_bytes": (SZ, [cfgp, U32, U32]),
+        "ds4c_attn_uses_tensor_cores": (C.c_int, [cfgp]),
         "ds4c_state_init": (st, [cfgp, lsp, U32, P]),
         "ds4c_compress_prefill": (st, [cfgp, lwp, lwp, lsp, P, U32, U64, P, SZ, P]),
         "ds4c_compress_decode_step": (st, [cfgp, lwp, lwp, lsp, P, C.POINTER(U64), U32, P, SZ, P]),
@@ -111,8 +112,12 @@ def u64_array(values):
 # Thin call wrappers with the ABI's names; pointers are ints (device
 # addresses), None for NULL.  Each returns the raw status.
 
-def ds4c_workspace_bytes(cfg, max_rows):
-    return lib().ds4c_workspace_bytes(C.byref(cfg), max_rows)
+def ds4c_workspace_bytes(cfg, max_tok, max_seq=0):
+    return lib().ds4c_workspace_bytes(C.byref(cfg), max_tok, max_seq)
+
+
+def ds4c_attn_uses_tensor_cores(cfg):
+    return lib().ds4c_attn_uses_tensor_cores(C.byref(cfg))
 
 
 def ds4c_state_init(cfg, state, n_seq, stream):

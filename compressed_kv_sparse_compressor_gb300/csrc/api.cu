@@ -38,17 +38,25 @@ ds4c_status check_cfg(const ds4c_layer_cfg *c) {
 // Projection width of one lane (kv and score each): coff * Dl.
 int proj_width(const ds4c_layer_cfg &c, bool attn) { return coff_of(c) * lane_width(c, attn); }
 
-// Workspace layout (all regions 256-byte aligned):
-//   proj: [rows][P] float, P = 2*W_attn (+ 2*W_idx on ratio-4 layers)
-//         columns: attn kv | attn score | idx kv | idx score
+// Workspace layout of one call (all regions 256-byte aligned):
+//   proj:   [rows][P] float, P = 2*W_attn (+ 2*W_idx on ratio-4 layers)
+//           columns: attn kv | attn score | idx kv | idx score
 //   scores: [rows][lds] float, lds = idx_cap rounded up to 4 (ratio 4)
+//   mirror: [mirror_rows][2][head_dim] bf16 raw rows for the tensor-core
+//           attention (128 + n_tok rows for a prefill chunk, 128 per sequence
+//           for a decode step)
 struct WsLayout {
     size_t proj_off, proj_ld;
     size_t scores_off, scores_ld;
+    size_t mirror_off;
     size_t total;
 };
 
-WsLayout ws_layout(const ds4c_layer_cfg &c, uint32_t rows) {
+bool tc_attention(const ds4c_layer_cfg &c) {
+    return attn_tc_supported((int)c.n_heads, (int)c.head_dim, (int)c.swa, (int)c.ratio, (int)c.top_k);
+}
+
+WsLayout ws_layout(const ds4c_layer_cfg &c, uint32_t rows, uint64_t mirror_rows) {
     WsLayout L{};
     size_t P = 0;
     if (c.ratio != 0) P = 2 * (size_t)proj_width(c, true) + (c.ratio == 4 ? 2 * (size_t)proj_width(c, false) : 0);
@@ -58,9 +66,13 @@ WsLayout ws_layout(const ds4c_layer_cfg &c, uint32_t rows) {
     L.scores_ld = (c.ratio == 4) ? align_up(c.idx_cap, 4) : 0;
     L.scores_off = o;
     o += align_up(sizeof(float) * L.scores_ld * rows, 256);
+    L.mirror_off = o;
+    if (tc_attention(c)) o += align_up((size_t)mirror_rows * 2 * c.head_dim * sizeof(uint16_t), 256);
     L.total = o < 256 ? 256 : o;
     return L;
 }
+WsLayout ws_prefill(const ds4c_layer_cfg &c, uint32_t n_tok) { return ws_layout(c, n_tok, 128 + (uint64_t)n_tok); }
+WsLayout ws_decode(const ds4c_layer_cfg &c, uint32_t n_seq) { return ws_layout(c, n_seq, 128 * (uint64_t)n_seq); }
 
 RopeTable rope_table(const ds4c_layer_cfg &c) {
     RopeTable t;
@@ -97,7 +109,7 @@ ds4c_status run_compress(const ds4c_layer_cfg *cfg, const ds4c_lane_weights *aw,
                          const ds4c_layer_state *st, const void *hidden, uint32_t rows, uint64_t pos0,
                          const DecodePos *dp, void *ws, cudaStream_t stream) {
     const ds4c_layer_cfg &c = *cfg;
-    const WsLayout L = ws_layout(c, rows);
+    const WsLayout L = (dp == nullptr) ? ws_prefill(c, rows) : ws_decode(c, rows);
     float *proj = reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + L.proj_off);
     const int Wa = proj_width(c, true), Wi = proj_width(c, false);
     GemmArgs g{};
@@ -141,6 +153,7 @@ ds4c_status run_compress(const ds4c_layer_cfg *cfg, const ds4c_lane_weights *aw,
         la.prequant = s.prequant;
         la.skv = s.state_kv;
         la.ssc = s.state_score;
+        la.split = (attn && tc_attention(c)) ? s.comp_split : nullptr;
         la.Dl = lane_width(c, attn);
         la.cap = (int)(attn ? c.comp_cap : c.idx_cap);
         la.is_attn = attn ? 1 : 0;
@@ -186,9 +199,16 @@ const char *ds4c_status_string(ds4c_status s) {
     return "unknown status";
 }
 
-size_t ds4c_workspace_bytes(const ds4c_layer_cfg *cfg, uint32_t max_rows) {
+size_t ds4c_workspace_bytes(const ds4c_layer_cfg *cfg, uint32_t max_tok, uint32_t max_seq) {
     if (check_cfg(cfg) != DS4C_OK) return 0;
-    return ws_layout(*cfg, max_rows > 0 ? max_rows : 1).total;
+    const size_t a = ws_prefill(*cfg, max_tok > 0 ? max_tok : 1).total;
+    const size_t b = max_seq > 0 ? ws_decode(*cfg, max_seq).total : 0;
+    return a > b ? a : b;
+}
+
+int ds4c_attn_uses_tensor_cores(const ds4c_layer_cfg *cfg) {
+    if (check_cfg(cfg) != DS4C_OK) return 0;
+    return tc_attention(*cfg) ? 1 : 0;
 }
 
 ds4c_status ds4c_state_init(const ds4c_layer_cfg *cfg, const ds4c_layer_state *st, uint32_t n_seq, cudaStream_t stream) {
@@ -232,8 +252,9 @@ ds4c_status ds4c_compress_prefill(const ds4c_layer_cfg *cfg, const ds4c_lane_wei
     const uint64_t end = pos0 + n_tok;
     if (end / c.ratio > c.comp_cap) return DS4C_ERR_CAPACITY;
     if (c.ratio == 4 && end / 4 > c.idx_cap) return DS4C_ERR_CAPACITY;
+    if (tc_attention(c) && !st->attn.comp_split) return DS4C_ERR_NULL;
     if (!ws) return DS4C_ERR_WORKSPACE;
-    if (ws_bytes < ws_layout(c, n_tok).total) return DS4C_ERR_WORKSPACE;
+    if (ws_bytes < ws_prefill(c, n_tok).total) return DS4C_ERR_WORKSPACE;
     return run_compress(cfg, attn, idx, st, hidden, n_tok, pos0, nullptr, ws, stream);
 }
 
@@ -265,8 +286,9 @@ ds4c_status ds4c_compress_decode_step(const ds4c_layer_cfg *cfg, const ds4c_lane
         if (c.ratio == 4 && end / 4 > c.idx_cap) return DS4C_ERR_CAPACITY;
         dp.pos[b] = pos_h[b];
     }
+    if (tc_attention(c) && !st->attn.comp_split) return DS4C_ERR_NULL;
     if (!ws) return DS4C_ERR_WORKSPACE;
-    if (ws_bytes < ws_layout(c, n_seq).total) return DS4C_ERR_WORKSPACE;
+    if (ws_bytes < ws_decode(c, n_seq).total) return DS4C_ERR_WORKSPACE;
     return run_compress(cfg, attn, idx, st, hidden, n_seq, 0, &dp, ws, stream);
 }
 
@@ -298,7 +320,7 @@ ds4c_status ds4c_indexer_topk(const ds4c_layer_cfg *cfg, const ds4c_layer_state 
     if (vis_max > c.idx_cap) return DS4C_ERR_CAPACITY;
     if (scores && score_stride < vis_max) return DS4C_ERR_CAPACITY;
     if (!ws) return DS4C_ERR_WORKSPACE;
-    const WsLayout L = ws_layout(c, rows);
+    const WsLayout L = (n_seq == 1) ? ws_prefill(c, rows) : ws_decode(c, rows);
     if (ws_bytes < L.total) return DS4C_ERR_WORKSPACE;
     IndexerArgs a{};
     a.q = q_idx;
@@ -328,7 +350,6 @@ ds4c_status ds4c_sparse_swa_attn(const ds4c_layer_cfg *cfg, const ds4c_layer_sta
     ds4c_status s = check_cfg(cfg);
     if (s != DS4C_OK) return s;
     const ds4c_layer_cfg &c = *cfg;
-    (void)ws_bytes;
     if (n_seq == 0 || n_tok == 0) return DS4C_ERR_SHAPE;
     if (n_seq > 1 && n_tok > 1) return DS4C_ERR_UNSUPPORTED;
     if (n_seq > (uint32_t)kMaxDecodeSeq) return DS4C_ERR_UNSUPPORTED;
@@ -348,27 +369,54 @@ ds4c_status ds4c_sparse_swa_attn(const ds4c_layer_cfg *cfg, const ds4c_layer_sta
             if (c.ratio != 0 && (pos_h[b] + 1) / c.ratio > c.comp_cap) return DS4C_ERR_CAPACITY;
         }
     }
-    AttnArgs a{};
-    a.q = q;
-    a.raw_new = raw_new;
-    a.ring = st->raw;
-    a.comp = st->attn.comp;
-    a.topk = topk;
-    a.out = out;
-    a.D = (int)c.head_dim;
-    a.H = (int)c.n_heads;
-    a.S = (int)c.swa;
-    a.ratio = (int)c.ratio;
-    a.k = (int)c.top_k;
-    a.comp_cap = (int)c.comp_cap;
-    a.scale = c.attn_scale;
-    a.n_seq = (int)n_seq;
-    a.n_tok = (int)n_tok;
-    a.pos0 = pos_h[0];
-    cudaError_t e = launch_attention(a, n_seq > 1 ? &dp : nullptr, stream);
+    cudaError_t e;
+    if (tc_attention(c)) {
+        if (c.ratio != 0 && !st->attn.comp_split) return DS4C_ERR_NULL;
+        const WsLayout L = (n_seq == 1) ? ws_prefill(c, n_tok) : ws_decode(c, n_seq);
+        if (!ws) return DS4C_ERR_WORKSPACE;
+        if (ws_bytes < L.total) return DS4C_ERR_WORKSPACE;
+        AttnTcArgs a{};
+        a.q = q;
+        a.raw_new = raw_new;
+        a.ring = st->raw;
+        a.comp_split = st->attn.comp_split;
+        a.raw_mirror = reinterpret_cast<uint16_t *>(reinterpret_cast<char *>(ws) + L.mirror_off);
+        a.topk = topk;
+        a.out = out;
+        a.D = (int)c.head_dim;
+        a.H = (int)c.n_heads;
+        a.ratio = (int)c.ratio;
+        a.k = (int)c.top_k;
+        a.comp_cap = (int)c.comp_cap;
+        a.scale = c.attn_scale;
+        a.n_seq = (int)n_seq;
+        a.n_tok = (int)n_tok;
+        a.n_seq_state = (int)n_seq;
+        a.pos0 = pos_h[0];
+        e = launch_attention_tc(a, n_seq > 1 ? &dp : nullptr, stream);
+    } else {
+        AttnArgs a{};
+        a.q = q;
+        a.raw_new = raw_new;
+        a.ring = st->raw;
+        a.comp = st->attn.comp;
+        a.topk = topk;
+        a.out = out;
+        a.D = (int)c.head_dim;
+        a.H = (int)c.n_heads;
+        a.S = (int)c.swa;
+        a.ratio = (int)c.ratio;
+        a.k = (int)c.top_k;
+        a.comp_cap = (int)c.comp_cap;
+        a.scale = c.attn_scale;
+        a.n_seq = (int)n_seq;
+        a.n_tok = (int)n_tok;
+        a.pos0 = pos_h[0];
+        e = launch_attention(a, n_seq > 1 ? &dp : nullptr, stream);
+    }
     if (e == cudaSuccess && commit_ring)
-        e = launch_ring_commit(st->raw, raw_new, a.D, a.S, (int)n_seq, (int)n_tok, pos_h[0], n_seq > 1 ? &dp : nullptr,
-                               stream);
+        e = launch_ring_commit(st->raw, raw_new, (int)c.head_dim, (int)c.swa, (int)n_seq, (int)n_tok, pos_h[0],
+                               n_seq > 1 ? &dp : nullptr, stream);
     return cuda_status(e);
 }
 
@@ -433,7 +481,8 @@ const char *ds4c_last_cuda_error(void) { return cudaGetErrorName(t_last_cuda_err
 ds4c_status ds4c_sync_status(cudaStream_t stream) {
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_status(e);
-    if (gemm_tc_read_clear_error() != 0) return DS4C_ERR_DEVICE;
+    const unsigned int e1 = gemm_tc_read_clear_error(), e2 = attn_tc_read_clear_error();
+    if (e1 != 0 || e2 != 0) return DS4C_ERR_DEVICE;
     return DS4C_OK;
 }
 

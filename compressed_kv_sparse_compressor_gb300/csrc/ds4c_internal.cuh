@@ -66,6 +66,7 @@ struct LaneArgs {
     float *comp;                       // [n_seq][cap][Dl]
     float *prequant;                   // same or null
     float *skv, *ssc;                  // [n_seq][coff*ratio][W]
+    uint16_t *split;                   // attention lane: [n_seq][cap][2][Dl] bf16 hi, lo (or null)
     int Dl, cap, is_attn;
 };
 struct CompressArgs {
@@ -118,6 +119,24 @@ struct AttnArgs {
     uint64_t pos0;
 };
 cudaError_t launch_attention(const AttnArgs &a, const DecodePos *p, cudaStream_t s);
+
+// Tensor-core attention (H = 64, D in {128, 256, 512}, swa = 128).
+struct AttnTcArgs {
+    const float *q;
+    const float *raw_new;
+    const float *ring;
+    const uint16_t *comp_split;   // [n_seq_state][comp_cap][2][D]
+    uint16_t *raw_mirror;         // workspace: [rows][2][D]
+    const int32_t *topk;
+    float *out;
+    int D, H, ratio, k, comp_cap;
+    float scale;
+    int n_seq, n_tok, n_seq_state;
+    uint64_t pos0;
+};
+bool attn_tc_supported(int H, int D, int S, int ratio, int k);
+cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *p, cudaStream_t s);
+unsigned int attn_tc_read_clear_error();
 cudaError_t launch_ring_commit(float *ring, const float *raw_new, int D, int S, int n_seq, int n_tok,
                                uint64_t pos0, const DecodePos *p, cudaStream_t s);
 

@@ -1,0 +1,809 @@
+// Sparse sliding-window attention on the 5th-generation tensor cores (K6),
+// "Metal グラフと圧縮 KV の実装を読む" §7: per query position t and head h one
+// softmax over the raw window rows and the compressed rows the layer selects,
+// K = V = the stored row, all heads sharing it.
+//
+// Formulation (one query token at a time, all H heads together):
+//   S^T[r][h] = sum_d X[r][d] Q[h][d]        M = 128 rows, N = H, K = D
+//   O^T[d][h] += sum_r X[r][d] P[r][h]       M = 128 d (D/128 blocks), N = H, K = rows
+//   L[.][h]   += sum_r 1 * P[r][h]           (the softmax denominator, one MMA)
+// Rows sit on TMEM lanes, heads on TMEM columns.  Accuracy: every operand is
+// split into bf16 hi + lo (x = hi + lo to 2^-17) and each product takes three
+// MMAs (hi*hi + hi*lo + lo*hi), fp32 accumulation in tensor memory; this keeps
+// the result within fp32-accumulation tolerance of the exact attention.
+//
+// Data: row tiles arrive by TMA from bf16 hi/lo mirrors: raw rows from a
+// position-ordered mirror the call builds in the workspace (one 128-row box per
+// query), compressed rows from the comp_split mirror the compressor maintains,
+// fetched with tile::gather4 by the row list (top-k on ratio-4 layers, every
+// visible row on ratio-128 layers).  A tile is streamed twice through a 3-deep
+// ring of 16 KB slot pairs: by 64-wide d-chunks for S, by 64-row halves of
+// 128-wide d-blocks for O (the same bytes form the K-major A operand of the
+// first product and the MN-major A operand of the second).
+//
+// Softmax: online with a lazy reference maximum: a tile only moves the
+// reference (and rescales O and L in tensor memory) when a logit exceeds it by
+// more than 2^8, so p <= 256 and the final O/L is exact for any reference.
+//
+// Warp roles (192 threads, persistent over query tokens):
+//   warp 0  row lists and TMA producer      warp 1  MMA issuer, TMEM owner
+//   warps 2-5  Q split, softmax, P, epilogue (thread = TMEM lane)
+// Every mbarrier wait is bounded; a wait that gives up raises the device error
+// word and the CTA winds down.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "ds4c_internal.cuh"
+
+namespace ds4c {
+
+__device__ unsigned int g_attn_tc_err;
+
+namespace {
+
+constexpr int ROWS = 128;
+constexpr int SLOT = 8192;            // [64 rows][64 d] bf16
+constexpr int PAIR = 2 * SLOT;
+constexpr int RING = 3;
+constexpr int THREADS = 192;
+constexpr int MAX_LIST = 1024;
+constexpr float TAU = 8.0f;           // log2 units
+constexpr unsigned long long WAIT_NS = 4000000000ull;
+
+template <int H, int D>
+struct L {
+    static constexpr int DC = D / 64;
+    static constexpr int DB = D / 128;
+    static constexpr int QB = DC * H * 128;            // bytes of Q hi (or lo)
+    static constexpr int PB = ROWS * H * 2;            // bytes of P hi (or lo)
+    static constexpr int OFF_QHI = 0;
+    static constexpr int OFF_QLO = OFF_QHI + QB;
+    static constexpr int OFF_X = OFF_QLO + QB;
+    static constexpr int OFF_PHI = OFF_X + RING * PAIR;
+    static constexpr int OFF_PLO = OFF_PHI + PB;
+    static constexpr int OFF_ONES = OFF_PLO + PB;
+    static constexpr int OFF_LIST = OFF_ONES + 4096;
+    static constexpr int OFF_RED = OFF_LIST + 4 * MAX_LIST;
+    static constexpr int OFF_FLAG = OFF_RED + 4 * 4 * H;
+    static constexpr int OFF_BAR = OFF_FLAG + 64;
+    static constexpr int N_BAR = 2 * RING + 9;
+    static constexpr int SMEM = OFF_BAR + 8 * N_BAR + 16 + 1024;
+    // TMEM columns
+    static constexpr int T_S = 0;                      // two S^T buffers of H columns
+    static constexpr int T_O = 2 * H;                  // DB blocks of H columns
+    static constexpr int T_L = 2 * H + DB * H;         // H columns
+    static constexpr int T_COLS = 512;
+    static_assert(T_L + H <= T_COLS, "tensor memory");
+    static_assert(SMEM <= 232448, "shared memory");
+};
+
+// barrier indices
+enum { B_FULL = 0, B_EMPTY = RING, B_QREADY = 2 * RING, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1, B_PFULL, B_PVDONE,
+       B_OFREE, B_SOFT };
+
+struct TcAttnParams {
+    float *out;
+    const float *q;
+    const int32_t *topk;
+    int n_q, n_seq, n_tok, k, ratio, comp_cap;
+    float scale_log2;
+    uint64_t pos0;
+    DecodePos dp;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((i & 255u) == 255u) {
+            if (*abort) return false;
+            const uint64_t now = globaltimer();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > WAIT_NS) {
+                *abort = 1;
+                atomicOr(&g_attn_tc_err, 1u);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int x, int r0, int r1, int r2, int r3,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+        "%4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start, leading / stride byte
+// offsets, version 1, layout (0 = no swizzle, 2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t make_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)layout << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16 with bf16 operands and f32 accumulation.
+__host__ __device__ constexpr uint32_t idesc(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(id), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+#define TMEM_LD16(taddr, r, o)                                                                                    \
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, " \
+                 "%13, %14, %15}, [%16];"                                                                        \
+                 : "=r"(r[o + 0]), "=r"(r[o + 1]), "=r"(r[o + 2]), "=r"(r[o + 3]), "=r"(r[o + 4]), "=r"(r[o + 5]),   \
+                   "=r"(r[o + 6]), "=r"(r[o + 7]), "=r"(r[o + 8]), "=r"(r[o + 9]), "=r"(r[o + 10]), "=r"(r[o + 11]), \
+                   "=r"(r[o + 12]), "=r"(r[o + 13]), "=r"(r[o + 14]), "=r"(r[o + 15])                              \
+                 : "r"(taddr))
+#define TMEM_ST16(taddr, r, o)                                                                                     \
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, " \
+                 "%13, %14, %15, %16};" ::"r"(taddr),                                                             \
+                 "r"(r[o + 0]), "r"(r[o + 1]), "r"(r[o + 2]), "r"(r[o + 3]), "r"(r[o + 4]), "r"(r[o + 5]),           \
+                 "r"(r[o + 6]), "r"(r[o + 7]), "r"(r[o + 8]), "r"(r[o + 9]), "r"(r[o + 10]), "r"(r[o + 11]),        \
+                 "r"(r[o + 12]), "r"(r[o + 13]), "r"(r[o + 14]), "r"(r[o + 15])                                   \
+                 : "memory")
+
+// Load H consecutive fp32 columns of this thread's TMEM lane.
+template <int H>
+__device__ __forceinline__ void tmem_load(uint32_t taddr, float (&v)[H]) {
+    uint32_t r[H];
+#pragma unroll
+    for (int c = 0; c < H; c += 16) TMEM_LD16(taddr + c, r, c);
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int c = 0; c < H; c++) v[c] = __uint_as_float(r[c]);
+}
+template <int H>
+__device__ __forceinline__ void tmem_store(uint32_t taddr, const float (&v)[H]) {
+    uint32_t r[H];
+#pragma unroll
+    for (int c = 0; c < H; c++) r[c] = __float_as_uint(v[c]);
+#pragma unroll
+    for (int c = 0; c < H; c += 16) TMEM_ST16(taddr + c, r, c);
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
+    hi = __bfloat162float(__float2bfloat16_rn(x));
+    lo = x - hi;
+}
+
+// Per-token geometry shared by all roles.
+struct Tok {
+    int n;             // query index
+    int seq;
+    uint64_t t;        // position
+    int raw_row0;      // raw mirror row of tile 0, row 0
+    int raw_lo, raw_hi;  // valid row range of tile 0
+    int n_comp;
+    int n_tiles;
+};
+
+__device__ __forceinline__ Tok token_geom(const TcAttnParams &p, int n) {
+    Tok k;
+    k.n = n;
+    if (p.n_seq == 1) {
+        k.seq = 0;
+        k.t = p.pos0 + (uint64_t)n;
+        k.raw_row0 = n + 1;                               // mirror row u <-> position pos0 - 128 + u
+        const int lo = (k.t >= 127) ? 0 : (int)(127 - k.t);
+        k.raw_lo = lo;
+        k.raw_hi = ROWS - 1;
+    } else {
+        k.seq = n;
+        k.t = p.dp.pos[n];
+        k.raw_row0 = n * ROWS;                            // mirror rows = the sequence's 128 ring slots
+        k.raw_lo = 0;
+        k.raw_hi = (k.t >= 127) ? ROWS - 1 : (int)k.t;    // slot s holds position s while t < 128
+    }
+    return k;
+}
+
+// Number of compressed rows a query attends (ratio 4: the top-k list read the
+// way the attention loop of [P2] §7 reads it; ratio 128: every visible row).
+// The whole warp calls this; the list (row indices into the comp mirror) is
+// written to `list` when non-null.
+__device__ __forceinline__ int comp_rows(const TcAttnParams &p, const Tok &k, int *list) {
+    const int lane = threadIdx.x & 31;
+    if (p.ratio == 128) {
+        const uint64_t v = (k.t + 1) / 128;
+        return v < (uint64_t)p.comp_cap ? (int)v : p.comp_cap;
+    }
+    if (p.ratio != 4) return 0;
+    const uint64_t visible = (k.t + 1) / 4;
+    const int32_t *tk = p.topk + (size_t)k.n * p.k;
+    int cnt = 0;
+    for (int base = 0; base < p.k; base += 32) {
+        const int i = base + lane;
+        const int32_t idx = (i < p.k) ? tk[i] : -1;
+        const bool stop = idx >= 0 && (uint64_t)idx >= visible;
+        const unsigned stop_m = __ballot_sync(0xffffffffu, stop);
+        const unsigned before = stop_m ? ((stop_m & (0u - stop_m)) - 1u) : 0xffffffffu;  // lanes before the first stop
+        const bool valid = idx >= 0 && !stop && (((before >> lane) & 1u) != 0u);
+        const unsigned vm = __ballot_sync(0xffffffffu, valid);
+        if (valid && list) list[cnt + __popc(vm & ((1u << lane) - 1u))] = k.seq * p.comp_cap + idx;
+        cnt += __popc(vm);
+        if (stop_m) break;
+    }
+    return cnt;
+}
+
+template <int H, int D>
+__global__ void __launch_bounds__(THREADS, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant__ CUtensorMap rawLo,
+               const __grid_constant__ CUtensorMap compHi, const __grid_constant__ CUtensorMap compLo,
+               const TcAttnParams p) {
+    using Lay = L<H, D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lay::OFF_BAR);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Lay::N_BAR);
+    volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *list = reinterpret_cast<int *>(sm + Lay::OFF_LIST);
+    float *red = reinterpret_cast<float *>(sm + Lay::OFF_RED);
+    volatile int *flags = reinterpret_cast<volatile int *>(sm + Lay::OFF_FLAG);
+    auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < RING; i++) {
+            mbar_init(bar(B_FULL + i), 1);
+            mbar_init(bar(B_EMPTY + i), 1);
+        }
+        mbar_init(bar(B_QREADY), 128);
+        mbar_init(bar(B_SFULL0), 1);
+        mbar_init(bar(B_SFULL1), 1);
+        mbar_init(bar(B_SFREE0), 128);
+        mbar_init(bar(B_SFREE1), 128);
+        mbar_init(bar(B_PFULL), 128);
+        mbar_init(bar(B_PVDONE), 1);
+        mbar_init(bar(B_OFREE), 128);
+        mbar_init(bar(B_SOFT), 128);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // the all-ones A operand of the denominator MMA (4 KB, layout-free)
+    for (int i = threadIdx.x; i < 4096 / 4; i += THREADS)
+        reinterpret_cast<uint32_t *>(sm + Lay::OFF_ONES)[i] = 0x3F803F80u;
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(Lay::T_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        fence_before();
+    }
+    fence_proxy_async();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        uint32_t unit = 0;
+        bool ok = true;
+        for (int n = blockIdx.x; n < p.n_q && ok; n += gridDim.x) {
+            const Tok k = token_geom(p, n);
+            __syncwarp();
+            const int nc = comp_rows(p, k, p.ratio == 4 ? list : nullptr);
+            __syncwarp();
+            const int n_tiles = 1 + (nc + ROWS - 1) / ROWS;
+            const int dummy = k.seq * p.comp_cap;
+            auto row_of = [&](int tile, int r) -> int {   // comp mirror row of tile >= 1, row r
+                const int i = (tile - 1) * ROWS + r;
+                if (i >= nc) return dummy;
+                return p.ratio == 4 ? list[i] : dummy + i;
+            };
+            // issue one 16 KB unit into the next ring pair
+            auto issue = [&](int tile, bool pv, int a, int hh, int lo) -> bool {
+                const int s = unit % RING;
+                const uint32_t ph = (unit / RING) & 1;
+                unit++;
+                if (lane == 0) {
+                    if (!mbar_wait(bar(B_EMPTY + s), ph ^ 1, abort)) return false;
+                    const uint32_t dst = smem_u32(sm + Lay::OFF_X + s * PAIR);
+                    const uint32_t fb = bar(B_FULL + s);
+                    mbar_expect_tx(fb, PAIR);
+                    if (tile == 0) {
+                        const CUtensorMap *m = lo ? &rawLo : &rawHi;
+                        if (!pv) {      // d-chunk a, rows 0..127
+                            tma_box(dst, m, 64 * a, k.raw_row0, fb);
+                            tma_box(dst + SLOT, m, 64 * a, k.raw_row0 + 64, fb);
+                        } else {        // d-block a, rows 64*hh..
+                            tma_box(dst, m, 128 * a, k.raw_row0 + 64 * hh, fb);
+                            tma_box(dst + SLOT, m, 128 * a + 64, k.raw_row0 + 64 * hh, fb);
+                        }
+                    } else {
+                        const CUtensorMap *m = lo ? &compLo : &compHi;
+                        if (!pv) {
+                            for (int g = 0; g < 32; g++)
+                                tma_gather4(dst + g * 512, m, 64 * a, row_of(tile, 4 * g), row_of(tile, 4 * g + 1),
+                                            row_of(tile, 4 * g + 2), row_of(tile, 4 * g + 3), fb);
+                        } else {
+                            for (int half = 0; half < 2; half++)
+                                for (int g = 0; g < 16; g++) {
+                                    const int r = 64 * hh + 4 * g;
+                                    tma_gather4(dst + half * SLOT + g * 512, m, 128 * a + 64 * half, row_of(tile, r),
+                                                row_of(tile, r + 1), row_of(tile, r + 2), row_of(tile, r + 3), fb);
+                                }
+                        }
+                    }
+                }
+                return true;
+            };
+            auto issue_qk = [&](int tile) -> bool {
+                for (int c = 0; c < Lay::DC; c++)
+                    for (int v = 0; v < 2; v++)
+                        if (!issue(tile, false, c, 0, v)) return false;
+                return true;
+            };
+            auto issue_pv = [&](int tile) -> bool {
+                for (int j = 0; j < Lay::DB; j++)
+                    for (int hh = 0; hh < 2; hh++)
+                        for (int v = 0; v < 2; v++)
+                            if (!issue(tile, true, j, hh, v)) return false;
+                return true;
+            };
+            bool good = issue_qk(0);
+            for (int i = 0; i < n_tiles && good; i++) {
+                if (i + 1 < n_tiles) good = issue_qk(i + 1);
+                if (good) good = issue_pv(i);
+            }
+            ok = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t ID_QK = idesc(128, H, 0, 0);
+        constexpr uint32_t ID_PV = idesc(128, H, 1, 1);
+        constexpr uint32_t ID_L = idesc(128, H, 0, 1);
+        const uint32_t qhi = smem_u32(sm + Lay::OFF_QHI), qlo = smem_u32(sm + Lay::OFF_QLO);
+        const uint32_t phi = smem_u32(sm + Lay::OFF_PHI), plo = smem_u32(sm + Lay::OFF_PLO);
+        const uint32_t ones = smem_u32(sm + Lay::OFF_ONES);
+        uint32_t unit = 0, g = 0, tok = 0;
+        bool ok = true;
+        // unit u of the ring: wait until loaded / hand back once its MMAs finish
+        auto wait_unit = [&](uint32_t u, uint32_t &base) -> bool {
+            base = smem_u32(sm + Lay::OFF_X + (u % RING) * PAIR);
+            return mbar_wait(bar(B_FULL + u % RING), (u / RING) & 1, abort);
+        };
+        auto free_unit = [&](uint32_t u) { mma_commit(bar(B_EMPTY + u % RING)); };
+        auto do_qk = [&](uint32_t gt) -> bool {
+            const int sb = gt & 1;
+            if (gt >= 2 && !mbar_wait(bar(B_SFREE0 + sb), ((gt >> 1) - 1) & 1, abort)) return false;
+            fence_after();
+            const uint32_t d_t = tmem + Lay::T_S + sb * H;
+            for (int c = 0; c < Lay::DC; c++, unit += 2) {
+                uint32_t xh, xl;
+                if (!wait_unit(unit, xh) || !wait_unit(unit + 1, xl)) return false;
+                fence_after();
+                for (int kk = 0; kk < 4; kk++) {
+                    const uint64_t ah = make_desc(xh + kk * 32, 16, 1024, 2);
+                    const uint64_t al = make_desc(xl + kk * 32, 16, 1024, 2);
+                    const uint64_t bh = make_desc(qhi + c * (H * 128) + kk * 32, 16, 1024, 2);
+                    const uint64_t bl = make_desc(qlo + c * (H * 128) + kk * 32, 16, 1024, 2);
+                    mma(d_t, ah, bh, ID_QK, (c > 0 || kk > 0) ? 1u : 0u);
+                    mma(d_t, ah, bl, ID_QK, 1u);
+                    mma(d_t, al, bh, ID_QK, 1u);
+                }
+                free_unit(unit);
+                free_unit(unit + 1);
+            }
+            mma_commit(bar(B_SFULL0 + sb));
+            return true;
+        };
+        auto do_pv = [&](int i) -> bool {
+            for (int j = 0; j < Lay::DB; j++) {
+                const uint32_t d_o = tmem + Lay::T_O + j * H;
+                for (int hh = 0; hh < 2; hh++, unit += 2) {
+                    uint32_t xh, xl;
+                    if (!wait_unit(unit, xh) || !wait_unit(unit + 1, xl)) return false;
+                    fence_after();
+                    for (int kk = 0; kk < 4; kk++) {
+                        const uint32_t koff = (uint32_t)(kk * 16 * 128);
+                        const uint32_t prow = (uint32_t)((64 * hh + 16 * kk) * 128);
+                        const uint64_t ah = make_desc(xh + koff, SLOT, 1024, 2);
+                        const uint64_t al = make_desc(xl + koff, SLOT, 1024, 2);
+                        const uint64_t bh = make_desc(phi + prow, 8192, 1024, 2);
+                        const uint64_t bl = make_desc(plo + prow, 8192, 1024, 2);
+                        const uint32_t acc = (i == 0 && hh == 0 && kk == 0) ? 0u : 1u;
+                        mma(d_o, ah, bh, ID_PV, acc);
+                        mma(d_o, ah, bl, ID_PV, 1u);
+                        mma(d_o, al, bh, ID_PV, 1u);
+                    }
+                    free_unit(unit);
+                    free_unit(unit + 1);
+                }
+            }
+            // denominator: L += ones * P (hi and lo)
+            const uint32_t d_l = tmem + Lay::T_L;
+            for (int kk = 0; kk < ROWS / 16; kk++) {
+                const uint64_t a1 = make_desc(ones, 128, 256, 0);
+                const uint64_t bh = make_desc(phi + kk * 16 * 128, 8192, 1024, 2);
+                const uint64_t bl = make_desc(plo + kk * 16 * 128, 8192, 1024, 2);
+                mma(d_l, a1, bh, ID_L, (i == 0 && kk == 0) ? 0u : 1u);
+                mma(d_l, a1, bl, ID_L, 1u);
+            }
+            mma_commit(bar(B_PVDONE));
+            return true;
+        };
+        for (int n = blockIdx.x; n < p.n_q && ok; n += gridDim.x, tok++) {
+            const Tok k = token_geom(p, n);
+            const int nc = comp_rows(p, k, nullptr);          // whole warp
+            const int n_tiles = 1 + (nc + ROWS - 1) / ROWS;
+            int good = 1;
+            if (lane == 0) {
+                good = mbar_wait(bar(B_QREADY), tok & 1, abort) ? 1 : 0;
+                if (good) {
+                    fence_after();
+                    good = do_qk(g) ? 1 : 0;
+                }
+                for (int i = 0; i < n_tiles && good; i++) {
+                    const uint32_t gi = g + i;
+                    if (i + 1 < n_tiles && !do_qk(gi + 1)) { good = 0; break; }
+                    if (!mbar_wait(bar(B_PFULL), gi & 1, abort)) { good = 0; break; }
+                    if (i == 0 && tok > 0 && !mbar_wait(bar(B_OFREE), (tok - 1) & 1, abort)) { good = 0; break; }
+                    fence_after();
+                    if (!do_pv(i)) { good = 0; break; }
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+            g += n_tiles;
+        }
+        // drain: every MMA issued so far has completed before the TMEM is freed
+        if (lane == 0 && g > 0) mbar_wait(bar(B_PVDONE), (g - 1) & 1, abort);
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax / epilogue
+        const int q4 = warp & 3;                 // TMEM lane quarter
+        const int r = q4 * 32 + lane;            // tile row / d within a block
+        const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+        const uint32_t qhi = smem_u32(sm + Lay::OFF_QHI), qlo = smem_u32(sm + Lay::OFF_QLO);
+        uint8_t *phi_p = sm + Lay::OFF_PHI;
+        uint8_t *plo_p = sm + Lay::OFF_PLO;
+        const int tid = threadIdx.x - 64;        // 0..127
+        (void)qhi;
+        (void)qlo;
+        auto load_q = [&](int n) {
+            const float4 *qs = reinterpret_cast<const float4 *>(p.q + (size_t)n * H * D);
+            for (int f = tid; f < H * D / 4; f += 128) {
+                const float4 v = qs[f];
+                const int h = f / (D / 4);
+                const int d = (f % (D / 4)) * 4;
+                const int c = d / 64, e = d % 64;
+                const int unit16 = (e / 8) ^ (h & 7);
+                const int off = c * (H * 128) + h * 128 + unit16 * 16 + (e % 8) * 2;
+                float h0, l0, h1, l1, h2, l2, h3, l3;
+                split_bf16(v.x, h0, l0);
+                split_bf16(v.y, h1, l1);
+                split_bf16(v.z, h2, l2);
+                split_bf16(v.w, h3, l3);
+                *reinterpret_cast<uint2 *>(sm + Lay::OFF_QHI + off) = make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3));
+                *reinterpret_cast<uint2 *>(sm + Lay::OFF_QLO + off) = make_uint2(pack_bf16x2(l0, l1), pack_bf16x2(l2, l3));
+            }
+            fence_proxy_async();
+            mbar_arrive(bar(B_QREADY));
+        };
+        uint32_t g = 0, tok = 0, sphase = 0;
+        bool ok = true;
+        // barrier of the 128 softmax threads on an mbarrier, so that its wait is bounded
+        auto soft_bar = [&]() -> bool {
+            mbar_arrive(bar(B_SOFT));
+            const bool r_ = mbar_wait(bar(B_SOFT), sphase, abort);
+            sphase ^= 1;
+            return r_;
+        };
+        int n = blockIdx.x;
+        if (n < p.n_q) load_q(n);
+        for (; n < p.n_q && ok; n += gridDim.x, tok++) {
+            const Tok k = token_geom(p, n);
+            const int nc = comp_rows(p, k, nullptr);
+            const int n_tiles = 1 + (nc + ROWS - 1) / ROWS;
+            float mref[H];
+#pragma unroll
+            for (int h = 0; h < H; h++) mref[h] = -INFINITY;
+            for (int i = 0; i < n_tiles; i++, g++) {
+                const int sb = g & 1;
+                if (!mbar_wait(bar(B_SFULL0 + sb), (g >> 1) & 1, abort)) { ok = false; break; }
+                fence_after();
+                float s[H];
+                tmem_load<H>(lane_base + Lay::T_S + sb * H, s);
+                fence_before();
+                mbar_arrive(bar(B_SFREE0 + sb));
+                const bool valid = (i == 0) ? (r >= k.raw_lo && r <= k.raw_hi) : ((i - 1) * ROWS + r < nc);
+                bool need = false;
+#pragma unroll
+                for (int h = 0; h < H; h++) {
+                    s[h] = valid ? s[h] * p.scale_log2 : -INFINITY;
+                    need |= s[h] > mref[h] + TAU;
+                }
+                // block-wide vote among the 128 softmax threads
+                const unsigned bal = __ballot_sync(0xffffffffu, need);
+                if (lane == 0) flags[(g & 1) * 4 + q4] = bal ? 1 : 0;
+                if (!soft_bar()) { ok = false; break; }
+                const bool any = flags[(g & 1) * 4 + 0] | flags[(g & 1) * 4 + 1] | flags[(g & 1) * 4 + 2] |
+                                 flags[(g & 1) * 4 + 3];
+                bool waited = false;
+                if (any) {
+                    // exact tile maximum per head
+                    float mx[H];
+#pragma unroll
+                    for (int h = 0; h < H; h++) {
+                        float v = s[h];
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+                        mx[h] = v;
+                    }
+                    if (lane == 0)
+                        for (int h = 0; h < H; h++) red[q4 * H + h] = mx[h];
+                    if (!soft_bar()) { ok = false; break; }
+                    float alpha[H];
+#pragma unroll
+                    for (int h = 0; h < H; h++) {
+                        const float mt = fmaxf(fmaxf(red[h], red[H + h]), fmaxf(red[2 * H + h], red[3 * H + h]));
+                        const float mn = fmaxf(mref[h], mt);
+                        alpha[h] = exp2f(mref[h] - mn);
+                        mref[h] = mn;
+                    }
+                    if (!soft_bar()) { ok = false; break; }   // red[] reusable
+                    if (i > 0) {
+                        if (!mbar_wait(bar(B_PVDONE), (g - 1) & 1, abort)) { ok = false; break; }
+                        waited = true;
+                        fence_after();
+                        float v[H];
+                        for (int j = 0; j < Lay::DB; j++) {
+                            tmem_load<H>(lane_base + Lay::T_O + j * H, v);
+#pragma unroll
+                            for (int h = 0; h < H; h++) v[h] *= alpha[h];
+                            tmem_store<H>(lane_base + Lay::T_O + j * H, v);
+                        }
+                        tmem_load<H>(lane_base + Lay::T_L, v);
+#pragma unroll
+                        for (int h = 0; h < H; h++) v[h] *= alpha[h];
+                        tmem_store<H>(lane_base + Lay::T_L, v);
+                        fence_before();
+                    }
+                }
+                if (i > 0 && !waited) {
+                    if (!mbar_wait(bar(B_PVDONE), (g - 1) & 1, abort)) { ok = false; break; }
+                }
+                // P^T row r (MN-major, 128-byte swizzle), hi and lo
+#pragma unroll
+                for (int u = 0; u < H / 8; u++) {
+                    float hv[8], lv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; e++) {
+                        const float pv = exp2f(s[u * 8 + e] - mref[u * 8 + e]);
+                        split_bf16(pv, hv[e], lv[e]);
+                    }
+                    const int off = r * (H * 2) + ((u ^ (r & 7)) * 16);
+                    *reinterpret_cast<uint4 *>(phi_p + off) = make_uint4(pack_bf16x2(hv[0], hv[1]), pack_bf16x2(hv[2], hv[3]),
+                                                                         pack_bf16x2(hv[4], hv[5]), pack_bf16x2(hv[6], hv[7]));
+                    *reinterpret_cast<uint4 *>(plo_p + off) = make_uint4(pack_bf16x2(lv[0], lv[1]), pack_bf16x2(lv[2], lv[3]),
+                                                                         pack_bf16x2(lv[4], lv[5]), pack_bf16x2(lv[6], lv[7]));
+                }
+                fence_proxy_async();
+                mbar_arrive(bar(B_PFULL));
+                if (i == n_tiles - 1) {
+                    // the last S of this token has been read: Q is free for the next token
+                    const int nn = n + gridDim.x;
+                    if (nn < p.n_q) load_q(nn);
+                    if (!mbar_wait(bar(B_PVDONE), g & 1, abort)) { ok = false; break; }
+                    fence_after();
+                    float l[H], v[H];
+                    tmem_load<H>(lane_base + Lay::T_L, l);
+                    float *o = p.out + (size_t)n * H * D;
+                    for (int j = 0; j < Lay::DB; j++) {
+                        tmem_load<H>(lane_base + Lay::T_O + j * H, v);
+#pragma unroll
+                        for (int h = 0; h < H; h++) o[(size_t)h * D + 128 * j + r] = v[h] / l[h];
+                    }
+                    fence_before();
+                    mbar_arrive(bar(B_OFREE));
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(Lay::T_COLS) : "memory");
+    }
+}
+
+// Raw mirror: bf16 hi/lo of the raw rows in the order the kernel reads them.
+// Prefill: row u <-> position pos0 - 128 + u (zeros before position 0), rows
+// 0 .. 127 from the ring, the rest from raw_new.  Decode: sequence b owns rows
+// 128b .. 128b+127 = its ring slots, with slot pos_b % 128 replaced by raw_new[b].
+__global__ void raw_split_kernel(uint16_t *__restrict__ mirror, const float *__restrict__ ring,
+                                 const float *__restrict__ raw_new, int D, int n_seq, int n_tok, uint64_t pos0,
+                                 DecodePos dp) {
+    const int u = blockIdx.x;
+    const float *src = nullptr;
+    if (n_seq == 1) {
+        const int64_t pos = (int64_t)pos0 - ROWS + u;
+        if (pos >= 0) src = (pos < (int64_t)pos0) ? ring + (size_t)(pos % ROWS) * D : raw_new + (size_t)(pos - (int64_t)pos0) * D;
+    } else {
+        const int b = u / ROWS, slot = u % ROWS;
+        const uint64_t pos = dp.pos[b];
+        src = ((uint64_t)slot == pos % ROWS) ? raw_new + (size_t)b * D : ring + ((size_t)b * ROWS + slot) * D;
+        if (pos < ROWS && (uint64_t)slot > pos) src = nullptr;      // slot not written yet
+    }
+    uint16_t *hi = mirror + (size_t)u * 2 * D;
+    uint16_t *lo = hi + D;
+    for (int j = threadIdx.x * 4; j < D; j += blockDim.x * 4) {
+        float4 v = src ? *reinterpret_cast<const float4 *>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float a[4] = {v.x, v.y, v.z, v.w}, h[4], l[4];
+        for (int e = 0; e < 4; e++) split_bf16(a[e], h[e], l[e]);
+        *reinterpret_cast<uint2 *>(hi + j) = make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
+        *reinterpret_cast<uint2 *>(lo + j) = make_uint2(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]));
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 2-D bf16 map over `rows` rows of D elements with row pitch `pitch` bytes.
+bool make_map(CUtensorMap *m, const void *base, uint64_t rows, int D, uint64_t pitch, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)pitch};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+template <int H, int D>
+cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, cudaStream_t s) {
+    using Lay = L<H, D>;
+    const uint64_t raw_rows = (a.n_seq == 1) ? (uint64_t)(ROWS + a.n_tok) : (uint64_t)a.n_seq * ROWS;
+    const uint64_t comp_rows_total = (uint64_t)a.n_seq_state * a.comp_cap;
+    CUtensorMap rh, rl, ch, cl;
+    const uint64_t pitch = (uint64_t)2 * D * 2;
+    if (!make_map(&rh, a.raw_mirror, raw_rows, D, pitch, 64) || !make_map(&rl, a.raw_mirror + D, raw_rows, D, pitch, 64))
+        return cudaErrorNotSupported;
+    if (a.comp_split && comp_rows_total > 0) {
+        if (!make_map(&ch, a.comp_split, comp_rows_total, D, pitch, 1) ||
+            !make_map(&cl, a.comp_split + D, comp_rows_total, D, pitch, 1))
+            return cudaErrorNotSupported;
+    } else {
+        ch = rh;
+        cl = rl;
+    }
+    cudaError_t e = ensure_dyn_smem(attn_tc_kernel<H, D>, Lay::SMEM);
+    if (e != cudaSuccess) return e;
+    const int nq = a.n_seq * a.n_tok;
+    const int grid = nq < sm_count() ? nq : sm_count();
+    attn_tc_kernel<H, D><<<grid, THREADS, Lay::SMEM, s>>>(rh, rl, ch, cl, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attn_tc_supported(int H, int D, int S, int ratio, int k) {
+    const bool hd = H == 64 && (D == 512 || D == 256 || D == 128);
+    return hd && S == ROWS && (ratio == 0 || ratio == 4 || ratio == 128) && (ratio != 4 || k <= MAX_LIST);
+}
+
+cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *dp, cudaStream_t s) {
+    const int nq = a.n_seq * a.n_tok;
+    if (nq <= 0) return cudaSuccess;
+    // raw mirror
+    DecodePos dd{};
+    if (a.n_seq > 1) dd = *dp;
+    const int raw_rows = (a.n_seq == 1) ? ROWS + a.n_tok : a.n_seq * ROWS;
+    raw_split_kernel<<<raw_rows, 128, 0, s>>>(a.raw_mirror, a.ring, a.raw_new, a.D, a.n_seq, a.n_tok, a.pos0, dd);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    TcAttnParams p{};
+    p.out = a.out;
+    p.q = a.q;
+    p.topk = a.topk;
+    p.n_q = nq;
+    p.n_seq = a.n_seq;
+    p.n_tok = a.n_tok;
+    p.k = a.k;
+    p.ratio = a.ratio;
+    p.comp_cap = a.comp_cap;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.pos0 = a.pos0;
+    p.dp = dd;
+#define DS4C_HD(h, d) \
+    if (a.H == h && a.D == d) return launch_hd<h, d>(a, p, s);
+    DS4C_HD(64, 512)
+    DS4C_HD(64, 256)
+    DS4C_HD(64, 128)
+#undef DS4C_HD
+    return cudaErrorNotSupported;
+}
+
+unsigned int attn_tc_read_clear_error() {
+    unsigned int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_attn_tc_err, sizeof v) != cudaSuccess) return 0;
+    if (v) cudaMemcpyToSymbol(g_attn_tc_err, &z, sizeof z);
+    return v;
+}
+
+}  // namespace ds4c

@@ -14,6 +14,7 @@
 // Thread layout: a group of G = Dl/4 threads owns one compressed row, each
 // thread a float4 column slice; a 128-thread block holds 128/G rows (ratio 4)
 // or one row with 4 row-splits of the 128-token window (ratio 128).
+#include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
 #include "ds4c_internal.cuh"
@@ -120,7 +121,24 @@ __device__ __forceinline__ void finish_row(const CompressArgs &a, const LaneArgs
             y.w = ldexpf(e4m3_roundtrip(ldexpf(y.w, -e)), e);
         }
     }
-    if (active) st4(L.comp + off, y);
+    if (active) {
+        st4(L.comp + off, y);
+        if (L.split) {
+            // bf16 hi / lo mirror of the appended row for the tensor-core attention
+            const __nv_bfloat162 h01 = __floats2bfloat162_rn(y.x, y.y), h23 = __floats2bfloat162_rn(y.z, y.w);
+            const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+            const __nv_bfloat162 l01 = __floats2bfloat162_rn(y.x - f01.x, y.y - f01.y);
+            const __nv_bfloat162 l23 = __floats2bfloat162_rn(y.z - f23.x, y.w - f23.y);
+            uint16_t *row = L.split + ((size_t)seq * L.cap + (size_t)c) * 2 * Dl;
+            uint2 hv, lv;
+            hv.x = *reinterpret_cast<const uint32_t *>(&h01);
+            hv.y = *reinterpret_cast<const uint32_t *>(&h23);
+            lv.x = *reinterpret_cast<const uint32_t *>(&l01);
+            lv.y = *reinterpret_cast<const uint32_t *>(&l23);
+            *reinterpret_cast<uint2 *>(row + j) = hv;
+            *reinterpret_cast<uint2 *>(row + Dl + j) = lv;
+        }
+    }
 }
 
 // Ratio 4: window c pools, per column j, rows 0..3 (previous window, columns

@@ -38,7 +38,7 @@ class DeviceLayer:
             attn_scale=shape.attn_scale, rope_base=shape.rope_base)
         f32 = dict(dtype=torch.float32, device=device)
         self.raw = torch.zeros(n_seq, shape.swa, D, **f32)
-        self.attn_comp = self.attn_kv = self.attn_score = self.attn_pre = None
+        self.attn_comp = self.attn_kv = self.attn_score = self.attn_pre = self.attn_split = None
         self.idx_comp = self.idx_kv = self.idx_score = None
         if r:
             self.attn_comp = torch.zeros(n_seq, self.comp_cap, D, **f32)
@@ -46,15 +46,19 @@ class DeviceLayer:
             self.attn_score = torch.zeros(n_seq, coff * r, coff * D, **f32)
             if with_prequant:
                 self.attn_pre = torch.zeros(n_seq, self.comp_cap, D, **f32)
+            if abi.ds4c_attn_uses_tensor_cores(self.cfg):
+                # bf16 hi / lo mirror of the compressed rows, read by the tensor-core attention
+                self.attn_split = torch.zeros(n_seq, self.comp_cap, 2, D, dtype=torch.int16, device=device)
         if r == 4:
             self.idx_comp = torch.zeros(n_seq, self.idx_cap, d, **f32)
             self.idx_kv = torch.zeros(n_seq, 8, 2 * d, **f32)
             self.idx_score = torch.zeros(n_seq, 8, 2 * d, **f32)
         self.state = abi.LayerState(
             raw=_ptr(self.raw),
-            attn=abi.LaneState(_ptr(self.attn_comp), _ptr(self.attn_kv), _ptr(self.attn_score), _ptr(self.attn_pre)),
-            idx=abi.LaneState(_ptr(self.idx_comp), _ptr(self.idx_kv), _ptr(self.idx_score), None))
-        self.ws_bytes = abi.ds4c_workspace_bytes(self.cfg, max(max_rows, n_seq))
+            attn=abi.LaneState(_ptr(self.attn_comp), _ptr(self.attn_kv), _ptr(self.attn_score), _ptr(self.attn_pre),
+                               _ptr(self.attn_split)),
+            idx=abi.LaneState(_ptr(self.idx_comp), _ptr(self.idx_kv), _ptr(self.idx_score), None, None))
+        self.ws_bytes = abi.ds4c_workspace_bytes(self.cfg, max_rows, n_seq if n_seq > 1 else 0)
         if self.ws_bytes == 0:
             raise abi.Ds4cError(abi.DS4C_ERR_SHAPE, "ds4c_workspace_bytes")
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
@@ -119,5 +123,6 @@ class DeviceLayer:
             return None if t is None else t[b].data_ptr()
         return abi.LayerState(
             raw=off(self.raw),
-            attn=abi.LaneState(off(self.attn_comp), off(self.attn_kv), off(self.attn_score), off(self.attn_pre)),
-            idx=abi.LaneState(off(self.idx_comp), off(self.idx_kv), off(self.idx_score), None))
+            attn=abi.LaneState(off(self.attn_comp), off(self.attn_kv), off(self.attn_score), off(self.attn_pre),
+                               off(self.attn_split)),
+            idx=abi.LaneState(off(self.idx_comp), off(self.idx_kv), off(self.idx_score), None, None))

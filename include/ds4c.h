@@ -103,12 +103,19 @@ typedef struct {
  *                window, rows 4..7 current window, [P2] §5);
  *   state_score: same shape, scores with the APE already added;
  *   prequant:    optional [n_seq][cap][Dl]: each compressed row as it was before the
- *                FP8 round trip (inspection output), NULL = not written. */
+ *                FP8 round trip (inspection output), NULL = not written;
+ *   comp_split:  attention lane only: [n_seq][cap][2][Dl] bfloat16 (uint16 bits),
+ *                hi = bf16(row) and lo = bf16(row - hi) of every appended row, written
+ *                by the compress calls next to comp and read by the tensor-core
+ *                attention (derived data: not part of the checkpoint).  Required when
+ *                ds4c_attn_uses_tensor_cores(cfg) is 1, ignored (may be NULL)
+ *                otherwise and on the indexer lane. */
 typedef struct {
     float *comp;
     float *state_kv;
     float *state_score;
     float *prequant;
+    uint16_t *comp_split;
 } ds4c_lane_state;
 
 /* A layer's state: raw: [n_seq][swa][head_dim] ring, slot p % swa holds the raw
@@ -120,10 +127,16 @@ typedef struct {
     ds4c_lane_state idx;
 } ds4c_layer_state;
 
-/* Bytes of workspace a call on `cfg` needs when it processes at most
- * `max_rows` rows (n_tok of a prefill chunk, or n_seq of a decode step).
- * Returns 0 for an invalid cfg. */
-DS4C_API size_t ds4c_workspace_bytes(const ds4c_layer_cfg *cfg, uint32_t max_rows);
+/* 1 when ds4c_sparse_swa_attn runs on the tensor cores for this shape
+ * (ratio 0/4/128 with n_heads in {16, 32, 64}, head_dim in {128, 256, 512},
+ * swa == 128), 0 when it runs on the CUDA cores.  On the tensor-core path the
+ * attention lane's comp_split mirror must be allocated. */
+DS4C_API int ds4c_attn_uses_tensor_cores(const ds4c_layer_cfg *cfg);
+
+/* Bytes of workspace that serves every call on `cfg` with prefill chunks of
+ * at most max_tok tokens and decode steps of at most max_seq sequences (0: no
+ * decode steps).  Returns 0 for an invalid cfg. */
+DS4C_API size_t ds4c_workspace_bytes(const ds4c_layer_cfg *cfg, uint32_t max_tok, uint32_t max_seq);
 
 /* Fresh state for n_seq sequences: frontier kv = 0 and score = -inf (so rows
  * no token wrote carry no pooling weight), raw ring zeroed.  Compressed rows

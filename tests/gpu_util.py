@@ -104,6 +104,19 @@ def check_compress(before: orc.State, after_gpu: orc.State, wa, wi, hidden: torc
     return ref
 
 
+def check_split_mirror(dl, upto_rows=None):
+    """The attention lane's bf16 mirror is the hi / lo split of the compressed rows, bit for bit."""
+    if dl.attn_split is None:
+        return
+    torch.cuda.synchronize()
+    comp = dl.attn_comp if upto_rows is None else dl.attn_comp[:, :upto_rows]
+    split = dl.attn_split if upto_rows is None else dl.attn_split[:, :upto_rows]
+    hi = comp.to(torch.bfloat16)
+    lo = (comp - hi.float()).to(torch.bfloat16)
+    assert torch.equal(split[:, :, 0], hi.view(torch.int16)), "mirror hi"
+    assert torch.equal(split[:, :, 1], lo.view(torch.int16)), "mirror lo"
+
+
 def ring_for(st: orc.State, raw_new: np.ndarray, pos0: int, t: int) -> orc.State:
     """State whose ring holds, at slot p % S, the raw row of every position
     p in [t-S+1, t-1], taking p >= pos0 from raw_new (test-side marshalling)."""

@@ -54,6 +54,9 @@ def test_checkpoint_floats_matches_oracle(L, orc):
 def test_invalid_configs_are_rejected(L):
     base = configs.C1.layer
     assert abi.ds4c_workspace_bytes(_cfg(base), 64) > 0
+    big = _cfg(configs.C5.layer, 32768, 32768)
+    assert abi.ds4c_attn_uses_tensor_cores(big) == 1 and abi.ds4c_attn_uses_tensor_cores(_cfg(base)) == 0
+    assert abi.ds4c_workspace_bytes(big, 4096, 32) >= abi.ds4c_workspace_bytes(big, 4096)
     for bad in (dict(ratio=3), dict(head_dim=96), dict(n_heads=12), dict(n_rot=6), dict(d_model=100),
                 dict(idx_head_dim=48), dict(swa=0), dict(top_k=0)):
         shape = configs.LayerShape(**{**base.__dict__, **bad})
@@ -64,7 +67,7 @@ FAKE = 1 << 20          # an aligned non-NULL address that is never dereferenced
 
 
 def _state():
-    lane = abi.LaneState(FAKE, FAKE, FAKE, None)
+    lane = abi.LaneState(FAKE, FAKE, FAKE, None, FAKE)
     return abi.LayerState(FAKE, lane, lane)
 
 

@@ -12,8 +12,8 @@ import torch
 
 import oracle as orc
 from compressed_kv_sparse_compressor_gb300 import configs
-from gpu_util import (check_attention_sampled, check_compress, check_indexer_sampled, device_layer, download,
-                      require_gpu)
+from gpu_util import (check_attention_sampled, check_compress, check_indexer_sampled, check_split_mirror,
+                      device_layer, download, require_gpu)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -47,6 +47,7 @@ def _checked_chunk(dl, wa, wi, shape, seed, p0, n, sample, layer=0):
     after = download(dl)
     if shape.ratio:
         check_compress(before, after, wa, wi, h.cpu(), p0)
+        check_split_mirror(dl)
     tk = None
     if shape.ratio == 4:
         vis = (p0 + n) // 4

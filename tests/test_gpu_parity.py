@@ -14,8 +14,8 @@ import torch
 
 import oracle as orc
 from compressed_kv_sparse_compressor_gb300 import configs
-from gpu_util import (ATOL, RTOL, check_attention_sampled, check_compress, check_indexer_sampled, device_layer,
-                      download, require_gpu)
+from gpu_util import (ATOL, RTOL, check_attention_sampled, check_compress, check_indexer_sampled,
+                      check_split_mirror, device_layer, download, require_gpu)
 from helpers import lane_np, np_in, orc_layer
 
 pytestmark = pytest.mark.gpu
@@ -37,6 +37,7 @@ def _run_chunk(dl, wa, wi, shape, seed, pos0, T, report, sample=None, check=True
     after = download(dl) if check else None
     if check and shape.ratio:
         check_compress(before, after, wa, wi, h.cpu(), pos0, report)
+        check_split_mirror(dl)
     topk = None
     n = np.arange(T) if sample is None else np.asarray(sample)
     if shape.ratio == 4:
@@ -118,9 +119,10 @@ def test_c1_chain_against_oracle_end_to_end():
 # Multi-tile shapes with ragged tails (D=512, d=128, 64 heads)
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("ratio", [0, 4, 128])
-def test_ragged_chunks(ratio):
-    shape = configs.LayerShape(d_model=512, head_dim=512, n_rot=64, idx_head_dim=128, n_heads=64, ratio=ratio,
+@pytest.mark.parametrize("ratio,heads", [(0, 64), (4, 64), (128, 64), (4, 32)])
+def test_ragged_chunks(ratio, heads):
+    """heads = 64: tensor-core attention; heads = 32: CUDA-core attention."""
+    shape = configs.LayerShape(d_model=512, head_dim=512, n_rot=64, idx_head_dim=128, n_heads=heads, ratio=ratio,
                                top_k=16, dtype="bf16", w_std=0.04)
     seed = 21
     T_total = 300 if ratio != 128 else 700
