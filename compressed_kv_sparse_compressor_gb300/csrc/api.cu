@@ -45,10 +45,14 @@ int proj_width(const ds4c_layer_cfg &c, bool attn) { return coff_of(c) * lane_wi
 //   mirror: [mirror_rows][2][head_dim] bf16 raw rows for the tensor-core
 //           attention (128 + n_tok rows for a prefill chunk, 128 per sequence
 //           for a decode step)
+//   parts:  decode steps on the tensor-core attention split each query's rows
+//           over `parts` work items: [n_seq*parts][H][D] + [n_seq*parts][2][H] float
 struct WsLayout {
     size_t proj_off, proj_ld;
     size_t scores_off, scores_ld;
     size_t mirror_off;
+    size_t part_o_off, part_ml_off;
+    int parts;
     size_t total;
 };
 
@@ -56,7 +60,7 @@ bool tc_attention(const ds4c_layer_cfg &c) {
     return attn_tc_supported((int)c.n_heads, (int)c.head_dim, (int)c.swa, (int)c.ratio, (int)c.top_k);
 }
 
-WsLayout ws_layout(const ds4c_layer_cfg &c, uint32_t rows, uint64_t mirror_rows) {
+WsLayout ws_layout(const ds4c_layer_cfg &c, uint32_t rows, uint64_t mirror_rows, bool decode) {
     WsLayout L{};
     size_t P = 0;
     if (c.ratio != 0) P = 2 * (size_t)proj_width(c, true) + (c.ratio == 4 ? 2 * (size_t)proj_width(c, false) : 0);
@@ -67,12 +71,23 @@ WsLayout ws_layout(const ds4c_layer_cfg &c, uint32_t rows, uint64_t mirror_rows)
     L.scores_off = o;
     o += align_up(sizeof(float) * L.scores_ld * rows, 256);
     L.mirror_off = o;
-    if (tc_attention(c)) o += align_up((size_t)mirror_rows * 2 * c.head_dim * sizeof(uint16_t), 256);
+    L.parts = 1;
+    if (tc_attention(c)) {
+        o += align_up((size_t)mirror_rows * 2 * c.head_dim * sizeof(uint16_t), 256);
+        if (decode) {
+            L.parts = attn_tc_decode_parts((int)c.ratio, (int)c.top_k, (int)c.comp_cap);
+            const size_t items = (size_t)rows * L.parts;
+            L.part_o_off = o;
+            o += align_up(items * c.n_heads * c.head_dim * sizeof(float), 256);
+            L.part_ml_off = o;
+            o += align_up(items * 2 * c.n_heads * sizeof(float), 256);
+        }
+    }
     L.total = o < 256 ? 256 : o;
     return L;
 }
-WsLayout ws_prefill(const ds4c_layer_cfg &c, uint32_t n_tok) { return ws_layout(c, n_tok, 128 + (uint64_t)n_tok); }
-WsLayout ws_decode(const ds4c_layer_cfg &c, uint32_t n_seq) { return ws_layout(c, n_seq, 128 * (uint64_t)n_seq); }
+WsLayout ws_prefill(const ds4c_layer_cfg &c, uint32_t n_tok) { return ws_layout(c, n_tok, 128 + (uint64_t)n_tok, false); }
+WsLayout ws_decode(const ds4c_layer_cfg &c, uint32_t n_seq) { return ws_layout(c, n_seq, 128 * (uint64_t)n_seq, true); }
 
 RopeTable rope_table(const ds4c_layer_cfg &c) {
     RopeTable t;
@@ -388,11 +403,15 @@ ds4c_status ds4c_sparse_swa_attn(const ds4c_layer_cfg *cfg, const ds4c_layer_sta
         a.ratio = (int)c.ratio;
         a.k = (int)c.top_k;
         a.comp_cap = (int)c.comp_cap;
+        a.n_rot = (int)c.n_rot;
         a.scale = c.attn_scale;
         a.n_seq = (int)n_seq;
         a.n_tok = (int)n_tok;
         a.n_seq_state = (int)n_seq;
         a.pos0 = pos_h[0];
+        a.parts = (n_seq > 1) ? L.parts : 1;
+        a.part_o = reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + L.part_o_off);
+        a.part_ml = reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + L.part_ml_off);
         e = launch_attention_tc(a, n_seq > 1 ? &dp : nullptr, stream);
     } else {
         AttnArgs a{};

@@ -129,11 +129,16 @@ struct AttnTcArgs {
     uint16_t *raw_mirror;         // workspace: [rows][2][D]
     const int32_t *topk;
     float *out;
-    int D, H, ratio, k, comp_cap;
+    int D, H, ratio, k, comp_cap, n_rot;
     float scale;
     int n_seq, n_tok, n_seq_state;
     uint64_t pos0;
+    int parts;                    // work items per query; > 1 splits the rows (decode)
+    float *part_o, *part_ml;      // workspace for the partial outputs when parts > 1
 };
+// Work items per decode query: one per 128-row tile (the raw window plus the
+// compressed rows a query can see), at most 8.
+int attn_tc_decode_parts(int ratio, int k, int comp_cap);
 bool attn_tc_supported(int H, int D, int S, int ratio, int k);
 cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *p, cudaStream_t s);
 unsigned int attn_tc_read_clear_error();

@@ -12,14 +12,18 @@
 // MMAs (hi*hi + hi*lo + lo*hi), fp32 accumulation in tensor memory; this keeps
 // the result within fp32-accumulation tolerance of the exact attention.
 //
-// Data: row tiles arrive by TMA from bf16 hi/lo mirrors: raw rows from a
+// Data: row tiles arrive from bf16 hi/lo mirrors: raw rows by TMA from a
 // position-ordered mirror the call builds in the workspace (one 128-row box per
 // query), compressed rows from the comp_split mirror the compressor maintains,
-// fetched with tile::gather4 by the row list (top-k on ratio-4 layers, every
-// visible row on ratio-128 layers).  A tile is streamed twice through a 3-deep
+// gathered by the row list (top-k on ratio-4 layers, every visible row on
+// ratio-128 layers) with 16-byte cp.async by the whole producer warp into the
+// same 128-byte-swizzled layout.  A tile is streamed twice through a 3-deep
 // ring of 16 KB slot pairs: by 64-wide d-chunks for S, by 64-row halves of
 // 128-wide d-blocks for O (the same bytes form the K-major A operand of the
-// first product and the MN-major A operand of the second).
+// first product and the MN-major A operand of the second).  Compressed rows
+// went through the E4M3 round trip on their first head_dim - n_rot dims, so
+// those values are exact in bf16 and their lo half is zero: the lo loads and
+// the lo MMAs of those dims are skipped.
 //
 // Softmax: online with a lazy reference maximum: a tile only moves the
 // reference (and rescales O and L in tensor memory) when a logit exceeds it by
@@ -65,7 +69,9 @@ struct L {
     static constexpr int OFF_ONES = OFF_PLO + PB;
     static constexpr int OFF_LIST = OFF_ONES + 4096;
     static constexpr int OFF_RED = OFF_LIST + 4 * MAX_LIST;
-    static constexpr int OFF_FLAG = OFF_RED + 4 * 4 * H;
+    static constexpr int OFF_MREF = OFF_RED + 4 * 4 * H;
+    static constexpr int OFF_ALPHA = OFF_MREF + 4 * H;
+    static constexpr int OFF_FLAG = OFF_ALPHA + 4 * H;
     static constexpr int OFF_BAR = OFF_FLAG + 64;
     static constexpr int N_BAR = 2 * RING + 9;
     static constexpr int SMEM = OFF_BAR + 8 * N_BAR + 16 + 1024;
@@ -86,7 +92,12 @@ struct TcAttnParams {
     float *out;
     const float *q;
     const int32_t *topk;
+    const uint16_t *comp_split;      // [rows][2][D]
     int n_q, n_seq, n_tok, k, ratio, comp_cap;
+    int nope_chunks, nope_blocks;    // 64-wide chunks / 128-wide blocks inside the FP8 dims
+    int parts;                       // work items per query (1: whole query; >1: split rows, partial outputs)
+    float *part_o;                   // [n_q * parts][H][D] unnormalised partial outputs
+    float *part_ml;                  // [n_q * parts][2][H] reference max (log2) and denominator
     float scale_log2;
     uint64_t pos0;
     DecodePos dp;
@@ -142,15 +153,6 @@ __device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap *map, in
         : "memory");
 }
 
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int x, int r0, int r1, int r2, int r3,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
-        "%4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-        : "memory");
-}
-
 // Shared-memory matrix descriptor (tcgen05): start, leading / stride byte
 // offsets, version 1, layout (0 = no swizzle, 2 = 128-byte swizzle).
 __device__ __forceinline__ uint64_t make_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
@@ -183,6 +185,13 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// the barrier counts one arrival when this thread's earlier cp.async copies land
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 
 #define TMEM_LD16(taddr, r, o)                                                                                    \
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, " \
@@ -288,10 +297,22 @@ __device__ __forceinline__ int comp_rows(const TcAttnParams &p, const Tok &k, in
     return cnt;
 }
 
+// Work item `it` = (query it / parts, part it % parts); the part covers tiles
+// [tb, te) of its query (empty when tb >= te).
+struct Item { int n, tb, te; };
+__device__ __forceinline__ Item item_tiles(const TcAttnParams &p, int it, int n_tiles) {
+    Item r;
+    r.n = it / p.parts;
+    const int part = it % p.parts;
+    const int w = (n_tiles + p.parts - 1) / p.parts;
+    r.tb = part * w;
+    r.te = min(r.tb + w, n_tiles);
+    return r;
+}
+
 template <int H, int D>
 __global__ void __launch_bounds__(THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant__ CUtensorMap rawLo,
-               const __grid_constant__ CUtensorMap compHi, const __grid_constant__ CUtensorMap compLo,
                const TcAttnParams p) {
     using Lay = L<H, D>;
     extern __shared__ uint8_t smem_raw[];
@@ -301,13 +322,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *list = reinterpret_cast<int *>(sm + Lay::OFF_LIST);
     float *red = reinterpret_cast<float *>(sm + Lay::OFF_RED);
+    float *mref_s = reinterpret_cast<float *>(sm + Lay::OFF_MREF);
+    float *alpha_s = reinterpret_cast<float *>(sm + Lay::OFF_ALPHA);
     volatile int *flags = reinterpret_cast<volatile int *>(sm + Lay::OFF_FLAG);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
         for (int i = 0; i < RING; i++) {
-            mbar_init(bar(B_FULL + i), 1);
+            mbar_init(bar(B_FULL + i), 32);        // one arrival per producer lane
             mbar_init(bar(B_EMPTY + i), 1);
         }
         mbar_init(bar(B_QREADY), 128);
@@ -341,74 +364,95 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         // ------------------------------------------------------------ producer
         uint32_t unit = 0;
         bool ok = true;
-        for (int n = blockIdx.x; n < p.n_q && ok; n += gridDim.x) {
-            const Tok k = token_geom(p, n);
+        const int n_items = p.n_q * p.parts;
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+            const Tok k = token_geom(p, it / p.parts);
             __syncwarp();
             const int nc = comp_rows(p, k, p.ratio == 4 ? list : nullptr);
             __syncwarp();
-            const int n_tiles = 1 + (nc + ROWS - 1) / ROWS;
+            const Item itm = item_tiles(p, it, 1 + (nc + ROWS - 1) / ROWS);
+            if (itm.tb >= itm.te) continue;
             const int dummy = k.seq * p.comp_cap;
             auto row_of = [&](int tile, int r) -> int {   // comp mirror row of tile >= 1, row r
                 const int i = (tile - 1) * ROWS + r;
                 if (i >= nc) return dummy;
                 return p.ratio == 4 ? list[i] : dummy + i;
             };
-            // issue one 16 KB unit into the next ring pair
+            // one 16 KB unit into the next ring pair; every lane takes part
             auto issue = [&](int tile, bool pv, int a, int hh, int lo) -> bool {
-                const int s = unit % RING;
+                const int s_ = unit % RING;
                 const uint32_t ph = (unit / RING) & 1;
                 unit++;
-                if (lane == 0) {
-                    if (!mbar_wait(bar(B_EMPTY + s), ph ^ 1, abort)) return false;
-                    const uint32_t dst = smem_u32(sm + Lay::OFF_X + s * PAIR);
-                    const uint32_t fb = bar(B_FULL + s);
-                    mbar_expect_tx(fb, PAIR);
-                    if (tile == 0) {
+                int okw = 1;
+                if (lane == 0) okw = mbar_wait(bar(B_EMPTY + s_), ph ^ 1, abort) ? 1 : 0;
+                if (__shfl_sync(0xffffffffu, okw, 0) == 0) return false;
+                const uint32_t dst = smem_u32(sm + Lay::OFF_X + s_ * PAIR);
+                const uint32_t fb = bar(B_FULL + s_);
+                if (tile == 0) {
+                    if (lane == 0) {
                         const CUtensorMap *m = lo ? &rawLo : &rawHi;
+                        mbar_expect_tx(fb, PAIR);
                         if (!pv) {      // d-chunk a, rows 0..127
                             tma_box(dst, m, 64 * a, k.raw_row0, fb);
                             tma_box(dst + SLOT, m, 64 * a, k.raw_row0 + 64, fb);
-                        } else {        // d-block a, rows 64*hh..
+                        } else {        // d-block a, rows 64*hh .. 64*hh+63
                             tma_box(dst, m, 128 * a, k.raw_row0 + 64 * hh, fb);
                             tma_box(dst + SLOT, m, 128 * a + 64, k.raw_row0 + 64 * hh, fb);
                         }
                     } else {
-                        const CUtensorMap *m = lo ? &compLo : &compHi;
-                        if (!pv) {
-                            for (int g = 0; g < 32; g++)
-                                tma_gather4(dst + g * 512, m, 64 * a, row_of(tile, 4 * g), row_of(tile, 4 * g + 1),
-                                            row_of(tile, 4 * g + 2), row_of(tile, 4 * g + 3), fb);
-                        } else {
-                            for (int half = 0; half < 2; half++)
-                                for (int g = 0; g < 16; g++) {
-                                    const int r = 64 * hh + 4 * g;
-                                    tma_gather4(dst + half * SLOT + g * 512, m, 128 * a + 64 * half, row_of(tile, r),
-                                                row_of(tile, r + 1), row_of(tile, r + 2), row_of(tile, r + 3), fb);
-                                }
+                        mbar_arrive(fb);
+                    }
+                } else {
+                    // 1024 chunks of 16 bytes, 32 per lane, in the 128-byte swizzle layout
+                    const uint16_t *split = p.comp_split + lo * D;
+                    if (!pv) {
+#pragma unroll
+                        for (int m = 0; m < 4; m++) {
+                            const int r = lane + 32 * m;
+                            const uint16_t *src = split + (size_t)row_of(tile, r) * 2 * D + 64 * a;
+                            const uint32_t drow = dst + r * 128;
+#pragma unroll
+                            for (int u = 0; u < 8; u++) cp_async16(drow + ((u ^ (r & 7)) << 4), src + 8 * u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int m = 0; m < 2; m++) {
+                            const int rr = lane + 32 * m;
+                            const uint16_t *src0 = split + (size_t)row_of(tile, 64 * hh + rr) * 2 * D + 128 * a;
+#pragma unroll
+                            for (int half = 0; half < 2; half++) {
+                                const uint32_t drow = dst + half * SLOT + rr * 128;
+#pragma unroll
+                                for (int u = 0; u < 8; u++)
+                                    cp_async16(drow + ((u ^ (rr & 7)) << 4), src0 + 64 * half + 8 * u);
+                            }
                         }
                     }
+                    cp_async_arrive(fb);
                 }
                 return true;
             };
             auto issue_qk = [&](int tile) -> bool {
-                for (int c = 0; c < Lay::DC; c++)
-                    for (int v = 0; v < 2; v++)
-                        if (!issue(tile, false, c, 0, v)) return false;
+                for (int c = 0; c < Lay::DC; c++) {
+                    if (!issue(tile, false, c, 0, 0)) return false;
+                    if ((tile == 0 || c >= p.nope_chunks) && !issue(tile, false, c, 0, 1)) return false;
+                }
                 return true;
             };
             auto issue_pv = [&](int tile) -> bool {
                 for (int j = 0; j < Lay::DB; j++)
-                    for (int hh = 0; hh < 2; hh++)
-                        for (int v = 0; v < 2; v++)
-                            if (!issue(tile, true, j, hh, v)) return false;
+                    for (int hh = 0; hh < 2; hh++) {
+                        if (!issue(tile, true, j, hh, 0)) return false;
+                        if ((tile == 0 || j >= p.nope_blocks) && !issue(tile, true, j, hh, 1)) return false;
+                    }
                 return true;
             };
-            bool good = issue_qk(0);
-            for (int i = 0; i < n_tiles && good; i++) {
-                if (i + 1 < n_tiles) good = issue_qk(i + 1);
+            bool good = issue_qk(itm.tb);
+            for (int i = itm.tb; i < itm.te && good; i++) {
+                if (i + 1 < itm.te) good = issue_qk(i + 1);
                 if (good) good = issue_pv(i);
             }
-            ok = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
+            ok = good;
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -426,51 +470,55 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             return mbar_wait(bar(B_FULL + u % RING), (u / RING) & 1, abort);
         };
         auto free_unit = [&](uint32_t u) { mma_commit(bar(B_EMPTY + u % RING)); };
-        auto do_qk = [&](uint32_t gt) -> bool {
+        auto do_qk = [&](uint32_t gt, int tile) -> bool {
             const int sb = gt & 1;
             if (gt >= 2 && !mbar_wait(bar(B_SFREE0 + sb), ((gt >> 1) - 1) & 1, abort)) return false;
             fence_after();
             const uint32_t d_t = tmem + Lay::T_S + sb * H;
-            for (int c = 0; c < Lay::DC; c++, unit += 2) {
-                uint32_t xh, xl;
-                if (!wait_unit(unit, xh) || !wait_unit(unit + 1, xl)) return false;
+            for (int c = 0; c < Lay::DC; c++) {
+                const bool has_lo = tile == 0 || c >= p.nope_chunks;
+                uint32_t xh, xl = 0;
+                if (!wait_unit(unit, xh)) return false;
+                if (has_lo && !wait_unit(unit + 1, xl)) return false;
+                fence_proxy_async();
                 fence_after();
                 for (int kk = 0; kk < 4; kk++) {
                     const uint64_t ah = make_desc(xh + kk * 32, 16, 1024, 2);
-                    const uint64_t al = make_desc(xl + kk * 32, 16, 1024, 2);
                     const uint64_t bh = make_desc(qhi + c * (H * 128) + kk * 32, 16, 1024, 2);
                     const uint64_t bl = make_desc(qlo + c * (H * 128) + kk * 32, 16, 1024, 2);
                     mma(d_t, ah, bh, ID_QK, (c > 0 || kk > 0) ? 1u : 0u);
                     mma(d_t, ah, bl, ID_QK, 1u);
-                    mma(d_t, al, bh, ID_QK, 1u);
+                    if (has_lo) mma(d_t, make_desc(xl + kk * 32, 16, 1024, 2), bh, ID_QK, 1u);
                 }
-                free_unit(unit);
-                free_unit(unit + 1);
+                free_unit(unit++);
+                if (has_lo) free_unit(unit++);
             }
             mma_commit(bar(B_SFULL0 + sb));
             return true;
         };
-        auto do_pv = [&](int i) -> bool {
+        auto do_pv = [&](int i, bool first) -> bool {
             for (int j = 0; j < Lay::DB; j++) {
                 const uint32_t d_o = tmem + Lay::T_O + j * H;
-                for (int hh = 0; hh < 2; hh++, unit += 2) {
-                    uint32_t xh, xl;
-                    if (!wait_unit(unit, xh) || !wait_unit(unit + 1, xl)) return false;
+                const bool has_lo = i == 0 || j >= p.nope_blocks;
+                for (int hh = 0; hh < 2; hh++) {
+                    uint32_t xh, xl = 0;
+                    if (!wait_unit(unit, xh)) return false;
+                    if (has_lo && !wait_unit(unit + 1, xl)) return false;
+                    fence_proxy_async();
                     fence_after();
                     for (int kk = 0; kk < 4; kk++) {
                         const uint32_t koff = (uint32_t)(kk * 16 * 128);
                         const uint32_t prow = (uint32_t)((64 * hh + 16 * kk) * 128);
                         const uint64_t ah = make_desc(xh + koff, SLOT, 1024, 2);
-                        const uint64_t al = make_desc(xl + koff, SLOT, 1024, 2);
                         const uint64_t bh = make_desc(phi + prow, 8192, 1024, 2);
                         const uint64_t bl = make_desc(plo + prow, 8192, 1024, 2);
-                        const uint32_t acc = (i == 0 && hh == 0 && kk == 0) ? 0u : 1u;
+                        const uint32_t acc = (first && hh == 0 && kk == 0) ? 0u : 1u;
                         mma(d_o, ah, bh, ID_PV, acc);
                         mma(d_o, ah, bl, ID_PV, 1u);
-                        mma(d_o, al, bh, ID_PV, 1u);
+                        if (has_lo) mma(d_o, make_desc(xl + koff, SLOT, 1024, 2), bh, ID_PV, 1u);
                     }
-                    free_unit(unit);
-                    free_unit(unit + 1);
+                    free_unit(unit++);
+                    if (has_lo) free_unit(unit++);
                 }
             }
             // denominator: L += ones * P (hi and lo)
@@ -479,34 +527,37 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                 const uint64_t a1 = make_desc(ones, 128, 256, 0);
                 const uint64_t bh = make_desc(phi + kk * 16 * 128, 8192, 1024, 2);
                 const uint64_t bl = make_desc(plo + kk * 16 * 128, 8192, 1024, 2);
-                mma(d_l, a1, bh, ID_L, (i == 0 && kk == 0) ? 0u : 1u);
+                mma(d_l, a1, bh, ID_L, (first && kk == 0) ? 0u : 1u);
                 mma(d_l, a1, bl, ID_L, 1u);
             }
             mma_commit(bar(B_PVDONE));
             return true;
         };
-        for (int n = blockIdx.x; n < p.n_q && ok; n += gridDim.x, tok++) {
-            const Tok k = token_geom(p, n);
+        const int n_items = p.n_q * p.parts;
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+            const Tok k = token_geom(p, it / p.parts);
             const int nc = comp_rows(p, k, nullptr);          // whole warp
-            const int n_tiles = 1 + (nc + ROWS - 1) / ROWS;
+            const Item itm = item_tiles(p, it, 1 + (nc + ROWS - 1) / ROWS);
+            if (itm.tb >= itm.te) continue;
             int good = 1;
             if (lane == 0) {
                 good = mbar_wait(bar(B_QREADY), tok & 1, abort) ? 1 : 0;
                 if (good) {
                     fence_after();
-                    good = do_qk(g) ? 1 : 0;
+                    good = do_qk(g, itm.tb) ? 1 : 0;
                 }
-                for (int i = 0; i < n_tiles && good; i++) {
-                    const uint32_t gi = g + i;
-                    if (i + 1 < n_tiles && !do_qk(gi + 1)) { good = 0; break; }
+                for (int i = itm.tb; i < itm.te && good; i++) {
+                    const uint32_t gi = g + (i - itm.tb);
+                    if (i + 1 < itm.te && !do_qk(gi + 1, i + 1)) { good = 0; break; }
                     if (!mbar_wait(bar(B_PFULL), gi & 1, abort)) { good = 0; break; }
-                    if (i == 0 && tok > 0 && !mbar_wait(bar(B_OFREE), (tok - 1) & 1, abort)) { good = 0; break; }
+                    if (i == itm.tb && tok > 0 && !mbar_wait(bar(B_OFREE), (tok - 1) & 1, abort)) { good = 0; break; }
                     fence_after();
-                    if (!do_pv(i)) { good = 0; break; }
+                    if (!do_pv(i, i == itm.tb)) { good = 0; break; }
                 }
             }
             ok = __shfl_sync(0xffffffffu, good, 0) != 0;
-            g += n_tiles;
+            g += itm.te - itm.tb;
+            tok++;
         }
         // drain: every MMA issued so far has completed before the TMEM is freed
         if (lane == 0 && g > 0) mbar_wait(bar(B_PVDONE), (g - 1) & 1, abort);
@@ -551,16 +602,37 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             sphase ^= 1;
             return r_;
         };
-        int n = blockIdx.x;
-        if (n < p.n_q) load_q(n);
-        for (; n < p.n_q && ok; n += gridDim.x, tok++) {
+        const int n_items = p.n_q * p.parts;
+        // next non-empty item of this CTA at or after `it` (n_items when none)
+        auto next_item = [&](int it) -> int {
+            for (; it < n_items; it += gridDim.x) {
+                const Tok kk = token_geom(p, it / p.parts);
+                const int ncc = comp_rows(p, kk, nullptr);
+                const Item ii = item_tiles(p, it, 1 + (ncc + ROWS - 1) / ROWS);
+                if (ii.tb < ii.te) return it;
+            }
+            return n_items;
+        };
+        {
+            const int first = next_item(blockIdx.x);
+            if (first < n_items) load_q(first / p.parts);
+        }
+        for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+            const int n = it / p.parts;
             const Tok k = token_geom(p, n);
             const int nc = comp_rows(p, k, nullptr);
-            const int n_tiles = 1 + (nc + ROWS - 1) / ROWS;
-            float mref[H];
-#pragma unroll
-            for (int h = 0; h < H; h++) mref[h] = -INFINITY;
-            for (int i = 0; i < n_tiles; i++, g++) {
+            const Item itm = item_tiles(p, it, 1 + (nc + ROWS - 1) / ROWS);
+            if (itm.tb >= itm.te) {
+                // empty part: no rows, zero weight in the combine
+                if (tid < H) {
+                    p.part_ml[(size_t)it * 2 * H + tid] = -INFINITY;
+                    p.part_ml[(size_t)it * 2 * H + H + tid] = 0.f;
+                }
+                continue;
+            }
+            if (tid < H) mref_s[tid] = -INFINITY;
+            if (!soft_bar()) { ok = false; break; }
+            for (int i = itm.tb; i < itm.te; i++, g++) {
                 const int sb = g & 1;
                 if (!mbar_wait(bar(B_SFULL0 + sb), (g >> 1) & 1, abort)) { ok = false; break; }
                 fence_after();
@@ -573,7 +645,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
 #pragma unroll
                 for (int h = 0; h < H; h++) {
                     s[h] = valid ? s[h] * p.scale_log2 : -INFINITY;
-                    need |= s[h] > mref[h] + TAU;
+                    need |= s[h] > mref_s[h] + TAU;
                 }
                 // block-wide vote among the 128 softmax threads
                 const unsigned bal = __ballot_sync(0xffffffffu, need);
@@ -583,28 +655,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                                  flags[(g & 1) * 4 + 3];
                 bool waited = false;
                 if (any) {
-                    // exact tile maximum per head
-                    float mx[H];
+                    // exact tile maximum per head, then the new reference and the rescale factors
 #pragma unroll
                     for (int h = 0; h < H; h++) {
                         float v = s[h];
 #pragma unroll
                         for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-                        mx[h] = v;
+                        if (lane == 0) red[q4 * H + h] = v;
                     }
-                    if (lane == 0)
-                        for (int h = 0; h < H; h++) red[q4 * H + h] = mx[h];
                     if (!soft_bar()) { ok = false; break; }
-                    float alpha[H];
-#pragma unroll
-                    for (int h = 0; h < H; h++) {
-                        const float mt = fmaxf(fmaxf(red[h], red[H + h]), fmaxf(red[2 * H + h], red[3 * H + h]));
-                        const float mn = fmaxf(mref[h], mt);
-                        alpha[h] = exp2f(mref[h] - mn);
-                        mref[h] = mn;
+                    if (tid < H) {
+                        const float mt = fmaxf(fmaxf(red[tid], red[H + tid]), fmaxf(red[2 * H + tid], red[3 * H + tid]));
+                        const float mo = mref_s[tid];
+                        const float mn = fmaxf(mo, mt);
+                        alpha_s[tid] = exp2f(mo - mn);
+                        mref_s[tid] = mn;
                     }
-                    if (!soft_bar()) { ok = false; break; }   // red[] reusable
-                    if (i > 0) {
+                    if (!soft_bar()) { ok = false; break; }
+                    if (i > itm.tb) {
                         if (!mbar_wait(bar(B_PVDONE), (g - 1) & 1, abort)) { ok = false; break; }
                         waited = true;
                         fence_after();
@@ -612,17 +680,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                         for (int j = 0; j < Lay::DB; j++) {
                             tmem_load<H>(lane_base + Lay::T_O + j * H, v);
 #pragma unroll
-                            for (int h = 0; h < H; h++) v[h] *= alpha[h];
+                            for (int h = 0; h < H; h++) v[h] *= alpha_s[h];
                             tmem_store<H>(lane_base + Lay::T_O + j * H, v);
                         }
                         tmem_load<H>(lane_base + Lay::T_L, v);
 #pragma unroll
-                        for (int h = 0; h < H; h++) v[h] *= alpha[h];
+                        for (int h = 0; h < H; h++) v[h] *= alpha_s[h];
                         tmem_store<H>(lane_base + Lay::T_L, v);
                         fence_before();
                     }
                 }
-                if (i > 0 && !waited) {
+                if (i > itm.tb && !waited) {
                     if (!mbar_wait(bar(B_PVDONE), (g - 1) & 1, abort)) { ok = false; break; }
                 }
                 // P^T row r (MN-major, 128-byte swizzle), hi and lo
@@ -631,7 +699,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                     float hv[8], lv[8];
 #pragma unroll
                     for (int e = 0; e < 8; e++) {
-                        const float pv = exp2f(s[u * 8 + e] - mref[u * 8 + e]);
+                        const float pv = exp2f(s[u * 8 + e] - mref_s[u * 8 + e]);
                         split_bf16(pv, hv[e], lv[e]);
                     }
                     const int off = r * (H * 2) + ((u ^ (r & 7)) * 16);
@@ -642,19 +710,35 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                 }
                 fence_proxy_async();
                 mbar_arrive(bar(B_PFULL));
-                if (i == n_tiles - 1) {
-                    // the last S of this token has been read: Q is free for the next token
-                    const int nn = n + gridDim.x;
-                    if (nn < p.n_q) load_q(nn);
+                if (i == itm.te - 1) {
+                    // the last S of this item has been read: Q is free for the next item
+                    const int nx = next_item(it + gridDim.x);
+                    if (nx < n_items) load_q(nx / p.parts);
                     if (!mbar_wait(bar(B_PVDONE), g & 1, abort)) { ok = false; break; }
                     fence_after();
                     float l[H], v[H];
                     tmem_load<H>(lane_base + Lay::T_L, l);
-                    float *o = p.out + (size_t)n * H * D;
-                    for (int j = 0; j < Lay::DB; j++) {
-                        tmem_load<H>(lane_base + Lay::T_O + j * H, v);
+                    if (p.parts == 1) {
+                        float *o = p.out + (size_t)n * H * D;
+                        for (int j = 0; j < Lay::DB; j++) {
+                            tmem_load<H>(lane_base + Lay::T_O + j * H, v);
 #pragma unroll
-                        for (int h = 0; h < H; h++) o[(size_t)h * D + 128 * j + r] = v[h] / l[h];
+                            for (int h = 0; h < H; h++) o[(size_t)h * D + 128 * j + r] = v[h] / l[h];
+                        }
+                    } else {
+                        float *o = p.part_o + (size_t)it * H * D;
+                        for (int j = 0; j < Lay::DB; j++) {
+                            tmem_load<H>(lane_base + Lay::T_O + j * H, v);
+#pragma unroll
+                            for (int h = 0; h < H; h++) o[(size_t)h * D + 128 * j + r] = v[h];
+                        }
+                        if (tid < H) {
+                            float lt = 0.f;
+#pragma unroll
+                            for (int h = 0; h < H; h++) lt = (h == tid) ? l[h] : lt;
+                            p.part_ml[(size_t)it * 2 * H + tid] = mref_s[tid];
+                            p.part_ml[(size_t)it * 2 * H + H + tid] = lt;
+                        }
                     }
                     fence_before();
                     mbar_arrive(bar(B_OFREE));
@@ -695,6 +779,30 @@ __global__ void raw_split_kernel(uint16_t *__restrict__ mirror, const float *__r
         for (int e = 0; e < 4; e++) split_bf16(a[e], h[e], l[e]);
         *reinterpret_cast<uint2 *>(hi + j) = make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
         *reinterpret_cast<uint2 *>(lo + j) = make_uint2(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]));
+    }
+}
+
+// Split rows: out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p over the
+// parts of a query (M = the largest reference of a non-empty part).
+__global__ void attn_combine_kernel(float *__restrict__ out, const float *__restrict__ part_o,
+                                    const float *__restrict__ part_ml, int H, int D, int parts) {
+    const int n = blockIdx.x;
+    for (int e = threadIdx.x; e < H * D; e += blockDim.x) {
+        const int h = e / D;
+        float M = -INFINITY;
+        for (int q = 0; q < parts; q++) {
+            const float *ml = part_ml + ((size_t)n * parts + q) * 2 * H;
+            if (ml[H + h] > 0.f) M = fmaxf(M, ml[h]);
+        }
+        float num = 0.f, den = 0.f;
+        for (int q = 0; q < parts; q++) {
+            const float *ml = part_ml + ((size_t)n * parts + q) * 2 * H;
+            if (!(ml[H + h] > 0.f)) continue;
+            const float w = exp2f(ml[h] - M);
+            num += w * part_o[((size_t)n * parts + q) * H * D + e];
+            den += w * ml[H + h];
+        }
+        out[(size_t)n * H * D + e] = num / den;
     }
 }
 
@@ -740,27 +848,29 @@ cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, cudaStream_t s
     using Lay = L<H, D>;
     const uint64_t raw_rows = (a.n_seq == 1) ? (uint64_t)(ROWS + a.n_tok) : (uint64_t)a.n_seq * ROWS;
     const uint64_t comp_rows_total = (uint64_t)a.n_seq_state * a.comp_cap;
-    CUtensorMap rh, rl, ch, cl;
+    CUtensorMap rh, rl;
     const uint64_t pitch = (uint64_t)2 * D * 2;
     if (!make_map(&rh, a.raw_mirror, raw_rows, D, pitch, 64) || !make_map(&rl, a.raw_mirror + D, raw_rows, D, pitch, 64))
         return cudaErrorNotSupported;
-    if (a.comp_split && comp_rows_total > 0) {
-        if (!make_map(&ch, a.comp_split, comp_rows_total, D, pitch, 1) ||
-            !make_map(&cl, a.comp_split + D, comp_rows_total, D, pitch, 1))
-            return cudaErrorNotSupported;
-    } else {
-        ch = rh;
-        cl = rl;
-    }
+    (void)comp_rows_total;
     cudaError_t e = ensure_dyn_smem(attn_tc_kernel<H, D>, Lay::SMEM);
     if (e != cudaSuccess) return e;
-    const int nq = a.n_seq * a.n_tok;
-    const int grid = nq < sm_count() ? nq : sm_count();
-    attn_tc_kernel<H, D><<<grid, THREADS, Lay::SMEM, s>>>(rh, rl, ch, cl, p);
+    const int items = a.n_seq * a.n_tok * p.parts;
+    const int grid = items < sm_count() ? items : sm_count();
+    attn_tc_kernel<H, D><<<grid, THREADS, Lay::SMEM, s>>>(rh, rl, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || p.parts == 1) return e;
+    attn_combine_kernel<<<a.n_seq * a.n_tok, 256, 0, s>>>(a.out, p.part_o, p.part_ml, H, D, p.parts);
     return cudaGetLastError();
 }
 
 }  // namespace
+
+int attn_tc_decode_parts(int ratio, int k, int comp_cap) {
+    const int rows = ratio == 4 ? (k < comp_cap ? k : comp_cap) : (ratio == 128 ? comp_cap : 0);
+    const int tiles = 1 + (rows + ROWS - 1) / ROWS;
+    return tiles < 8 ? tiles : 8;
+}
 
 bool attn_tc_supported(int H, int D, int S, int ratio, int k) {
     const bool hd = H == 64 && (D == 512 || D == 256 || D == 128);
@@ -781,6 +891,12 @@ cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *dp, cudaSt
     p.out = a.out;
     p.q = a.q;
     p.topk = a.topk;
+    p.comp_split = a.comp_split;
+    p.nope_chunks = (a.D - a.n_rot) / 64;
+    p.nope_blocks = (a.D - a.n_rot) / 128;
+    p.parts = a.parts > 0 ? a.parts : 1;
+    p.part_o = a.part_o;
+    p.part_ml = a.part_ml;
     p.n_q = nq;
     p.n_seq = a.n_seq;
     p.n_tok = a.n_tok;
