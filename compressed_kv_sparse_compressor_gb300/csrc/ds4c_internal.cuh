@@ -12,7 +12,7 @@ namespace ds4c {
 
 constexpr int kMaxRot = 128;
 constexpr int kMaxDecodeSeq = 1024;
-constexpr uint32_t kMaxIdxCap = 53248;
+constexpr uint32_t kMaxIdxCap = 40960;
 
 inline int lane_width(const ds4c_layer_cfg &c, bool attn) { return attn ? (int)c.head_dim : (int)c.idx_head_dim; }
 inline int coff_of(const ds4c_layer_cfg &c) { return c.ratio == 4 ? 2 : 1; }

@@ -269,9 +269,11 @@ __device__ __forceinline__ Tok token_geom(const TcAttnParams &p, int n) {
 }
 
 // Number of compressed rows a query attends (ratio 4: the top-k list read the
-// way the attention loop of [P2] §7 reads it; ratio 128: every visible row).
-// The whole warp calls this; the list (row indices into the comp mirror) is
-// written to `list` when non-null.
+// way the attention loop of [P2] §7 reads it -- entries < 0 skipped, the first
+// entry >= visible ends the list; ratio 128: every visible row).  The whole
+// warp calls this; each lane loads 16 consecutive entries at once, so a 512-
+// entry list costs one memory latency.  The list (row indices into the comp
+// mirror) is written to `list` when non-null.
 __device__ __forceinline__ int comp_rows(const TcAttnParams &p, const Tok &k, int *list) {
     const int lane = threadIdx.x & 31;
     if (p.ratio == 128) {
@@ -282,16 +284,37 @@ __device__ __forceinline__ int comp_rows(const TcAttnParams &p, const Tok &k, in
     const uint64_t visible = (k.t + 1) / 4;
     const int32_t *tk = p.topk + (size_t)k.n * p.k;
     int cnt = 0;
-    for (int base = 0; base < p.k; base += 32) {
-        const int i = base + lane;
-        const int32_t idx = (i < p.k) ? tk[i] : -1;
-        const bool stop = idx >= 0 && (uint64_t)idx >= visible;
-        const unsigned stop_m = __ballot_sync(0xffffffffu, stop);
-        const unsigned before = stop_m ? ((stop_m & (0u - stop_m)) - 1u) : 0xffffffffu;  // lanes before the first stop
-        const bool valid = idx >= 0 && !stop && (((before >> lane) & 1u) != 0u);
-        const unsigned vm = __ballot_sync(0xffffffffu, valid);
-        if (valid && list) list[cnt + __popc(vm & ((1u << lane) - 1u))] = k.seq * p.comp_cap + idx;
-        cnt += __popc(vm);
+    for (int base = 0; base < p.k; base += 512) {
+        int32_t v[16];
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+            const int i = base + lane * 16 + j;
+            v[j] = (i < p.k) ? __ldg(tk + i) : -1;
+        }
+        int first_stop = 16, local = 0;
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+            const bool stop = v[j] >= 0 && (uint64_t)v[j] >= visible;
+            if (stop && first_stop == 16) first_stop = j;
+            if (v[j] >= 0 && first_stop == 16) local++;
+        }
+        const unsigned stop_m = __ballot_sync(0xffffffffu, first_stop < 16);
+        const int f = stop_m ? __ffs(stop_m) - 1 : 32;     // first lane holding a stop
+        const int contrib = lane < f ? local : (lane == f ? local : 0);
+        // exclusive prefix of the contributions
+        int incl = contrib;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (list && contrib > 0) {
+            int w = cnt + incl - contrib;
+#pragma unroll
+            for (int j = 0; j < 16; j++)
+                if (j < first_stop && v[j] >= 0) list[w++] = k.seq * p.comp_cap + v[j];
+        }
+        cnt += __shfl_sync(0xffffffffu, incl, 31);
         if (stop_m) break;
     }
     return cnt;
@@ -574,24 +597,43 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         (void)qhi;
         (void)qlo;
         auto load_q = [&](int n) {
+            // 16 independent 16-byte loads in flight per thread, then split and store
             const float4 *qs = reinterpret_cast<const float4 *>(p.q + (size_t)n * H * D);
-            for (int f = tid; f < H * D / 4; f += 128) {
-                const float4 v = qs[f];
-                const int h = f / (D / 4);
-                const int d = (f % (D / 4)) * 4;
-                const int c = d / 64, e = d % 64;
-                const int unit16 = (e / 8) ^ (h & 7);
-                const int off = c * (H * 128) + h * 128 + unit16 * 16 + (e % 8) * 2;
-                float h0, l0, h1, l1, h2, l2, h3, l3;
-                split_bf16(v.x, h0, l0);
-                split_bf16(v.y, h1, l1);
-                split_bf16(v.z, h2, l2);
-                split_bf16(v.w, h3, l3);
-                *reinterpret_cast<uint2 *>(sm + Lay::OFF_QHI + off) = make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3));
-                *reinterpret_cast<uint2 *>(sm + Lay::OFF_QLO + off) = make_uint2(pack_bf16x2(l0, l1), pack_bf16x2(l2, l3));
+            constexpr int NF = H * D / 4;
+            for (int f0 = tid; f0 < NF; f0 += 128 * 16) {
+                float4 vv[16];
+#pragma unroll
+                for (int u = 0; u < 16; u++) {
+                    const int f = f0 + 128 * u;
+                    vv[u] = (f < NF) ? __ldg(qs + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < 16; u++) {
+                    const int f = f0 + 128 * u;
+                    if (f >= NF) break;
+                    const float4 v = vv[u];
+                    const int h = f / (D / 4);
+                    const int d = (f % (D / 4)) * 4;
+                    const int c = d / 64, e = d % 64;
+                    const int unit16 = (e / 8) ^ (h & 7);
+                    const int off = c * (H * 128) + h * 128 + unit16 * 16 + (e % 8) * 2;
+                    float h0, l0, h1, l1, h2, l2, h3, l3;
+                    split_bf16(v.x, h0, l0);
+                    split_bf16(v.y, h1, l1);
+                    split_bf16(v.z, h2, l2);
+                    split_bf16(v.w, h3, l3);
+                    *reinterpret_cast<uint2 *>(sm + Lay::OFF_QHI + off) = make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3));
+                    *reinterpret_cast<uint2 *>(sm + Lay::OFF_QLO + off) = make_uint2(pack_bf16x2(l0, l1), pack_bf16x2(l2, l3));
+                }
             }
             fence_proxy_async();
             mbar_arrive(bar(B_QREADY));
+        };
+        // bring a later query's Q into L2 while this one is processed
+        auto prefetch_q = [&](int n) {
+            const char *base = reinterpret_cast<const char *>(p.q + (size_t)n * H * D);
+            for (int off = tid * 128; off < H * D * 4; off += 128 * 128)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(base + off));
         };
         uint32_t g = 0, tok = 0, sphase = 0;
         bool ok = true;
@@ -619,6 +661,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         }
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const int n = it / p.parts;
+            if (it + gridDim.x < n_items && (it + gridDim.x) / p.parts != n) prefetch_q((it + gridDim.x) / p.parts);
             const Tok k = token_geom(p, n);
             const int nc = comp_rows(p, k, nullptr);
             const Item itm = item_tiles(p, it, 1 + (nc + ROWS - 1) / ROWS);
@@ -784,25 +827,37 @@ __global__ void raw_split_kernel(uint16_t *__restrict__ mirror, const float *__r
 
 // Split rows: out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p over the
 // parts of a query (M = the largest reference of a non-empty part).
-__global__ void attn_combine_kernel(float *__restrict__ out, const float *__restrict__ part_o,
-                                    const float *__restrict__ part_ml, int H, int D, int parts) {
-    const int n = blockIdx.x;
-    for (int e = threadIdx.x; e < H * D; e += blockDim.x) {
-        const int h = e / D;
+__global__ void __launch_bounds__(128) attn_combine_kernel(float *__restrict__ out, const float *__restrict__ part_o,
+                                                           const float *__restrict__ part_ml, int H, int D, int parts) {
+    __shared__ float w[8];
+    __shared__ float inv_den;
+    const int n = blockIdx.x / H, h = blockIdx.x % H;
+    if (threadIdx.x == 0) {
         float M = -INFINITY;
         for (int q = 0; q < parts; q++) {
             const float *ml = part_ml + ((size_t)n * parts + q) * 2 * H;
             if (ml[H + h] > 0.f) M = fmaxf(M, ml[h]);
         }
-        float num = 0.f, den = 0.f;
+        float den = 0.f;
         for (int q = 0; q < parts; q++) {
             const float *ml = part_ml + ((size_t)n * parts + q) * 2 * H;
-            if (!(ml[H + h] > 0.f)) continue;
-            const float w = exp2f(ml[h] - M);
-            num += w * part_o[((size_t)n * parts + q) * H * D + e];
-            den += w * ml[H + h];
+            const float wq = (ml[H + h] > 0.f) ? exp2f(ml[h] - M) : 0.f;
+            w[q] = wq;
+            den += wq * ml[H + h];
         }
-        out[(size_t)n * H * D + e] = num / den;
+        inv_den = 1.0f / den;
+    }
+    __syncthreads();
+    for (int d = threadIdx.x * 4; d < D; d += blockDim.x * 4) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < parts; q++) {
+            const float wq = w[q];
+            if (wq == 0.f) continue;
+            const float4 o = *reinterpret_cast<const float4 *>(part_o + (((size_t)n * parts + q) * H + h) * D + d);
+            acc.x += wq * o.x; acc.y += wq * o.y; acc.z += wq * o.z; acc.w += wq * o.w;
+        }
+        const float id = inv_den;
+        *reinterpret_cast<float4 *>(out + ((size_t)n * H + h) * D + d) = make_float4(acc.x * id, acc.y * id, acc.z * id, acc.w * id);
     }
 }
 
@@ -860,7 +915,7 @@ cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, cudaStream_t s
     attn_tc_kernel<H, D><<<grid, THREADS, Lay::SMEM, s>>>(rh, rl, p);
     e = cudaGetLastError();
     if (e != cudaSuccess || p.parts == 1) return e;
-    attn_combine_kernel<<<a.n_seq * a.n_tok, 256, 0, s>>>(a.out, p.part_o, p.part_ml, H, D, p.parts);
+    attn_combine_kernel<<<a.n_seq * a.n_tok * H, 128, 0, s>>>(a.out, p.part_o, p.part_ml, H, D, p.parts);
     return cudaGetLastError();
 }
 

@@ -28,14 +28,24 @@ __device__ unsigned int g_gemm_tc_err;
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int TMEM_COLS = 512;
+constexpr int BM = 128, BK = 64;
 constexpr int THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr unsigned long long WAIT_NS = 4000000000ull;
+
+// Tile width BN: 256 for prefill chunks; 32 for decode-sized M, where the
+// weights are the traffic and more, narrower tiles spread them over the SMs.
+template <int BN>
+struct GT {
+    static constexpr int STAGES = BN >= 128 ? 4 : 8;
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+    // instruction descriptor: kind::f16, A = B = bf16, D = f32, both K-major, M = 128, N = BN
+    static constexpr uint32_t IDESC =
+        (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+};
 
 struct TcParams {
     int M, K;
@@ -115,15 +125,12 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
     return d;
 }
 
-// Instruction descriptor: kind::f16, A = B = bf16, D = f32, both K-major.
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(IDESC), "r"(accumulate)
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -155,10 +162,13 @@ __device__ __forceinline__ void tile_coords(const TcParams &p, int tile, int &g,
     mt = local % p.m_tiles;
 }
 
+template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
                const __grid_constant__ CUtensorMap mapB1, const __grid_constant__ CUtensorMap mapB2,
                const __grid_constant__ CUtensorMap mapB3, TcParams p) {
+    using G = GT<BN>;
+    constexpr int STAGES = G::STAGES, A_BYTES = G::A_BYTES, STAGE_BYTES = G::STAGE_BYTES, TMEM_COLS = G::TMEM_COLS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
@@ -236,7 +246,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
                     const uint32_t sb = sa + A_BYTES;
 #pragma unroll
                     for (int k = 0; k < BK / 16; k++)
-                        mma_bf16(d_tmem, sw128_desc(sa + k * 32), sw128_desc(sb + k * 32), (kb > 0 || k > 0) ? 1u : 0u);
+                        mma_bf16(d_tmem, sw128_desc(sa + k * 32), sw128_desc(sb + k * 32), G::IDESC,
+                                 (kb > 0 || k > 0) ? 1u : 0u);
                     mma_commit(smem_u32(&empty[s]));
                 }
                 if (ok) mma_commit(smem_u32(&acc_full[acc]));
@@ -327,11 +338,9 @@ int sm_count() {
     return n;
 }
 
-}  // namespace
-
-cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
-    if (a.dtype != DS4C_BF16 || a.M < 64 || a.K % 8 != 0 || a.n_groups < 1 || a.n_groups > 4)
-        return cudaErrorNotSupported;
+template <int BN>
+cudaError_t launch_bn(const GemmArgs &a, cudaStream_t s) {
+    using G = GT<BN>;
     if (((uintptr_t)a.A & 15) != 0) return cudaErrorNotSupported;
     TcParams p{};
     p.M = a.M;
@@ -344,13 +353,13 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
     for (int g = 0; g < 4; g++) {
         const int gi = g < a.n_groups ? g : a.n_groups - 1;
         if (g < a.n_groups) {
-            const GemmGroup &G = a.g[g];
-            if (((uintptr_t)G.B & 15) != 0 || (G.ldc % 4) != 0 || ((uintptr_t)G.C & 15) != 0) return cudaErrorNotSupported;
-            if (!make_map(&mB[g], G.B, (uint64_t)G.N, (uint64_t)a.K, BN)) return cudaErrorNotSupported;
-            p.N[g] = G.N;
-            p.C[g] = G.C;
-            p.ldc[g] = G.ldc;
-            p.n_tiles[g] = (G.N + BN - 1) / BN;
+            const GemmGroup &G_ = a.g[g];
+            if (((uintptr_t)G_.B & 15) != 0 || (G_.ldc % 4) != 0 || ((uintptr_t)G_.C & 15) != 0) return cudaErrorNotSupported;
+            if (!make_map(&mB[g], G_.B, (uint64_t)G_.N, (uint64_t)a.K, BN)) return cudaErrorNotSupported;
+            p.N[g] = G_.N;
+            p.C[g] = G_.C;
+            p.ldc[g] = G_.ldc;
+            p.n_tiles[g] = (G_.N + BN - 1) / BN;
             p.tile_start[g] = start;
             start += p.n_tiles[g] * p.m_tiles;
         } else {
@@ -358,11 +367,21 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
         }
     }
     p.tile_start[a.n_groups] = start;
-    cudaError_t e = ensure_dyn_smem(gemm_tc_kernel, SMEM_BYTES);
+    cudaError_t e = ensure_dyn_smem(gemm_tc_kernel<BN>, G::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int grid = start < sm_count() ? start : sm_count();
-    gemm_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(mA, mB[0], mB[1], mB[2], mB[3], p);
+    gemm_tc_kernel<BN><<<grid, THREADS, G::SMEM_BYTES, s>>>(mA, mB[0], mB[1], mB[2], mB[3], p);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
+    if (a.dtype != DS4C_BF16 || a.M < 1 || a.K % 8 != 0 || a.n_groups < 1 || a.n_groups > 4)
+        return cudaErrorNotSupported;
+    if (((uintptr_t)a.A & 15) != 0) return cudaErrorNotSupported;
+    // decode-sized M: narrow tiles, so the weight traffic spreads over many SMs
+    return a.M <= 256 ? launch_bn<32>(a, s) : launch_bn<256>(a, s);
 }
 
 unsigned int gemm_tc_read_clear_error() {

@@ -18,88 +18,128 @@ namespace ds4c {
 namespace {
 
 // ---------------------------------------------------------------------------
-// K4 prefill: n_tok queries of one sequence, 64x64 (query x row) tile per
-// 256-thread block, 4x4 per thread, d consumed in 32-wide slices in order.
+// K4 prefill: n_tok queries of one sequence against every visible row.  128 x
+// 128 (query x row) tile per 256-thread block, 8 x 8 outputs per thread, d
+// consumed in 16-wide slices in index order (so each output is exactly the
+// in-order fmaf chain), slices double-buffered in shared memory (k-major, so
+// a thread reads its 8 queries / 8 rows of one k as two 16-byte loads).
+// Tiles wholly past the visibility triangle are skipped.
 // ---------------------------------------------------------------------------
-constexpr int SB = 64, SK = 32;
+constexpr int SB = 128, SK = 16, SP = SB + 4;
+
+// 128 rows x 16 k of q and of the index rows: 512 float4 each, 2 per thread
+__device__ __forceinline__ void fetch_slice(float4 (&qv)[2], float4 (&rv)[2], const IndexerArgs &a, int j0, int c0,
+                                            uint64_t vis_max, int i0) {
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+        const int f = threadIdx.x + 256 * h;
+        const int r = f >> 2, k4 = (f & 3) * 4;
+        const int j = j0 + r, c = c0 + r;
+        qv[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+        rv[h] = qv[h];
+        if (j < a.n_tok) qv[h] = *reinterpret_cast<const float4 *>(a.q + (size_t)j * a.d + i0 + k4);
+        if ((uint64_t)c < vis_max) rv[h] = *reinterpret_cast<const float4 *>(a.rows + (size_t)c * a.d + i0 + k4);
+    }
+}
+__device__ __forceinline__ void store_slice(float (*As)[SP], float (*Bs)[SP], const float4 (&qv)[2], const float4 (&rv)[2]) {
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+        const int f = threadIdx.x + 256 * h;
+        const int r = f >> 2, k4 = (f & 3) * 4;
+        As[k4 + 0][r] = qv[h].x; As[k4 + 1][r] = qv[h].y; As[k4 + 2][r] = qv[h].z; As[k4 + 3][r] = qv[h].w;
+        Bs[k4 + 0][r] = rv[h].x; Bs[k4 + 1][r] = rv[h].y; Bs[k4 + 2][r] = rv[h].z; Bs[k4 + 3][r] = rv[h].w;
+    }
+}
 
 __global__ void __launch_bounds__(256) score_prefill_kernel(IndexerArgs a) {
     const int j0 = blockIdx.y * SB, c0 = blockIdx.x * SB;
     const int jlast = min(j0 + SB, a.n_tok) - 1;
     const uint64_t vis_max = (a.pos0 + (uint64_t)jlast + 1) / 4;
     if ((uint64_t)c0 >= vis_max) return;
-    __shared__ float Qs[SK][SB + 4];
-    __shared__ float Rs[SK][SB + 4];
+    __shared__ __align__(16) float As[2][SK][SP];
+    __shared__ __align__(16) float Bs[2][SK][SP];
     const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-    float acc[4][4];
+    float acc[8][8];
 #pragma unroll
-    for (int i = 0; i < 4; i++)
+    for (int i = 0; i < 8; i++)
 #pragma unroll
-        for (int k = 0; k < 4; k++) acc[i][k] = 0.f;
-    for (int i0 = 0; i0 < a.d; i0 += SK) {
-        for (int e = threadIdx.x; e < SB * SK; e += 256) {
-            const int r = e / SK, ii = e % SK;
-            const int j = j0 + r, c = c0 + r;
-            Qs[ii][r] = (j < a.n_tok) ? a.q[(size_t)j * a.d + i0 + ii] : 0.f;
-            Rs[ii][r] = ((uint64_t)c < vis_max) ? a.rows[(size_t)c * a.d + i0 + ii] : 0.f;
+        for (int k = 0; k < 8; k++) acc[i][k] = 0.f;
+    float4 qv[2], rv[2];
+    fetch_slice(qv, rv, a, j0, c0, vis_max, 0);
+    store_slice(As[0], Bs[0], qv, rv);
+    __syncthreads();
+    const int nslices = a.d / SK;
+    for (int sl = 0; sl < nslices; sl++) {
+        const int cur = sl & 1;
+        if (sl + 1 < nslices) fetch_slice(qv, rv, a, j0, c0, vis_max, (sl + 1) * SK);   // in flight during the FMAs
+#pragma unroll
+        for (int kk = 0; kk < SK; kk++) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(&As[cur][kk][ty * 8]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&As[cur][kk][ty * 8 + 4]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[cur][kk][tx * 8]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[cur][kk][tx * 8 + 4]);
+            const float qa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float rb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+#pragma unroll
+                for (int k = 0; k < 8; k++) acc[i][k] = __fmaf_rn(qa[i], rb[k], acc[i][k]);
         }
-        __syncthreads();
-#pragma unroll 4
-        for (int ii = 0; ii < SK; ii++) {
-            float qv[4], rv[4];
-#pragma unroll
-            for (int i = 0; i < 4; i++) qv[i] = Qs[ii][ty * 4 + i];
-#pragma unroll
-            for (int k = 0; k < 4; k++) rv[k] = Rs[ii][tx * 4 + k];
-#pragma unroll
-            for (int i = 0; i < 4; i++)
-#pragma unroll
-                for (int k = 0; k < 4; k++) acc[i][k] = __fmaf_rn(qv[i], rv[k], acc[i][k]);
-        }
+        if (sl + 1 < nslices) store_slice(As[cur ^ 1], Bs[cur ^ 1], qv, rv);
         __syncthreads();
     }
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-        const int j = j0 + ty * 4 + i;
+    for (int i = 0; i < 8; i++) {
+        const int j = j0 + ty * 8 + i;
         if (j >= a.n_tok) continue;
         const uint64_t vis = (a.pos0 + (uint64_t)j + 1) / 4;
+        float *dst = a.scores + (size_t)j * a.lds;
+        const int cb = c0 + tx * 8;
+        if ((uint64_t)cb + 8 <= vis && (a.lds % 4) == 0) {
+            *reinterpret_cast<float4 *>(dst + cb) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+            *reinterpret_cast<float4 *>(dst + cb + 4) = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+        } else {
 #pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const int c = c0 + tx * 4 + k;
-            if ((uint64_t)c < vis) a.scores[(size_t)j * a.lds + c] = acc[i][k];
+            for (int k = 0; k < 8; k++)
+                if ((uint64_t)(cb + k) < vis) dst[cb + k] = acc[i][k];
         }
     }
 }
 
 // ---------------------------------------------------------------------------
 // K4 decode: one query per sequence; a 128-thread block scores 128 rows of
-// its sequence, one row per thread.  Rows are staged through shared memory
-// with a padded stride so the in-order reads are conflict-free.
+// its sequence, one row per thread: the thread loads its whole row (d floats)
+// with independent 16-byte loads, then runs the in-order fma chain against q
+// (broadcast from shared memory).
 // ---------------------------------------------------------------------------
+template <int DD>
 __global__ void __launch_bounds__(128) score_decode_kernel(IndexerArgs a, DecodePos dp) {
-    extern __shared__ float sm[];
+    __shared__ float qs[DD];
     const int b = blockIdx.y;
     const uint64_t vis = (dp.pos[b] + 1) / 4;
-    const int c0 = blockIdx.x * 128;
-    if ((uint64_t)c0 >= vis) return;
-    const int d = a.d, ld = d + 1;
-    float *qs = sm;                 // [d]
-    float *rs = sm + d;             // [128][d+1]
-    const float *rows = a.rows + (size_t)b * a.seq_stride;
-    for (int i = threadIdx.x; i < d; i += 128) qs[i] = a.q[(size_t)b * d + i];
-    const uint64_t left = vis - (uint64_t)c0;
-    const int nrows = left < 128 ? (int)left : 128;
-    for (int e = threadIdx.x; e < 128 * d; e += 128) {
-        const int r = e / d, i = e % d;
-        rs[r * ld + i] = (r < nrows) ? rows[(size_t)(c0 + r) * d + i] : 0.f;
-    }
+    const int c = blockIdx.x * 128 + threadIdx.x;
+    if ((uint64_t)(blockIdx.x * 128) >= vis) return;
+    for (int i = threadIdx.x; i < DD; i += 128) qs[i] = a.q[(size_t)b * DD + i];
     __syncthreads();
-    if (threadIdx.x < nrows) {
-        float s = 0.f;
-        const float *row = rs + threadIdx.x * ld;
-        for (int i = 0; i < d; i++) s = __fmaf_rn(qs[i], row[i], s);
-        a.scores[(size_t)b * a.lds + c0 + threadIdx.x] = s;
+    if ((uint64_t)c >= vis) return;
+    const float4 *row = reinterpret_cast<const float4 *>(a.rows + (size_t)b * a.seq_stride + (size_t)c * DD);
+    float4 v[DD / 4];
+    // issue every load of the row before the first use (volatile keeps the order)
+#pragma unroll
+    for (int i = 0; i < DD / 4; i++)
+        asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(v[i].x), "=f"(v[i].y), "=f"(v[i].z), "=f"(v[i].w)
+                     : "l"(row + i));
+    asm volatile("" ::: "memory");   // the q reads below stay after the row loads
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < DD / 4; i++) {
+        s = __fmaf_rn(qs[4 * i + 0], v[i].x, s);
+        s = __fmaf_rn(qs[4 * i + 1], v[i].y, s);
+        s = __fmaf_rn(qs[4 * i + 2], v[i].z, s);
+        s = __fmaf_rn(qs[4 * i + 3], v[i].w, s);
     }
+    a.scores[(size_t)b * a.lds + c] = s;
 }
 
 // ---------------------------------------------------------------------------
@@ -112,86 +152,125 @@ __device__ __forceinline__ uint32_t order_key(float s) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Block-wide exclusive scan of a 0/1 flag over TK_THREADS threads.
-__device__ __forceinline__ int block_excl_scan(int flag, int *warp_tot, int &total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned bal = __ballot_sync(0xffffffffu, flag);
-    const int in_warp = __popc(bal & ((1u << lane) - 1u));
-    if (lane == 0) warp_tot[warp] = __popc(bal);
-    __syncthreads();
-    int before = 0, tot = 0;
-    for (int w = 0; w < TK_THREADS / 32; w++) {
-        const int v = warp_tot[w];
-        if (w < warp) before += v;
-        tot += v;
-    }
-    __syncthreads();
-    total = tot;
-    return before + in_warp;
-}
+constexpr int TK_BINS = 16;          // 4-bit radix digits, 8 passes
+constexpr int TK_CAND = 4096;        // survivors are compacted once they fit here
+constexpr int TK_WARPS = TK_THREADS / 32;
+// dynamic shared memory: counters [16][512] | candidates [4096] | keys [V]
+constexpr size_t TK_FIXED_SMEM = sizeof(uint32_t) * (TK_BINS * TK_THREADS + TK_CAND);
 
 __global__ void __launch_bounds__(TK_THREADS) topk_kernel(IndexerArgs a, DecodePos dp) {
-    extern __shared__ uint32_t keys[];
-    __shared__ uint32_t hist[256];
-    __shared__ int warp_tot[TK_THREADS / 32];
-    __shared__ uint32_t sh_prefix;
-    __shared__ int sh_remaining;
+    extern __shared__ uint32_t sm_tk[];
+    uint32_t *cnt = sm_tk;                              // cnt[bin * 512 + tid], private per thread
+    uint32_t *cand = sm_tk + TK_BINS * TK_THREADS;
+    uint32_t *keys = cand + TK_CAND;
+    __shared__ uint32_t tot[TK_BINS];
+    __shared__ uint32_t sh_prefix, sh_match, sh_ncand;
+    __shared__ int sh_remaining, sh_compacted;
+    __shared__ int sh_gt[TK_WARPS], sh_eq[TK_WARPS];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int q = blockIdx.x;
     const uint64_t pos = (a.n_seq == 1) ? a.pos0 + (uint64_t)q : dp.pos[q];
     const int V = (int)((pos + 1) / 4);
     const int k = a.k;
     int32_t *out = a.topk + (size_t)q * k;
     if (V <= k) {
-        for (int i = threadIdx.x; i < k; i += TK_THREADS) out[i] = (i < V) ? i : -1;
+        for (int i = tid; i < k; i += TK_THREADS) out[i] = (i < V) ? i : -1;
         return;
     }
     const float *s = a.scores + (size_t)q * a.lds;
-    for (int c = threadIdx.x; c < V; c += TK_THREADS) keys[c] = order_key(s[c]);
-    if (threadIdx.x == 0) { sh_prefix = 0; sh_remaining = k; }
+    for (int c = tid; c < V; c += TK_THREADS) keys[c] = order_key(s[c]);
+    if (tid == 0) { sh_prefix = 0; sh_remaining = k; sh_compacted = 0; sh_ncand = 0; }
     __syncthreads();
-    // Radix select, 8 bits per pass from the top: find the key K* of the k-th
-    // largest element; `remaining` = how many elements equal to K* to keep.
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = threadIdx.x; i < 256; i += TK_THREADS) hist[i] = 0;
-        __syncthreads();
+    // Radix select, 4 bits per pass from the top: the key K* of the k-th largest
+    // element and how many elements equal to K* to keep.  Counters are private
+    // to each thread (no atomics); once the keys that still match the resolved
+    // prefix fit in the candidate buffer, later passes scan only those.
+    for (int shift = 28; shift >= 0; shift -= 4) {
+#pragma unroll
+        for (int d = 0; d < TK_BINS; d++) cnt[d * TK_THREADS + tid] = 0;
         const uint32_t prefix = sh_prefix;
-        const uint32_t hmask = (shift == 24) ? 0u : (0xffffffffu << (shift + 8));
-        for (int c = threadIdx.x; c < V; c += TK_THREADS) {
-            const uint32_t key = keys[c];
-            if ((key & hmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        const uint32_t hmask = (shift == 28) ? 0u : (0xffffffffu << (shift + 4));
+        const bool compacted = sh_compacted != 0;
+        const uint32_t *src = compacted ? cand : keys;
+        const int n = compacted ? (int)sh_ncand : V;
+        for (int i = tid; i < n; i += TK_THREADS) {
+            const uint32_t key = src[i];
+            if ((key & hmask) == prefix) cnt[((key >> shift) & 15u) * TK_THREADS + tid] += 1u;
         }
         __syncthreads();
-        if (threadIdx.x == 0) {
+        if (warp < TK_BINS) {
+            uint32_t v = 0;
+            for (int j = lane; j < TK_THREADS; j += 32) v += cnt[warp * TK_THREADS + j];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) tot[warp] = v;
+        }
+        __syncthreads();
+        if (tid == 0) {
             int rem = sh_remaining;
-            int bin = 255;
+            int bin = TK_BINS - 1;
             for (; bin > 0; bin--) {
-                const int h = (int)hist[bin];
+                const int h = (int)tot[bin];
                 if (h >= rem) break;
                 rem -= h;
             }
             sh_prefix = prefix | ((uint32_t)bin << shift);
             sh_remaining = rem;
+            sh_match = tot[bin];
         }
         __syncthreads();
+        if (!compacted && shift > 0 && sh_match <= (uint32_t)TK_CAND) {
+            // collect the keys that match the prefix resolved so far
+            const uint32_t np = sh_prefix, nm = 0xffffffffu << shift;
+            for (int base = warp * 32; base < V; base += TK_THREADS) {
+                const int c = base + lane;
+                const uint32_t key = (c < V) ? keys[c] : 0u;
+                const bool hit = c < V && (key & nm) == np;
+                const unsigned m = __ballot_sync(0xffffffffu, hit);
+                uint32_t off = 0;
+                if (lane == 0 && m) off = atomicAdd(&sh_ncand, (uint32_t)__popc(m));
+                off = __shfl_sync(0xffffffffu, off, 0);
+                if (hit) cand[off + __popc(m & ((1u << lane) - 1u))] = key;
+            }
+            if (tid == 0) sh_compacted = 1;
+            __syncthreads();
+        }
     }
     const uint32_t kstar = sh_prefix;
     const int remaining = sh_remaining;
-    // Ordered compaction: keep key > K*, and the first `remaining` (by index)
-    // of key == K*.
+    // Ordered selection: keep key > K*, and the first `remaining` (by index) of
+    // key == K*.  Each warp owns a contiguous range of indices; one exchange of
+    // per-warp counts gives every warp its output offset.
+    const int per = ((V + TK_WARPS - 1) / TK_WARPS + 31) & ~31;
+    const int w0 = warp * per, w1 = min(V, w0 + per);
+    int gt_w = 0, eq_w = 0;
+    for (int base = w0; base < w1; base += 32) {
+        const int c = base + lane;
+        const uint32_t key = (c < w1) ? keys[c] : 0u;
+        gt_w += __popc(__ballot_sync(0xffffffffu, c < w1 && key > kstar));
+        eq_w += __popc(__ballot_sync(0xffffffffu, c < w1 && key == kstar));
+    }
+    if (lane == 0) { sh_gt[warp] = gt_w; sh_eq[warp] = eq_w; }
+    __syncthreads();
     int eq_run = 0, sel_run = 0;
-    for (int base = 0; base < V; base += TK_THREADS) {
-        const int c = base + threadIdx.x;
-        const uint32_t key = (c < V) ? keys[c] : 0u;
-        const int gt = (c < V) && key > kstar;
-        const int eq = (c < V) && key == kstar;
-        int eq_tot;
-        const int eq_rank = eq_run + block_excl_scan(eq, warp_tot, eq_tot);
-        const int sel = gt || (eq && eq_rank < remaining);
-        int sel_tot;
-        const int slot = sel_run + block_excl_scan(sel, warp_tot, sel_tot);
-        if (sel) out[slot] = c;
-        eq_run += eq_tot;
-        sel_run += sel_tot;
+    for (int w = 0; w < warp; w++) {
+        const int take = max(0, min(sh_eq[w], remaining - eq_run));
+        sel_run += sh_gt[w] + take;
+        eq_run += sh_eq[w];
+    }
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base = w0; base < w1; base += 32) {
+        const int c = base + lane;
+        const uint32_t key = (c < w1) ? keys[c] : 0u;
+        const bool gt = c < w1 && key > kstar;
+        const bool eq = c < w1 && key == kstar;
+        const unsigned eqm = __ballot_sync(0xffffffffu, eq);
+        const int eq_rank = eq_run + __popc(eqm & lt);
+        const bool sel = gt || (eq && eq_rank < remaining);
+        const unsigned selm = __ballot_sync(0xffffffffu, sel);
+        if (sel) out[sel_run + __popc(selm & lt)] = c;
+        eq_run += __popc(eqm);
+        sel_run += __popc(selm);
     }
 }
 
@@ -206,7 +285,7 @@ cudaError_t launch_indexer_prefill(const IndexerArgs &a, cudaStream_t s) {
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    const size_t smem = sizeof(uint32_t) * (size_t)(vis_max > 0 ? vis_max : 1);
+    const size_t smem = TK_FIXED_SMEM + sizeof(uint32_t) * (size_t)(vis_max > 0 ? vis_max : 1);
     cudaError_t e = ensure_dyn_smem(topk_kernel, smem);
     if (e != cudaSuccess) return e;
     DecodePos dp{};
@@ -217,18 +296,22 @@ cudaError_t launch_indexer_prefill(const IndexerArgs &a, cudaStream_t s) {
 cudaError_t launch_indexer_decode(const IndexerArgs &a, const DecodePos &p, cudaStream_t s) {
     uint64_t vis_max = 0;
     for (int b = 0; b < a.n_seq; b++) vis_max = ((p.pos[b] + 1) / 4 > vis_max) ? (p.pos[b] + 1) / 4 : vis_max;
+    cudaError_t e;
     if (vis_max > 0) {
         dim3 grid((unsigned)((vis_max + 127) / 128), (unsigned)a.n_seq);
-        const size_t smem = sizeof(float) * ((size_t)a.d + 128 * ((size_t)a.d + 1));
-        cudaError_t e = ensure_dyn_smem(score_decode_kernel, smem);
-        if (e != cudaSuccess) return e;
-        score_decode_kernel<<<grid, 128, smem, s>>>(a, p);
+        switch (a.d) {
+            case 64: score_decode_kernel<64><<<grid, 128, 0, s>>>(a, p); break;
+            case 128: score_decode_kernel<128><<<grid, 128, 0, s>>>(a, p); break;
+            case 256: score_decode_kernel<256><<<grid, 128, 0, s>>>(a, p); break;
+            case 512: score_decode_kernel<512><<<grid, 128, 0, s>>>(a, p); break;
+            default: return cudaErrorInvalidValue;
+        }
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    const size_t smem = sizeof(uint32_t) * (size_t)(vis_max > 0 ? vis_max : 1);
-    cudaError_t e2 = ensure_dyn_smem(topk_kernel, smem);
-    if (e2 != cudaSuccess) return e2;
+    const size_t smem = TK_FIXED_SMEM + sizeof(uint32_t) * (size_t)(vis_max > 0 ? vis_max : 1);
+    e = ensure_dyn_smem(topk_kernel, smem);
+    if (e != cudaSuccess) return e;
     topk_kernel<<<a.n_seq, TK_THREADS, smem, s>>>(a, p);
     return cudaGetLastError();
 }

@@ -64,7 +64,7 @@ enum { DS4C_F32 = 0, DS4C_BF16 = 1 };
  * Supported: ratio in {0,4,128}; head_dim and idx_head_dim in {64,128,256,512};
  * n_rot a multiple of 4, 4 <= n_rot <= min(head_dim, idx_head_dim), at most 128;
  * d_model a multiple of 8; n_heads a multiple of 8, at most 128;
- * 1 <= swa <= 1024; 1 <= top_k <= 2048; idx_cap <= 53248. */
+ * 1 <= swa <= 1024; 1 <= top_k <= 2048; idx_cap <= 40960. */
 typedef struct {
     uint32_t d_model;       /* hidden width fed to the projections */
     uint32_t head_dim;      /* D: width of a raw / compressed attention row (K = V = the row) */

@@ -20,7 +20,9 @@ def _gpu():
 @pytest.mark.parametrize("dtype,d_model,T,D,d", [
     ("bf16", 512, 300, 512, 128),      # ragged M, 2 n-tiles per kv matrix
     ("bf16", 4096, 4096, 512, 128),    # full chunk of the long-context layer
-    ("bf16", 4096, 64, 512, 128),      # smallest M on the tensor-core path
+    ("bf16", 4096, 64, 512, 128),      # narrow-tile tensor-core path
+    ("bf16", 4096, 32, 512, 128),      # decode batch of 32 sequences
+    ("bf16", 512, 1, 512, 128),        # a single row
     ("f32", 256, 64, 128, 64),         # fp32 throughout: CUDA-core path
 ])
 def test_projection_matches_matmul(dtype, d_model, T, D, d):
