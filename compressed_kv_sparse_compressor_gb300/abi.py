@@ -26,7 +26,9 @@ EXPORTS = (
     "ds4c_workspace_bytes", "ds4c_state_init", "ds4c_compress_prefill", "ds4c_compress_decode_step",
     "ds4c_indexer_topk", "ds4c_sparse_swa_attn", "ds4c_checkpoint_floats", "ds4c_checkpoint_gather",
     "ds4c_sync_status", "ds4c_status_string", "ds4c_last_cuda_error", "ds4c_attn_uses_tensor_cores",
+    "ds4c_indexer_topk_noalloc",
 )
+NOALLOC_SCORE_FLOATS = 2 * 1024 * 1024
 
 
 class Ds4cError(RuntimeError):
@@ -81,6 +83,7 @@ def lib() -> C.CDLL:
         "ds4c_compress_decode_step": (st, [cfgp, lwp, lwp, lsp, P, C.POINTER(U64), U32, P, SZ, P]),
         "ds4c_indexer_topk": (st, [cfgp, lsp, P, C.POINTER(U64), U32, U32, P, P, SZ, P, SZ, P]),
         "ds4c_sparse_swa_attn": (st, [cfgp, lsp, P, P, P, C.POINTER(U64), U32, U32, P, C.c_int, P, SZ, P]),
+        "ds4c_indexer_topk_noalloc": (st, [cfgp, lsp, P, C.POINTER(U64), U32, U32, P, P]),
         "ds4c_checkpoint_floats": (SZ, [cfgp, U64]),
         "ds4c_checkpoint_gather": (st, [cfgp, lsp, U32, U64, P, SZ, C.POINTER(SZ), P]),
         "ds4c_sync_status": (st, [P]),
@@ -139,6 +142,10 @@ def ds4c_compress_decode_step(cfg, attn_w, idx_w, state, hidden, pos_h, n_seq, w
 def ds4c_indexer_topk(cfg, state, q_idx, pos_h, n_seq, n_tok, topk, scores, score_stride, ws, ws_bytes, stream):
     return lib().ds4c_indexer_topk(C.byref(cfg), C.byref(state), q_idx, pos_h, n_seq, n_tok, topk, scores,
                                    score_stride, ws, ws_bytes, stream)
+
+
+def ds4c_indexer_topk_noalloc(cfg, state, q_idx, pos_h, n_seq, n_tok, topk, stream):
+    return lib().ds4c_indexer_topk_noalloc(C.byref(cfg), C.byref(state), q_idx, pos_h, n_seq, n_tok, topk, stream)
 
 
 def ds4c_sparse_swa_attn(cfg, state, q, raw_new, topk, pos_h, n_seq, n_tok, out, commit_ring, ws, ws_bytes, stream):

@@ -635,7 +635,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             for (int off = tid * 128; off < H * D * 4; off += 128 * 128)
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(base + off));
         };
-        uint32_t g = 0, tok = 0, sphase = 0;
+        uint32_t g = 0, sphase = 0;
         bool ok = true;
         // barrier of the 128 softmax threads on an mbarrier, so that its wait is bounded
         auto soft_bar = [&]() -> bool {

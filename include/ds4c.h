@@ -195,6 +195,34 @@ DS4C_API ds4c_status ds4c_sparse_swa_attn(const ds4c_layer_cfg *cfg, const ds4c_
                                  float *out, int commit_ring, void *ws, size_t ws_bytes,
                                  cudaStream_t stream);
 
+/* Score capacity of ds4c_indexer_topk_noalloc: 2M floats (8 MiB). */
+#define DS4C_NOALLOC_SCORE_FLOATS (2u * 1024u * 1024u)
+
+/* ds4c_indexer_topk for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this is a deployment variant of the indexer call.
+ * Some callers cannot call cudaMalloc or hand over a workspace: runtimes that
+ * own all device memory through their own pool and forbid allocation on the
+ * serving path (an allocation can synchronise the device or fragment the
+ * pool), or code running where no allocator is reachable.  This call takes
+ * the same arguments and gives the same result as ds4c_indexer_topk with
+ * scores = NULL, but keeps its score matrix in a fixed file-scope device array
+ * of DS4C_NOALLOC_SCORE_FLOATS floats instead of the caller's workspace.
+ *   - Limit: n_seq * n_tok * round_up((last query position + 1) / 4, 4) must not
+ *     exceed DS4C_NOALLOC_SCORE_FLOATS, otherwise DS4C_ERR_CAPACITY and nothing
+ *     is launched (e.g. a 32-sequence decode step at 65536 context fits; a
+ *     4096-token prefill chunk at 131072 context does not).
+ *   - The array exists on every GPU that loads the library, until the process
+ *     exits.  The first call on a device looks up the array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture.
+ *   - Every call shares the array: calls whose kernels overlap on the GPU (on
+ *     streams without ordering between them) race on it.  A call reads only
+ *     scores it wrote itself, so no part of the array needs clearing.
+ *   - It allocates nothing and calls no allocating library routine. */
+DS4C_API ds4c_status ds4c_indexer_topk_noalloc(const ds4c_layer_cfg *cfg, const ds4c_layer_state *state,
+                                               const float *q_idx, const uint64_t *pos_h, uint32_t n_seq,
+                                               uint32_t n_tok, int32_t *topk, cudaStream_t stream);
+
 /* Floats of one sequence's checkpoint after pos tokens:
  *   min(pos, swa)*D + [ratio != 0] ((pos/ratio)*D + 2*(coff*ratio)*(coff*D))
  *   + [ratio == 4] ((pos/4)*d + 2*8*(2d)). */
