@@ -59,11 +59,12 @@ template <int H, int D>
 struct L {
     static constexpr int DC = D / 64;
     static constexpr int DB = D / 128;
-    static constexpr int QB = DC * H * 128;            // bytes of Q hi (or lo)
+    // Q: chunk c (64 d) at OFF_Q + c * QCH holds the fp32 box [H][64] as the
+    // TMA lands it, then in place its bf16 split: hi [H][64] at +0, lo at +QCH/2
+    static constexpr int QCH = H * 64 * 4;
     static constexpr int PB = ROWS * H * 2;            // bytes of P hi (or lo)
-    static constexpr int OFF_QHI = 0;
-    static constexpr int OFF_QLO = OFF_QHI + QB;
-    static constexpr int OFF_X = OFF_QLO + QB;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_X = OFF_Q + DC * QCH;
     static constexpr int OFF_PHI = OFF_X + RING * PAIR;
     static constexpr int OFF_PLO = OFF_PHI + PB;
     static constexpr int OFF_ONES = OFF_PLO + PB;
@@ -73,7 +74,7 @@ struct L {
     static constexpr int OFF_ALPHA = OFF_MREF + 4 * H;
     static constexpr int OFF_FLAG = OFF_ALPHA + 4 * H;
     static constexpr int OFF_BAR = OFF_FLAG + 64;
-    static constexpr int N_BAR = 2 * RING + 9;
+    static constexpr int N_BAR = 2 * RING + 10;
     static constexpr int SMEM = OFF_BAR + 8 * N_BAR + 16 + 1024;
     // TMEM columns
     static constexpr int T_S = 0;                      // two S^T buffers of H columns
@@ -82,11 +83,12 @@ struct L {
     static constexpr int T_COLS = 512;
     static_assert(T_L + H <= T_COLS, "tensor memory");
     static_assert(SMEM <= 232448, "shared memory");
+    static_assert(PB == 64 * H * 4, "an output staging box [H][64] fp32 fills P hi (or lo)");
 };
 
 // barrier indices
 enum { B_FULL = 0, B_EMPTY = RING, B_QREADY = 2 * RING, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1, B_PFULL, B_PVDONE,
-       B_OFREE, B_SOFT };
+       B_OFREE, B_SOFT, B_QLOAD };
 
 struct TcAttnParams {
     float *out;
@@ -152,6 +154,18 @@ __device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap *map, in
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
+
+// shared -> global tensor store of one box, tracked by the issuing thread's bulk groups
+__device__ __forceinline__ void tma_store_box(const CUtensorMap *map, int x, int y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared-memory sources of this thread's committed stores have been read
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Shared-memory matrix descriptor (tcgen05): start, leading / stride byte
 // offsets, version 1, layout (0 = no swizzle, 2 = 128-byte swizzle).
@@ -333,9 +347,22 @@ __device__ __forceinline__ Item item_tiles(const TcAttnParams &p, int it, int n_
     return r;
 }
 
+// Next work item of this CTA at or after `it` that has rows (n_items when
+// none).  The whole warp calls this.
+__device__ __forceinline__ int next_item(const TcAttnParams &p, int it, int n_items) {
+    for (; it < n_items; it += gridDim.x) {
+        const Tok kk = token_geom(p, it / p.parts);
+        const int ncc = comp_rows(p, kk, nullptr);
+        const Item ii = item_tiles(p, it, 1 + (ncc + ROWS - 1) / ROWS);
+        if (ii.tb < ii.te) return it;
+    }
+    return n_items;
+}
+
 template <int H, int D>
 __global__ void __launch_bounds__(THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant__ CUtensorMap rawLo,
+               const __grid_constant__ CUtensorMap qMap, const __grid_constant__ CUtensorMap oMap,
                const TcAttnParams p) {
     using Lay = L<H, D>;
     extern __shared__ uint8_t smem_raw[];
@@ -365,6 +392,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         mbar_init(bar(B_PVDONE), 1);
         mbar_init(bar(B_OFREE), 128);
         mbar_init(bar(B_SOFT), 128);
+        mbar_init(bar(B_QLOAD), 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -482,9 +510,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         constexpr uint32_t ID_QK = idesc(128, H, 0, 0);
         constexpr uint32_t ID_PV = idesc(128, H, 1, 1);
         constexpr uint32_t ID_L = idesc(128, H, 0, 1);
-        const uint32_t qhi = smem_u32(sm + Lay::OFF_QHI), qlo = smem_u32(sm + Lay::OFF_QLO);
+        const uint32_t qs = smem_u32(sm + Lay::OFF_Q);
         const uint32_t phi = smem_u32(sm + Lay::OFF_PHI), plo = smem_u32(sm + Lay::OFF_PLO);
         const uint32_t ones = smem_u32(sm + Lay::OFF_ONES);
+        // fp32 Q of query n into the Q chunks (lane 0; the Q buffer is free)
+        auto issue_q = [&](int n) {
+            mbar_expect_tx(bar(B_QLOAD), Lay::DC * Lay::QCH);
+            for (int c = 0; c < Lay::DC; c++) tma_box(qs + c * Lay::QCH, &qMap, 64 * c, n * H, bar(B_QLOAD));
+        };
         uint32_t unit = 0, g = 0, tok = 0;
         bool ok = true;
         // unit u of the ring: wait until loaded / hand back once its MMAs finish
@@ -507,8 +540,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                 fence_after();
                 for (int kk = 0; kk < 4; kk++) {
                     const uint64_t ah = make_desc(xh + kk * 32, 16, 1024, 2);
-                    const uint64_t bh = make_desc(qhi + c * (H * 128) + kk * 32, 16, 1024, 2);
-                    const uint64_t bl = make_desc(qlo + c * (H * 128) + kk * 32, 16, 1024, 2);
+                    const uint64_t bh = make_desc(qs + c * Lay::QCH + kk * 32, 16, 1024, 2);
+                    const uint64_t bl = make_desc(qs + c * Lay::QCH + Lay::QCH / 2 + kk * 32, 16, 1024, 2);
                     mma(d_t, ah, bh, ID_QK, (c > 0 || kk > 0) ? 1u : 0u);
                     mma(d_t, ah, bl, ID_QK, 1u);
                     if (has_lo) mma(d_t, make_desc(xl + kk * 32, 16, 1024, 2), bh, ID_QK, 1u);
@@ -557,11 +590,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             return true;
         };
         const int n_items = p.n_q * p.parts;
+        {
+            const int first = next_item(p, blockIdx.x, n_items);
+            if (lane == 0 && first < n_items) issue_q(first / p.parts);
+        }
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const Tok k = token_geom(p, it / p.parts);
             const int nc = comp_rows(p, k, nullptr);          // whole warp
             const Item itm = item_tiles(p, it, 1 + (nc + ROWS - 1) / ROWS);
             if (itm.tb >= itm.te) continue;
+            const int nx = next_item(p, it + gridDim.x, n_items);
             int good = 1;
             if (lane == 0) {
                 good = mbar_wait(bar(B_QREADY), tok & 1, abort) ? 1 : 0;
@@ -573,6 +611,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                     const uint32_t gi = g + (i - itm.tb);
                     if (i + 1 < itm.te && !do_qk(gi + 1, i + 1)) { good = 0; break; }
                     if (!mbar_wait(bar(B_PFULL), gi & 1, abort)) { good = 0; break; }
+                    // every S of this item has been read, so its Q MMAs are complete: load the next Q
+                    if (i == itm.te - 1 && nx < n_items) issue_q(nx / p.parts);
                     if (i == itm.tb && tok > 0 && !mbar_wait(bar(B_OFREE), (tok - 1) & 1, abort)) { good = 0; break; }
                     fence_after();
                     if (!do_pv(i, i == itm.tb)) { good = 0; break; }
@@ -590,52 +630,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         const int q4 = warp & 3;                 // TMEM lane quarter
         const int r = q4 * 32 + lane;            // tile row / d within a block
         const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
-        const uint32_t qhi = smem_u32(sm + Lay::OFF_QHI), qlo = smem_u32(sm + Lay::OFF_QLO);
         uint8_t *phi_p = sm + Lay::OFF_PHI;
         uint8_t *plo_p = sm + Lay::OFF_PLO;
         const int tid = threadIdx.x - 64;        // 0..127
-        (void)qhi;
-        (void)qlo;
-        auto load_q = [&](int n) {
-            // 16 independent 16-byte loads in flight per thread, then split and store
-            const float4 *qs = reinterpret_cast<const float4 *>(p.q + (size_t)n * H * D);
-            constexpr int NF = H * D / 4;
-            for (int f0 = tid; f0 < NF; f0 += 128 * 16) {
-                float4 vv[16];
-#pragma unroll
-                for (int u = 0; u < 16; u++) {
-                    const int f = f0 + 128 * u;
-                    vv[u] = (f < NF) ? __ldg(qs + f) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-                for (int u = 0; u < 16; u++) {
-                    const int f = f0 + 128 * u;
-                    if (f >= NF) break;
-                    const float4 v = vv[u];
-                    const int h = f / (D / 4);
-                    const int d = (f % (D / 4)) * 4;
-                    const int c = d / 64, e = d % 64;
-                    const int unit16 = (e / 8) ^ (h & 7);
-                    const int off = c * (H * 128) + h * 128 + unit16 * 16 + (e % 8) * 2;
-                    float h0, l0, h1, l1, h2, l2, h3, l3;
-                    split_bf16(v.x, h0, l0);
-                    split_bf16(v.y, h1, l1);
-                    split_bf16(v.z, h2, l2);
-                    split_bf16(v.w, h3, l3);
-                    *reinterpret_cast<uint2 *>(sm + Lay::OFF_QHI + off) = make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3));
-                    *reinterpret_cast<uint2 *>(sm + Lay::OFF_QLO + off) = make_uint2(pack_bf16x2(l0, l1), pack_bf16x2(l2, l3));
-                }
-            }
-            fence_proxy_async();
-            mbar_arrive(bar(B_QREADY));
-        };
-        // bring a later query's Q into L2 while this one is processed
-        auto prefetch_q = [&](int n) {
-            const char *base = reinterpret_cast<const char *>(p.q + (size_t)n * H * D);
-            for (int off = tid * 128; off < H * D * 4; off += 128 * 128)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(base + off));
-        };
-        uint32_t g = 0, sphase = 0;
+        uint32_t g = 0, sphase = 0, qph = 0;
         bool ok = true;
         // barrier of the 128 softmax threads on an mbarrier, so that its wait is bounded
         auto soft_bar = [&]() -> bool {
@@ -644,24 +642,41 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             sphase ^= 1;
             return r_;
         };
-        const int n_items = p.n_q * p.parts;
-        // next non-empty item of this CTA at or after `it` (n_items when none)
-        auto next_item = [&](int it) -> int {
-            for (; it < n_items; it += gridDim.x) {
-                const Tok kk = token_geom(p, it / p.parts);
-                const int ncc = comp_rows(p, kk, nullptr);
-                const Item ii = item_tiles(p, it, 1 + (ncc + ROWS - 1) / ROWS);
-                if (ii.tb < ii.te) return it;
+        // Q split: once the fp32 boxes have landed, each 64-d chunk [H][64] fp32
+        // is rewritten in place as its bf16 hi (K-major, 128-byte swizzle) and lo
+        // halves, one chunk per round (all reads of a round before its writes).
+        auto split_q = [&]() -> bool {
+            if (!mbar_wait(bar(B_QLOAD), qph, abort)) return false;
+            qph ^= 1;
+            constexpr int PER = H * 64 / 4 / 128;          // float4 per thread per chunk
+            for (int c = 0; c < Lay::DC; c++) {
+                uint8_t *qc = sm + Lay::OFF_Q + c * Lay::QCH;
+                float4 v[PER];
+#pragma unroll
+                for (int j = 0; j < PER; j++) v[j] = *reinterpret_cast<const float4 *>(qc + (j * 128 + tid) * 16);
+                if (!soft_bar()) return false;
+#pragma unroll
+                for (int j = 0; j < PER; j++) {
+                    const int f = j * 128 + tid;
+                    const int h = f / 16, d = (f % 16) * 4;
+                    const int off = h * 128 + (((d / 8) ^ (h & 7)) * 16) + (d % 8) * 2;
+                    float h0, l0, h1, l1, h2, l2, h3, l3;
+                    split_bf16(v[j].x, h0, l0);
+                    split_bf16(v[j].y, h1, l1);
+                    split_bf16(v[j].z, h2, l2);
+                    split_bf16(v[j].w, h3, l3);
+                    *reinterpret_cast<uint2 *>(qc + off) = make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3));
+                    *reinterpret_cast<uint2 *>(qc + off + Lay::QCH / 2) = make_uint2(pack_bf16x2(l0, l1), pack_bf16x2(l2, l3));
+                }
             }
-            return n_items;
+            fence_proxy_async();
+            mbar_arrive(bar(B_QREADY));
+            return true;
         };
-        {
-            const int first = next_item(blockIdx.x);
-            if (first < n_items) load_q(first / p.parts);
-        }
+        const int n_items = p.n_q * p.parts;
+        if (next_item(p, blockIdx.x, n_items) < n_items && !split_q()) ok = false;
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const int n = it / p.parts;
-            if (it + gridDim.x < n_items && (it + gridDim.x) / p.parts != n) prefetch_q((it + gridDim.x) / p.parts);
             const Tok k = token_geom(p, n);
             const int nc = comp_rows(p, k, nullptr);
             const Item itm = item_tiles(p, it, 1 + (nc + ROWS - 1) / ROWS);
@@ -698,14 +713,32 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                                  flags[(g & 1) * 4 + 3];
                 bool waited = false;
                 if (any) {
-                    // exact tile maximum per head, then the new reference and the rescale factors
+                    // exact tile maximum per head, then the new reference and the rescale factors.
+                    // Warp maximum by a transposing butterfly: at offset o each lane keeps the
+                    // half of its heads selected by lane bit o and takes the partner's maxima for
+                    // it, so after the five steps lane l holds heads 2l and 2l + 1.
+                    static_assert(H == 64, "the butterfly below assumes 64 heads");
+                    float m[H / 2];
+                    {
+                        const bool up = (lane & 16) != 0;
 #pragma unroll
-                    for (int h = 0; h < H; h++) {
-                        float v = s[h];
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-                        if (lane == 0) red[q4 * H + h] = v;
+                        for (int k = 0; k < H / 2; k++) {
+                            const float send = up ? s[k] : s[k + H / 2];
+                            const float keep = up ? s[k + H / 2] : s[k];
+                            m[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+                        }
                     }
+#pragma unroll
+                    for (int o = 8; o > 0; o >>= 1) {
+                        const bool up = (lane & o) != 0;
+#pragma unroll
+                        for (int k = 0; k < 2 * o; k++) {
+                            const float send = up ? m[k] : m[k + 2 * o];
+                            const float keep = up ? m[k + 2 * o] : m[k];
+                            m[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+                        }
+                    }
+                    *reinterpret_cast<float2 *>(red + q4 * H + 2 * lane) = make_float2(m[0], m[1]);
                     if (!soft_bar()) { ok = false; break; }
                     if (tid < H) {
                         const float mt = fmaxf(fmaxf(red[tid], red[H + tid]), fmaxf(red[2 * H + tid], red[3 * H + tid]));
@@ -754,20 +787,43 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                 fence_proxy_async();
                 mbar_arrive(bar(B_PFULL));
                 if (i == itm.te - 1) {
-                    // the last S of this item has been read: Q is free for the next item
-                    const int nx = next_item(it + gridDim.x);
-                    if (nx < n_items) load_q(nx / p.parts);
+                    // the last S of this item has been read: split the next item's Q
+                    const int nx = next_item(p, it + gridDim.x, n_items);
+                    if (nx < n_items && !split_q()) { ok = false; break; }
                     if (!mbar_wait(bar(B_PVDONE), g & 1, abort)) { ok = false; break; }
                     fence_after();
                     float l[H], v[H];
                     tmem_load<H>(lane_base + Lay::T_L, l);
                     if (p.parts == 1) {
-                        float *o = p.out + (size_t)n * H * D;
+                        // out[n][h][128 j + r] = O / L through two staging boxes [H][64] fp32 in
+                        // the P buffers (rows r < 64 at P hi, r >= 64 at P lo), stored by TMA
+                        float *stg = reinterpret_cast<float *>(phi_p + (r >> 6) * Lay::PB);
+                        const int rr = r & 63;
+#pragma unroll
+                        for (int h = 0; h < H; h++) l[h] = 1.0f / l[h];
                         for (int j = 0; j < Lay::DB; j++) {
                             tmem_load<H>(lane_base + Lay::T_O + j * H, v);
+                            if (j == Lay::DB - 1) {
+                                fence_before();
+                                mbar_arrive(bar(B_OFREE));
+                            }
+                            if (j > 0) {
+                                if (tid == 0) bulk_wait_read();
+                                if (!soft_bar()) { ok = false; break; }
+                            }
 #pragma unroll
-                            for (int h = 0; h < H; h++) o[(size_t)h * D + 128 * j + r] = v[h] / l[h];
+                            for (int h = 0; h < H; h++) stg[h * 64 + rr] = v[h] * l[h];
+                            fence_proxy_async();
+                            if (!soft_bar()) { ok = false; break; }
+                            if (tid == 0) {
+                                tma_store_box(&oMap, 128 * j, n * H, smem_u32(phi_p));
+                                tma_store_box(&oMap, 128 * j + 64, n * H, smem_u32(plo_p));
+                                bulk_commit();
+                            }
                         }
+                        if (!ok) break;
+                        // the next P writes reuse the staging boxes
+                        if (tid == 0) bulk_wait_read();
                     } else {
                         float *o = p.part_o + (size_t)it * H * D;
                         for (int j = 0; j < Lay::DB; j++) {
@@ -782,13 +838,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                             p.part_ml[(size_t)it * 2 * H + tid] = mref_s[tid];
                             p.part_ml[(size_t)it * 2 * H + H + tid] = lt;
                         }
+                        fence_before();
+                        mbar_arrive(bar(B_OFREE));
                     }
-                    fence_before();
-                    mbar_arrive(bar(B_OFREE));
                 }
             }
         }
     }
+    if (threadIdx.x == 64) bulk_wait_all();
     __syncthreads();
     if (warp == 1) {
         fence_after();
@@ -887,6 +944,19 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, int D, uint64_t p
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D fp32 map over a dense [rows][D] array, boxes of 64 x box_rows, no swizzle.
+bool make_map_f32(CUtensorMap *m, const float *base, uint64_t rows, int D, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 4};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
     static int n = 0;
     if (n == 0) {
@@ -907,12 +977,16 @@ cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, cudaStream_t s
     const uint64_t pitch = (uint64_t)2 * D * 2;
     if (!make_map(&rh, a.raw_mirror, raw_rows, D, pitch, 64) || !make_map(&rl, a.raw_mirror + D, raw_rows, D, pitch, 64))
         return cudaErrorNotSupported;
+    // Q in and out, both [n_q * H][D] fp32, one 64 x H box per 64-d chunk
+    const uint64_t qrows = (uint64_t)a.n_seq * a.n_tok * H;
+    CUtensorMap qm, om;
+    if (!make_map_f32(&qm, a.q, qrows, D, H) || !make_map_f32(&om, a.out, qrows, D, H)) return cudaErrorNotSupported;
     (void)comp_rows_total;
     cudaError_t e = ensure_dyn_smem(attn_tc_kernel<H, D>, Lay::SMEM);
     if (e != cudaSuccess) return e;
     const int items = a.n_seq * a.n_tok * p.parts;
     const int grid = items < sm_count() ? items : sm_count();
-    attn_tc_kernel<H, D><<<grid, THREADS, Lay::SMEM, s>>>(rh, rl, p);
+    attn_tc_kernel<H, D><<<grid, THREADS, Lay::SMEM, s>>>(rh, rl, qm, om, p);
     e = cudaGetLastError();
     if (e != cudaSuccess || p.parts == 1) return e;
     attn_combine_kernel<<<a.n_seq * a.n_tok * H, 128, 0, s>>>(a.out, p.part_o, p.part_ml, H, D, p.parts);
