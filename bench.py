@@ -189,8 +189,9 @@ class Prefill:
             self.events = ev
 
     def launches_per_step(self):
-        # state init: 5 fills; per chunk: GEMM 1, pool 2, commit 2, score 1, top-k 1, attention 1, ring 1
-        return 5 + 9 * self.n_chunks + 1
+        # state init: 5 fills; per chunk: GEMM 1, pool 2, commit 2, score 1, top-k 1, raw mirror 1,
+        # attention 1, ring 1; then the gather
+        return 5 + 10 * self.n_chunks + 1
 
     def breakdown(self):
         """Per-call device time (ms) of the last timed step."""

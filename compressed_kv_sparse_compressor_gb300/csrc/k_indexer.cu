@@ -9,7 +9,7 @@
 // blocked SIMT "GEMM" whose per-element k loop stays sequential.
 //
 // Top-k: radix select on order-preserving 32-bit keys (one CTA per query,
-// keys resident in shared memory), then an ordered compaction that emits the
+// the keys re-read from the score row each pass), then an ordered compaction that emits the
 // selected indices in ascending order, ties at the threshold broken toward
 // the lower index.
 #include "ds4c_internal.cuh"
@@ -143,9 +143,14 @@ __global__ void __launch_bounds__(128) score_decode_kernel(IndexerArgs a, Decode
 }
 
 // ---------------------------------------------------------------------------
-// K5 top-k.
+// K5 top-k, one CTA per query, in two forms.  Prefill (thousands of queries):
+// 256 threads, the scores stay in global memory (each pass re-reads the row:
+// the first read comes from HBM, the later ones hit L2), so a CTA holds only
+// its counters and candidate buffer (32 KB) and several CTAs share an SM,
+// hiding each other's barrier and scan latencies.  Decode (one query per
+// sequence, a few dozen CTAs): 1024 threads with the row's keys resident in
+// shared memory, so each pass is short.
 // ---------------------------------------------------------------------------
-constexpr int TK_THREADS = 512;
 
 __device__ __forceinline__ uint32_t order_key(float s) {
     uint32_t u = __float_as_uint(s + 0.0f);          // -0 -> +0
@@ -154,15 +159,19 @@ __device__ __forceinline__ uint32_t order_key(float s) {
 
 constexpr int TK_BINS = 16;          // 4-bit radix digits, 8 passes
 constexpr int TK_CAND = 4096;        // survivors are compacted once they fit here
-constexpr int TK_WARPS = TK_THREADS / 32;
-// dynamic shared memory: counters [16][512] | candidates [4096] | keys [V]
-constexpr size_t TK_FIXED_SMEM = sizeof(uint32_t) * (TK_BINS * TK_THREADS + TK_CAND);
+constexpr int TK_UNR = 4;            // independent score loads in flight per thread
+// dynamic shared memory: counters [16][threads] | candidates [4096] | (resident keys [V])
+template <int TK_THREADS>
+constexpr size_t tk_fixed_smem() { return sizeof(uint32_t) * (TK_BINS * TK_THREADS + TK_CAND); }
+constexpr int TK_PREFILL = 256, TK_DECODE = 1024;
 
+template <int TK_THREADS, bool RESIDENT>
 __global__ void __launch_bounds__(TK_THREADS) topk_kernel(IndexerArgs a, DecodePos dp) {
+    constexpr int TK_WARPS = TK_THREADS / 32;
     extern __shared__ uint32_t sm_tk[];
-    uint32_t *cnt = sm_tk;                              // cnt[bin * 512 + tid], private per thread
+    uint32_t *cnt = sm_tk;                              // cnt[bin * threads + tid], private per thread
     uint32_t *cand = sm_tk + TK_BINS * TK_THREADS;
-    uint32_t *keys = cand + TK_CAND;
+    uint32_t *keys = cand + TK_CAND;                    // RESIDENT only
     __shared__ uint32_t tot[TK_BINS];
     __shared__ uint32_t sh_prefix, sh_match, sh_ncand;
     __shared__ int sh_remaining, sh_compacted;
@@ -178,7 +187,23 @@ __global__ void __launch_bounds__(TK_THREADS) topk_kernel(IndexerArgs a, DecodeP
         return;
     }
     const float *s = a.scores + (size_t)q * a.lds;
-    for (int c = tid; c < V; c += TK_THREADS) keys[c] = order_key(s[c]);
+    if (RESIDENT) {
+        for (int base = 0; base < V; base += TK_THREADS * TK_UNR) {
+            float v[TK_UNR];
+#pragma unroll
+            for (int u = 0; u < TK_UNR; u++) {
+                const int i = base + u * TK_THREADS + tid;
+                if (i < V) v[u] = __ldcs(s + i);
+            }
+#pragma unroll
+            for (int u = 0; u < TK_UNR; u++) {
+                const int i = base + u * TK_THREADS + tid;
+                if (i < V) keys[i] = order_key(v[u]);
+            }
+        }
+    }
+    // key of visible row i
+    auto key_at = [&](int i) -> uint32_t { return RESIDENT ? keys[i] : order_key(__ldg(s + i)); };
     if (tid == 0) { sh_prefix = 0; sh_remaining = k; sh_compacted = 0; sh_ncand = 0; }
     __syncthreads();
     // Radix select, 4 bits per pass from the top: the key K* of the k-th largest
@@ -190,20 +215,34 @@ __global__ void __launch_bounds__(TK_THREADS) topk_kernel(IndexerArgs a, DecodeP
         for (int d = 0; d < TK_BINS; d++) cnt[d * TK_THREADS + tid] = 0;
         const uint32_t prefix = sh_prefix;
         const uint32_t hmask = (shift == 28) ? 0u : (0xffffffffu << (shift + 4));
-        const bool compacted = sh_compacted != 0;
-        const uint32_t *src = compacted ? cand : keys;
-        const int n = compacted ? (int)sh_ncand : V;
-        for (int i = tid; i < n; i += TK_THREADS) {
-            const uint32_t key = src[i];
-            if ((key & hmask) == prefix) cnt[((key >> shift) & 15u) * TK_THREADS + tid] += 1u;
+        if (sh_compacted) {
+            const int n = (int)sh_ncand;
+            for (int i = tid; i < n; i += TK_THREADS) {
+                const uint32_t key = cand[i];
+                if ((key & hmask) == prefix) cnt[((key >> shift) & 15u) * TK_THREADS + tid] += 1u;
+            }
+        } else {
+            for (int base = 0; base < V; base += TK_THREADS * TK_UNR) {
+                uint32_t kv[TK_UNR];
+#pragma unroll
+                for (int u = 0; u < TK_UNR; u++) {
+                    const int i = base + u * TK_THREADS + tid;
+                    kv[u] = (i < V) ? key_at(i) : 0u;
+                }
+#pragma unroll
+                for (int u = 0; u < TK_UNR; u++) {
+                    const int i = base + u * TK_THREADS + tid;
+                    if (i < V && (kv[u] & hmask) == prefix) cnt[((kv[u] >> shift) & 15u) * TK_THREADS + tid] += 1u;
+                }
+            }
         }
         __syncthreads();
-        if (warp < TK_BINS) {
+        for (int bin = warp; bin < TK_BINS; bin += TK_WARPS) {
             uint32_t v = 0;
-            for (int j = lane; j < TK_THREADS; j += 32) v += cnt[warp * TK_THREADS + j];
+            for (int j = lane; j < TK_THREADS; j += 32) v += cnt[bin * TK_THREADS + j];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane == 0) tot[warp] = v;
+            if (lane == 0) tot[bin] = v;
         }
         __syncthreads();
         if (tid == 0) {
@@ -219,12 +258,12 @@ __global__ void __launch_bounds__(TK_THREADS) topk_kernel(IndexerArgs a, DecodeP
             sh_match = tot[bin];
         }
         __syncthreads();
-        if (!compacted && shift > 0 && sh_match <= (uint32_t)TK_CAND) {
+        if (!sh_compacted && shift > 0 && sh_match <= (uint32_t)TK_CAND) {
             // collect the keys that match the prefix resolved so far
             const uint32_t np = sh_prefix, nm = 0xffffffffu << shift;
             for (int base = warp * 32; base < V; base += TK_THREADS) {
                 const int c = base + lane;
-                const uint32_t key = (c < V) ? keys[c] : 0u;
+                const uint32_t key = (c < V) ? key_at(c) : 0u;
                 const bool hit = c < V && (key & nm) == np;
                 const unsigned m = __ballot_sync(0xffffffffu, hit);
                 uint32_t off = 0;
@@ -232,6 +271,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_kernel(IndexerArgs a, DecodeP
                 off = __shfl_sync(0xffffffffu, off, 0);
                 if (hit) cand[off + __popc(m & ((1u << lane) - 1u))] = key;
             }
+            __syncthreads();
             if (tid == 0) sh_compacted = 1;
             __syncthreads();
         }
@@ -246,7 +286,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_kernel(IndexerArgs a, DecodeP
     int gt_w = 0, eq_w = 0;
     for (int base = w0; base < w1; base += 32) {
         const int c = base + lane;
-        const uint32_t key = (c < w1) ? keys[c] : 0u;
+        const uint32_t key = (c < w1) ? key_at(c) : 0u;
         gt_w += __popc(__ballot_sync(0xffffffffu, c < w1 && key > kstar));
         eq_w += __popc(__ballot_sync(0xffffffffu, c < w1 && key == kstar));
     }
@@ -261,7 +301,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_kernel(IndexerArgs a, DecodeP
     const unsigned lt = (1u << lane) - 1u;
     for (int base = w0; base < w1; base += 32) {
         const int c = base + lane;
-        const uint32_t key = (c < w1) ? keys[c] : 0u;
+        const uint32_t key = (c < w1) ? key_at(c) : 0u;
         const bool gt = c < w1 && key > kstar;
         const bool eq = c < w1 && key == kstar;
         const unsigned eqm = __ballot_sync(0xffffffffu, eq);
@@ -285,11 +325,11 @@ cudaError_t launch_indexer_prefill(const IndexerArgs &a, cudaStream_t s) {
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    const size_t smem = TK_FIXED_SMEM + sizeof(uint32_t) * (size_t)(vis_max > 0 ? vis_max : 1);
-    cudaError_t e = ensure_dyn_smem(topk_kernel, smem);
+    constexpr size_t smem = tk_fixed_smem<TK_PREFILL>();
+    cudaError_t e = ensure_dyn_smem(topk_kernel<TK_PREFILL, false>, smem);
     if (e != cudaSuccess) return e;
     DecodePos dp{};
-    topk_kernel<<<a.n_tok, TK_THREADS, smem, s>>>(a, dp);
+    topk_kernel<TK_PREFILL, false><<<a.n_tok, TK_PREFILL, smem, s>>>(a, dp);
     return cudaGetLastError();
 }
 
@@ -309,10 +349,16 @@ cudaError_t launch_indexer_decode(const IndexerArgs &a, const DecodePos &p, cuda
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    const size_t smem = TK_FIXED_SMEM + sizeof(uint32_t) * (size_t)(vis_max > 0 ? vis_max : 1);
-    e = ensure_dyn_smem(topk_kernel, smem);
-    if (e != cudaSuccess) return e;
-    topk_kernel<<<a.n_seq, TK_THREADS, smem, s>>>(a, p);
+    const size_t smem = tk_fixed_smem<TK_DECODE>() + sizeof(uint32_t) * (size_t)(vis_max > 0 ? vis_max : 1);
+    if (smem <= (size_t)200 * 1024) {
+        e = ensure_dyn_smem(topk_kernel<TK_DECODE, true>, smem);
+        if (e != cudaSuccess) return e;
+        topk_kernel<TK_DECODE, true><<<a.n_seq, TK_DECODE, smem, s>>>(a, p);
+    } else {            // the keys do not fit: read them from the score rows each pass
+        e = ensure_dyn_smem(topk_kernel<TK_DECODE, false>, tk_fixed_smem<TK_DECODE>());
+        if (e != cudaSuccess) return e;
+        topk_kernel<TK_DECODE, false><<<a.n_seq, TK_DECODE, tk_fixed_smem<TK_DECODE>(), s>>>(a, p);
+    }
     return cudaGetLastError();
 }
 
