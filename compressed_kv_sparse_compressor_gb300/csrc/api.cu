@@ -47,11 +47,15 @@ int proj_width(const ds4c_layer_cfg &c, bool attn) { return coff_of(c) * lane_wi
 //           for a decode step)
 //   parts:  decode steps on the tensor-core attention split each query's rows
 //           over `parts` work items: [n_seq*parts][H][D] + [n_seq*parts][2][H] float
+//   gemm:   decode steps of bf16 layers with at most 128 sequences: split-K
+//           partials of the projections, [kSplitK][rows][P] float
+constexpr int kSplitK = 16;
 struct WsLayout {
     size_t proj_off, proj_ld;
     size_t scores_off, scores_ld;
     size_t mirror_off;
     size_t part_o_off, part_ml_off;
+    size_t gemm_part_off;            // 0: no split-K region
     int parts;
     size_t total;
 };
@@ -82,6 +86,10 @@ WsLayout ws_layout(const ds4c_layer_cfg &c, uint32_t rows, uint64_t mirror_rows,
             L.part_ml_off = o;
             o += align_up(items * 2 * c.n_heads * sizeof(float), 256);
         }
+    }
+    if (decode && c.dtype == DS4C_BF16 && P > 0 && rows <= 128) {
+        L.gemm_part_off = o;
+        o += align_up(sizeof(float) * (size_t)kSplitK * rows * P, 256);
     }
     L.total = o < 256 ? 256 : o;
     return L;
@@ -139,6 +147,12 @@ ds4c_status run_compress(const ds4c_layer_cfg *cfg, const ds4c_lane_weights *aw,
         g.n_groups = 4;
         g.g[2] = GemmGroup{iw->wkv, proj + 2 * Wa, (int64_t)L.proj_ld, Wi};
         g.g[3] = GemmGroup{iw->wgate, proj + 2 * Wa + Wi, (int64_t)L.proj_ld, Wi};
+    }
+    if (L.gemm_part_off != 0) {
+        g.c_base = proj;
+        g.part = reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + L.gemm_part_off);
+        g.part_ld = (int64_t)L.proj_ld;
+        g.max_ksplit = kSplitK;
     }
     cudaError_t e = cudaErrorNotSupported;
     if (c.dtype == DS4C_BF16) e = launch_gemm_tc(g, stream);
@@ -500,8 +514,8 @@ const char *ds4c_last_cuda_error(void) { return cudaGetErrorName(t_last_cuda_err
 ds4c_status ds4c_sync_status(cudaStream_t stream) {
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_status(e);
-    const unsigned int e1 = gemm_tc_read_clear_error(), e2 = attn_tc_read_clear_error();
-    if (e1 != 0 || e2 != 0) return DS4C_ERR_DEVICE;
+    const unsigned int e1 = gemm_tc_read_clear_error(), e2 = attn_tc_read_clear_error(), e3 = idx_read_clear_error();
+    if (e1 != 0 || e2 != 0 || e3 != 0) return DS4C_ERR_DEVICE;
     return DS4C_OK;
 }
 

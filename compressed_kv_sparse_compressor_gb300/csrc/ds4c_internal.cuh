@@ -46,6 +46,12 @@ struct GemmArgs {
     int dtype;          // DS4C_F32 / DS4C_BF16
     int n_groups;
     GemmGroup g[4];
+    // Optional split-K (tensor-core path): every group's C lies in one block
+    // [M][part_ld] starting at c_base; part holds max_ksplit such blocks.
+    float *c_base = nullptr;
+    float *part = nullptr;
+    int64_t part_ld = 0;
+    int max_ksplit = 1;
 };
 cudaError_t launch_gemm_simt(const GemmArgs &a, cudaStream_t s);
 // tcgen05 path for bf16 operands; returns cudaErrorNotSupported when the
@@ -102,6 +108,8 @@ struct IndexerArgs {
 };
 cudaError_t launch_indexer_prefill(const IndexerArgs &a, cudaStream_t s);
 cudaError_t launch_indexer_decode(const IndexerArgs &a, const DecodePos &p, cudaStream_t s);
+// device error word of the indexer kernels (a bounded wait gave up); read and cleared
+unsigned int idx_read_clear_error();
 
 // ----------------------------------------------------------------------------
 // Sparse SWA attention + ring commit

@@ -794,53 +794,46 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                     fence_after();
                     float l[H], v[H];
                     tmem_load<H>(lane_base + Lay::T_L, l);
-                    if (p.parts == 1) {
-                        // out[n][h][128 j + r] = O / L through two staging boxes [H][64] fp32 in
-                        // the P buffers (rows r < 64 at P hi, r >= 64 at P lo), stored by TMA
-                        float *stg = reinterpret_cast<float *>(phi_p + (r >> 6) * Lay::PB);
-                        const int rr = r & 63;
+                    // whole query: out[n][h][d] = O / L; split rows: the unnormalised partial
+                    // part_o[it][h][d] plus this part's reference maximum and denominator
+                    const bool whole = p.parts == 1;
+                    if (!whole && tid < H) {
+                        float lt = 0.f;
 #pragma unroll
-                        for (int h = 0; h < H; h++) l[h] = 1.0f / l[h];
-                        for (int j = 0; j < Lay::DB; j++) {
-                            tmem_load<H>(lane_base + Lay::T_O + j * H, v);
-                            if (j == Lay::DB - 1) {
-                                fence_before();
-                                mbar_arrive(bar(B_OFREE));
-                            }
-                            if (j > 0) {
-                                if (tid == 0) bulk_wait_read();
-                                if (!soft_bar()) { ok = false; break; }
-                            }
-#pragma unroll
-                            for (int h = 0; h < H; h++) stg[h * 64 + rr] = v[h] * l[h];
-                            fence_proxy_async();
-                            if (!soft_bar()) { ok = false; break; }
-                            if (tid == 0) {
-                                tma_store_box(&oMap, 128 * j, n * H, smem_u32(phi_p));
-                                tma_store_box(&oMap, 128 * j + 64, n * H, smem_u32(plo_p));
-                                bulk_commit();
-                            }
-                        }
-                        if (!ok) break;
-                        // the next P writes reuse the staging boxes
-                        if (tid == 0) bulk_wait_read();
-                    } else {
-                        float *o = p.part_o + (size_t)it * H * D;
-                        for (int j = 0; j < Lay::DB; j++) {
-                            tmem_load<H>(lane_base + Lay::T_O + j * H, v);
-#pragma unroll
-                            for (int h = 0; h < H; h++) o[(size_t)h * D + 128 * j + r] = v[h];
-                        }
-                        if (tid < H) {
-                            float lt = 0.f;
-#pragma unroll
-                            for (int h = 0; h < H; h++) lt = (h == tid) ? l[h] : lt;
-                            p.part_ml[(size_t)it * 2 * H + tid] = mref_s[tid];
-                            p.part_ml[(size_t)it * 2 * H + H + tid] = lt;
-                        }
-                        fence_before();
-                        mbar_arrive(bar(B_OFREE));
+                        for (int h = 0; h < H; h++) lt = (h == tid) ? l[h] : lt;
+                        p.part_ml[(size_t)it * 2 * H + tid] = mref_s[tid];
+                        p.part_ml[(size_t)it * 2 * H + H + tid] = lt;
                     }
+#pragma unroll
+                    for (int h = 0; h < H; h++) l[h] = whole ? 1.0f / l[h] : 1.0f;
+                    const int orow = (whole ? n : it) * H;
+                    // through two staging boxes [H][64] fp32 in the P buffers (rows r < 64 at
+                    // P hi, r >= 64 at P lo), stored by TMA
+                    float *stg = reinterpret_cast<float *>(phi_p + (r >> 6) * Lay::PB);
+                    const int rr = r & 63;
+                    for (int j = 0; j < Lay::DB; j++) {
+                        tmem_load<H>(lane_base + Lay::T_O + j * H, v);
+                        if (j == Lay::DB - 1) {
+                            fence_before();
+                            mbar_arrive(bar(B_OFREE));
+                        }
+                        if (j > 0) {
+                            if (tid == 0) bulk_wait_read();
+                            if (!soft_bar()) { ok = false; break; }
+                        }
+#pragma unroll
+                        for (int h = 0; h < H; h++) stg[h * 64 + rr] = v[h] * l[h];
+                        fence_proxy_async();
+                        if (!soft_bar()) { ok = false; break; }
+                        if (tid == 0) {
+                            tma_store_box(&oMap, 128 * j, orow, smem_u32(phi_p));
+                            tma_store_box(&oMap, 128 * j + 64, orow, smem_u32(plo_p));
+                            bulk_commit();
+                        }
+                    }
+                    if (!ok) break;
+                    // the next P writes reuse the staging boxes
+                    if (tid == 0) bulk_wait_read();
                 }
             }
         }
@@ -979,8 +972,12 @@ cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, cudaStream_t s
         return cudaErrorNotSupported;
     // Q in and out, both [n_q * H][D] fp32, one 64 x H box per 64-d chunk
     const uint64_t qrows = (uint64_t)a.n_seq * a.n_tok * H;
+    // the output map covers out, or the partial outputs [n_q * parts][H][D] when rows are split
     CUtensorMap qm, om;
-    if (!make_map_f32(&qm, a.q, qrows, D, H) || !make_map_f32(&om, a.out, qrows, D, H)) return cudaErrorNotSupported;
+    const bool whole = p.parts == 1;
+    if (!make_map_f32(&qm, a.q, qrows, D, H) ||
+        !make_map_f32(&om, whole ? a.out : a.part_o, whole ? qrows : qrows * (uint64_t)p.parts, D, H))
+        return cudaErrorNotSupported;
     (void)comp_rows_total;
     cudaError_t e = ensure_dyn_smem(attn_tc_kernel<H, D>, Lay::SMEM);
     if (e != cudaSuccess) return e;

@@ -143,12 +143,14 @@ __device__ __forceinline__ void finish_row(const CompressArgs &a, const LaneArgs
 
 // Ratio 4: window c pools, per column j, rows 0..3 (previous window, columns
 // [0, Dl)) and rows 4..7 (current window, columns [Dl, 2Dl)).
+// One pooling task per G threads of a 128-thread block (decode: task = the
+// sequence; prefill: the window index from pos0); every thread of the block
+// calls this.
 template <int G>
-__global__ void __launch_bounds__(128) compress_r4_kernel(CompressArgs a, int lane_id, DecodePos dp, int decode) {
-    __shared__ float red[32];
+__device__ __forceinline__ void pool_r4(const CompressArgs &a, int lane_id, const DecodePos &dp, int decode, int task,
+                                        float *red) {
     const LaneArgs L = a.lane[lane_id];
     const int W = 2 * L.Dl;
-    const int task = blockIdx.x * (128 / G) + threadIdx.x / G;
     const int j = (threadIdx.x % G) * 4;
     int seq = 0;
     uint64_t pos0, c;
@@ -202,6 +204,12 @@ __global__ void __launch_bounds__(128) compress_r4_kernel(CompressArgs a, int la
         x.w = den.w > 0.f ? sum.w / den.w : 0.f;
     }
     finish_row<G>(a, L, active, seq, c, j, x, red);
+}
+
+template <int G>
+__global__ void __launch_bounds__(128) compress_r4_kernel(CompressArgs a, int lane_id, DecodePos dp, int decode) {
+    __shared__ float red[32];
+    pool_r4<G>(a, lane_id, dp, decode, blockIdx.x * (128 / G) + threadIdx.x / G, red);
 }
 
 // Ratio 128: window c pools rows 0..127 at column j.  NS row-splits of the
@@ -291,15 +299,12 @@ __global__ void __launch_bounds__(G * 4) compress_r128_kernel(CompressArgs a, in
 // Frontier commit (K2b): after the pools of a segment (tokens pos0 .. end-1),
 // write the frontier the recurrence leaves behind.  One thread per float4
 // column of W = coff*Dl, looping over the frontier rows.
-__global__ void commit_kernel(CompressArgs a, int lane_id, DecodePos dp, int decode) {
+__device__ __forceinline__ void commit_col(const CompressArgs &a, int lane_id, const DecodePos &dp, int decode, int seq,
+                                           int col) {
     const LaneArgs L = a.lane[lane_id];
     const int ratio = a.ratio;
     const int coff = ratio == 4 ? 2 : 1;
     const int W = coff * L.Dl;
-    const int col = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
-    const int seq = decode ? blockIdx.y : 0;
-    if (col >= W) return;
-    if (decode && seq >= a.n_seg) return;
     const uint64_t pos0 = decode ? dp.pos[seq] : a.pos0;
     const uint64_t end = pos0 + (decode ? 1 : a.T);
     const int64_t ws_row0 = decode ? seq : 0;
@@ -346,6 +351,31 @@ __global__ void commit_kernel(CompressArgs a, int lane_id, DecodePos dp, int dec
             st4(ssc + (size_t)q * W + col, ws_sc((uint64_t)p));
         }
     }
+}
+
+__global__ void commit_kernel(CompressArgs a, int lane_id, DecodePos dp, int decode) {
+    const LaneArgs &L = a.lane[lane_id];
+    const int W = (a.ratio == 4 ? 2 : 1) * L.Dl;
+    const int col = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    const int seq = decode ? blockIdx.y : 0;
+    if (col >= W) return;
+    if (decode && seq >= a.n_seg) return;
+    commit_col(a, lane_id, dp, decode, seq, col);
+}
+
+// Decode step of a ratio-4 layer in one launch: block (sequence b, lane l)
+// pools b's window when its token completes one (G = Dl/4 threads do the
+// work, the rest of the block only takes part in the barriers), then, after
+// the block barrier, writes the frontier the step leaves behind.
+template <int GA, int GI>
+__global__ void __launch_bounds__(128) compress_decode_r4_kernel(CompressArgs a, DecodePos dp) {
+    __shared__ float red[32];
+    const int seq = blockIdx.x, lane_id = blockIdx.y;
+    if (lane_id == 0) pool_r4<GA>(a, 0, dp, 1, (threadIdx.x / GA == 0) ? seq : a.n_seg, red);
+    else pool_r4<GI>(a, 1, dp, 1, (threadIdx.x / GI == 0) ? seq : a.n_seg, red);
+    __syncthreads();
+    const int W = 2 * a.lane[lane_id].Dl;
+    for (int col = threadIdx.x * 4; col < W; col += 128 * 4) commit_col(a, lane_id, dp, 1, seq, col);
 }
 
 cudaError_t pool_lane(const CompressArgs &a, int lane, const DecodePos &dp, int decode, int n_tasks, cudaStream_t s) {
@@ -397,6 +427,22 @@ cudaError_t launch_compress_prefill(const CompressArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_compress_decode(const CompressArgs &a, const DecodePos &p, int n_seq, cudaStream_t s) {
+    if (a.ratio == 4 && a.n_lanes == 2 && n_seq > 0) {
+        const int ga = a.lane[0].Dl / 4, gi = a.lane[1].Dl / 4;
+        const dim3 grid((unsigned)n_seq, 2);
+#define DS4C_CDEC(A, I)                                                              \
+        if (ga == A && gi == I) {                                                   \
+            compress_decode_r4_kernel<A, I><<<grid, 128, 0, s>>>(a, p);             \
+            return cudaGetLastError();                                              \
+        }
+        DS4C_CDEC(128, 32)
+        DS4C_CDEC(128, 16)
+        DS4C_CDEC(64, 16)
+        DS4C_CDEC(32, 16)
+        DS4C_CDEC(128, 64)
+        DS4C_CDEC(64, 32)
+#undef DS4C_CDEC
+    }
     for (int l = 0; l < a.n_lanes; l++) {
         cudaError_t e = pool_lane(a, l, p, 1, n_seq, s);
         if (e != cudaSuccess) return e;

@@ -51,11 +51,14 @@ struct TcParams {
     int M, K;
     int m_tiles;
     int n_groups;
-    int tile_start[5];     // prefix sums of tiles per group
+    int ksplit;            // K ranges per output tile (1: whole K)
+    int a_rows;            // rows of the A box (BM, or fewer when M is small: the MMA rows past them are unused)
+    int tile_start[5];     // prefix sums of tiles per group (ksplit tiles per output tile)
     int n_tiles[4];
     int N[4];
-    float *C[4];
+    float *C[4];           // ksplit == 1: the outputs; else partial k of group g at C[g] + k * part_stride
     int64_t ldc[4];
+    int64_t part_stride;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -154,12 +157,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void tile_coords(const TcParams &p, int tile, int &g, int &mt, int &nt) {
+__device__ __forceinline__ void tile_coords(const TcParams &p, int tile, int &g, int &mt, int &nt, int &ks) {
     g = 0;
     while (g + 1 < p.n_groups && tile >= p.tile_start[g + 1]) g++;
     const int local = tile - p.tile_start[g];
-    nt = local / p.m_tiles;
-    mt = local % p.m_tiles;
+    ks = local % p.ksplit;
+    const int o = local / p.ksplit;
+    nt = o / p.m_tiles;
+    mt = o % p.m_tiles;
 }
 
 template <int BN>
@@ -179,6 +184,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int total = p.tile_start[p.n_groups];
     const int kb_count = (p.K + BK - 1) / BK;
+    const int kb_per = (kb_count + p.ksplit - 1) / p.ksplit;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; s++) {
@@ -210,17 +216,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
             uint32_t it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                int g, mt, nt;
-                tile_coords(p, tile, g, mt, nt);
+                int g, mt, nt, ks;
+                tile_coords(p, tile, g, mt, nt, ks);
                 const CUtensorMap *mb = g == 0 ? &mapB0 : g == 1 ? &mapB1 : g == 2 ? &mapB2 : &mapB3;
-                for (int kb = 0; kb < kb_count; kb++, it++) {
+                const int kb0 = ks * kb_per, kb1 = min(kb_count, kb0 + kb_per);
+                for (int kb = kb0; kb < kb1; kb++, it++) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
                     if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort)) { ok = false; break; }
                     uint8_t *sa = smem + s * STAGE_BYTES;
                     uint8_t *sb = sa + A_BYTES;
                     const uint32_t bar = smem_u32(&full[s]);
-                    mbar_expect_tx(bar, STAGE_BYTES);
+                    mbar_expect_tx(bar, (uint32_t)(p.a_rows * BK * 2 + (STAGE_BYTES - A_BYTES)));
                     tma_load_2d(smem_u32(sa), &mapA, kb * BK, mt * BM, bar);
                     tma_load_2d(smem_u32(sb), mb, kb * BK, nt * BN, bar);
                 }
@@ -237,7 +244,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
                 if (!mbar_wait(smem_u32(&acc_empty[acc]), aph ^ 1, abort)) break;
                 fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < kb_count; kb++, it++) {
+                int g_, mt_, nt_, ks_;
+                tile_coords(p, tile, g_, mt_, nt_, ks_);
+                const int kb0 = ks_ * kb_per, kb1 = min(kb_count, kb0 + kb_per);
+                for (int kb = kb0; kb < kb1; kb++, it++) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
                     if (!mbar_wait(smem_u32(&full[s]), ph, abort)) { ok = false; break; }
@@ -247,7 +257,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
 #pragma unroll
                     for (int k = 0; k < BK / 16; k++)
                         mma_bf16(d_tmem, sw128_desc(sa + k * 32), sw128_desc(sb + k * 32), G::IDESC,
-                                 (kb > 0 || k > 0) ? 1u : 0u);
+                                 (kb > kb0 || k > 0) ? 1u : 0u);
                     mma_commit(smem_u32(&empty[s]));
                 }
                 if (ok) mma_commit(smem_u32(&acc_full[acc]));
@@ -264,15 +274,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
         const int row = quarter * 32 + lane;
         uint32_t local = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, local++) {
-            int g, mt, nt;
-            tile_coords(p, tile, g, mt, nt);
+            int g, mt, nt, ks;
+            tile_coords(p, tile, g, mt, nt, ks);
             const int acc = local & 1;
             const uint32_t aph = (local >> 1) & 1;
             if (!mbar_wait(smem_u32(&acc_full[acc]), aph, abort)) break;
             fence_after();
             const int m = mt * BM + row;
             const int n0 = nt * BN;
-            float *crow = p.C[g] + (size_t)m * p.ldc[g];
+            float *crow = p.C[g] + (size_t)ks * p.part_stride + (size_t)m * p.ldc[g];
 #pragma unroll 1
             for (int c = 0; c < BN / 32; c++) {
                 uint32_t r[32];
@@ -338,6 +348,20 @@ int sm_count() {
     return n;
 }
 
+// Sum of the split-K partials, in split order: C[m][n] = sum_k part[k][m][n]
+// over the whole [M][ldc] block the groups write into.
+__global__ void splitk_reduce_kernel(float *__restrict__ C, const float *__restrict__ part, int64_t n4, int64_t stride,
+                                     int ksplit) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n4) return;
+    float4 acc = reinterpret_cast<const float4 *>(part)[i];
+    for (int k = 1; k < ksplit; k++) {
+        const float4 v = reinterpret_cast<const float4 *>(part + (size_t)k * stride)[i];
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    reinterpret_cast<float4 *>(C)[i] = acc;
+}
+
 template <int BN>
 cudaError_t launch_bn(const GemmArgs &a, cudaStream_t s) {
     using G = GT<BN>;
@@ -347,8 +371,21 @@ cudaError_t launch_bn(const GemmArgs &a, cudaStream_t s) {
     p.K = a.K;
     p.m_tiles = (a.M + BM - 1) / BM;
     p.n_groups = a.n_groups;
+    // split K when the output tiles alone leave most SMs idle and a partial buffer is given
+    int ksplit = 1;
+    if (a.part && a.c_base) {
+        int out_tiles = 0;
+        for (int g = 0; g < a.n_groups; g++) out_tiles += p.m_tiles * ((a.g[g].N + BN - 1) / BN);
+        const int kb_count = (a.K + BK - 1) / BK;
+        while (ksplit * 2 <= a.max_ksplit && out_tiles * ksplit * 2 <= 4 * sm_count() && kb_count / (ksplit * 2) >= 4)
+            ksplit *= 2;
+    }
+    p.ksplit = ksplit;
+    p.part_stride = (int64_t)a.M * a.part_ld;
     CUtensorMap mA, mB[4];
-    if (!make_map(&mA, a.A, (uint64_t)a.M, (uint64_t)a.K, BM)) return cudaErrorNotSupported;
+    // small M: a box of the rows present (multiple of 8), not of the whole MMA tile
+    p.a_rows = a.M >= BM ? BM : ((a.M + 7) / 8) * 8;
+    if (!make_map(&mA, a.A, (uint64_t)a.M, (uint64_t)a.K, (uint32_t)p.a_rows)) return cudaErrorNotSupported;
     int start = 0;
     for (int g = 0; g < 4; g++) {
         const int gi = g < a.n_groups ? g : a.n_groups - 1;
@@ -357,11 +394,11 @@ cudaError_t launch_bn(const GemmArgs &a, cudaStream_t s) {
             if (((uintptr_t)G_.B & 15) != 0 || (G_.ldc % 4) != 0 || ((uintptr_t)G_.C & 15) != 0) return cudaErrorNotSupported;
             if (!make_map(&mB[g], G_.B, (uint64_t)G_.N, (uint64_t)a.K, BN)) return cudaErrorNotSupported;
             p.N[g] = G_.N;
-            p.C[g] = G_.C;
+            p.C[g] = ksplit > 1 ? a.part + (G_.C - a.c_base) : G_.C;
             p.ldc[g] = G_.ldc;
             p.n_tiles[g] = (G_.N + BN - 1) / BN;
             p.tile_start[g] = start;
-            start += p.n_tiles[g] * p.m_tiles;
+            start += p.n_tiles[g] * p.m_tiles * ksplit;
         } else {
             mB[g] = mB[gi];
         }
@@ -371,6 +408,10 @@ cudaError_t launch_bn(const GemmArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const int grid = start < sm_count() ? start : sm_count();
     gemm_tc_kernel<BN><<<grid, THREADS, G::SMEM_BYTES, s>>>(mA, mB[0], mB[1], mB[2], mB[3], p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || ksplit == 1) return e;
+    const int64_t n4 = (int64_t)a.M * a.part_ld / 4;
+    splitk_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(a.c_base, a.part, n4, p.part_stride, ksplit);
     return cudaGetLastError();
 }
 

@@ -12,9 +12,15 @@
 // the keys re-read from the score row each pass), then an ordered compaction that emits the
 // selected indices in ascending order, ties at the threshold broken toward
 // the lower index.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "ds4c_internal.cuh"
 
 namespace ds4c {
+
+__device__ unsigned int g_idx_err;
+
 namespace {
 
 // ---------------------------------------------------------------------------
@@ -140,6 +146,103 @@ __global__ void __launch_bounds__(128) score_decode_kernel(IndexerArgs a, Decode
         s = __fmaf_rn(qs[4 * i + 3], v[i].w, s);
     }
     a.scores[(size_t)b * a.lds + c] = s;
+}
+
+// ---------------------------------------------------------------------------
+// K4 decode, staged form (d <= 128): a 128-thread block scores 128 rows of its
+// sequence.  The rows arrive in shared memory by TMA as d/32 boxes of [128
+// rows][32 floats] in the 128-byte swizzle, so that thread t reads its own row
+// (16-byte chunk j of row t sits at chunk j ^ (t & 7)) without bank conflicts;
+// then the same in-order fma chain.  Several blocks share an SM, so the HBM
+// stream has many boxes in flight.
+// ---------------------------------------------------------------------------
+constexpr unsigned long long IDX_WAIT_NS = 4000000000ull;
+
+__device__ __forceinline__ uint32_t idx_smem_u32(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+template <int DD>
+__global__ void __launch_bounds__(128) score_decode_tma_kernel(const __grid_constant__ CUtensorMap rowsMap, IndexerArgs a,
+                                                               DecodePos dp, int idx_cap) {
+    static_assert(DD % 32 == 0 && DD <= 128, "staged rows: d/32 boxes of 16 KB");
+    constexpr int SEG = DD / 32;
+    extern __shared__ uint8_t sm_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~(uintptr_t)1023);
+    __shared__ uint64_t bar;
+    __shared__ float qs[DD];
+    const int b = blockIdx.y;
+    const uint64_t vis = (dp.pos[b] + 1) / 4;
+    const int c0 = blockIdx.x * 128;
+    if ((uint64_t)c0 >= vis) return;
+    const uint32_t bar_a = idx_smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_a) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_a), "r"(SEG * 128 * 128) : "memory");
+        const int y = b * idx_cap + c0;
+#pragma unroll
+        for (int sg = 0; sg < SEG; sg++)
+            asm volatile(
+                "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+                    idx_smem_u32(sm + sg * 16384)),
+                "l"(reinterpret_cast<uint64_t>(&rowsMap)), "r"(32 * sg), "r"(y), "r"(bar_a)
+                : "memory");
+    }
+    for (int i = threadIdx.x; i < DD; i += 128) qs[i] = a.q[(size_t)b * DD + i];
+    __syncthreads();
+    // bounded wait for the boxes; a wait that gives up raises the error word
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar_a)
+            : "memory");
+        if (done) break;
+        if ((it & 255u) == 255u) {
+            uint64_t now;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > IDX_WAIT_NS) {
+                atomicOr(&g_idx_err, 1u);
+                return;
+            }
+        }
+    }
+    const int t = threadIdx.x;
+    const int c = c0 + t;
+    if ((uint64_t)c >= vis) return;
+    float4 v[DD / 4];
+#pragma unroll
+    for (int sg = 0; sg < SEG; sg++)
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            v[sg * 8 + j] = *reinterpret_cast<const float4 *>(sm + sg * 16384 + t * 128 + ((j ^ (t & 7)) * 16));
+    float sc = 0.f;
+#pragma unroll
+    for (int i = 0; i < DD / 4; i++) {
+        sc = __fmaf_rn(qs[4 * i + 0], v[i].x, sc);
+        sc = __fmaf_rn(qs[4 * i + 1], v[i].y, sc);
+        sc = __fmaf_rn(qs[4 * i + 2], v[i].z, sc);
+        sc = __fmaf_rn(qs[4 * i + 3], v[i].w, sc);
+    }
+    a.scores[(size_t)b * a.lds + c] = sc;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 idx_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
 }
 
 // ---------------------------------------------------------------------------
@@ -337,7 +440,41 @@ cudaError_t launch_indexer_decode(const IndexerArgs &a, const DecodePos &p, cuda
     uint64_t vis_max = 0;
     for (int b = 0; b < a.n_seq; b++) vis_max = ((p.pos[b] + 1) / 4 > vis_max) ? (p.pos[b] + 1) / 4 : vis_max;
     cudaError_t e;
-    if (vis_max > 0) {
+    // staged rows by TMA when the row width allows it (d = 32, 64, 96 or 128)
+    const int64_t idx_cap = a.d > 0 ? a.seq_stride / a.d : 0;
+    bool staged = vis_max > 0 && a.d <= 128 && a.d % 32 == 0 && (reinterpret_cast<uintptr_t>(a.rows) & 15u) == 0 &&
+                  idx_cap * a.d == a.seq_stride;
+    CUtensorMap rm;
+    if (staged) {
+        auto fn = idx_encode_fn();
+        cuuint64_t dims[2] = {(cuuint64_t)a.d, (cuuint64_t)((uint64_t)a.n_seq * (uint64_t)idx_cap)};
+        cuuint64_t strides[1] = {(cuuint64_t)a.d * 4};
+        cuuint32_t box[2] = {32, 128};
+        cuuint32_t estr[2] = {1, 1};
+        staged = fn && fn(&rm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(a.rows), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    if (staged) {
+        dim3 grid((unsigned)((vis_max + 127) / 128), (unsigned)a.n_seq);
+        const size_t smem = (size_t)(a.d / 32) * 16384 + 1024;
+#define DS4C_SCORE_TMA(dd)                                                                                   \
+    case dd:                                                                                                 \
+        e = ensure_dyn_smem(score_decode_tma_kernel<dd>, smem);                                              \
+        if (e != cudaSuccess) return e;                                                                      \
+        score_decode_tma_kernel<dd><<<grid, 128, smem, s>>>(rm, a, p, (int)idx_cap);                          \
+        break;
+        switch (a.d) {
+            DS4C_SCORE_TMA(32)
+            DS4C_SCORE_TMA(64)
+            DS4C_SCORE_TMA(96)
+            DS4C_SCORE_TMA(128)
+            default: return cudaErrorInvalidValue;
+        }
+#undef DS4C_SCORE_TMA
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    } else if (vis_max > 0) {
         dim3 grid((unsigned)((vis_max + 127) / 128), (unsigned)a.n_seq);
         switch (a.d) {
             case 64: score_decode_kernel<64><<<grid, 128, 0, s>>>(a, p); break;
@@ -360,6 +497,13 @@ cudaError_t launch_indexer_decode(const IndexerArgs &a, const DecodePos &p, cuda
         topk_kernel<TK_DECODE, false><<<a.n_seq, TK_DECODE, tk_fixed_smem<TK_DECODE>(), s>>>(a, p);
     }
     return cudaGetLastError();
+}
+
+unsigned int idx_read_clear_error() {
+    unsigned int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_idx_err, sizeof v) != cudaSuccess) return 0;
+    if (v) cudaMemcpyToSymbol(g_idx_err, &z, sizeof z);
+    return v;
 }
 
 }  // namespace ds4c
