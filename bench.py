@@ -44,6 +44,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=256)
+    ap.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
+                    help="profiling: run only the prefill or only the decode measurement")
+    ap.add_argument("--profile-step", action="store_true",
+                    help="after timing, run one more step between cudaProfilerStart/Stop (for ncu --profile-from-start off)")
     return ap.parse_args()
 
 
@@ -214,6 +218,11 @@ def run_ours(args, rank, world, local_rank):
         b.build()
     if world > 1:
         torch.distributed.barrier()
+    if args.only == "decode":
+        P, _ = peaks()
+        dec = run_decode(device, P, profile=args.profile_step)
+        return {"metric": "decode step us at 64K ctx", "value": dec["us_per_step"], "unit": "us", "n_gpus": world,
+                "higher_is_better": False, "data": "synthetic", "config": {"workload": dec["workload"]}, "decode": dec}
     n_tok = args.tokens or configs.C5.n_tok
     pf = Prefill(n_tok, device)
     for _ in range(max(args.warmup, 3)):
@@ -238,6 +247,11 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     clk = clocks.stop()
     pf.dl.sync()
+    if args.profile_step:
+        torch.cuda.profiler.start()
+        pf.step()
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
     ms = t0.elapsed_time(t1) / args.steps
     ms_t = torch.tensor([ms], device=device)
     if world > 1:
@@ -257,7 +271,7 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_e2e:
         e2e = run_e2e(pf, args, device)
     dec = None
-    if not args.no_decode:
+    if not args.no_decode and args.only == "all":
         dec = run_decode(device, P)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -337,7 +351,7 @@ def run_e2e(pf, args, device):
             "ms_per_step": round(ms, 3), "steps": steps}
 
 
-def run_decode(device, P):
+def run_decode(device, P, profile=False):
     """C4: 32 sequences at 65536 + (b mod 4); state built by the compressor, ring from raw rows."""
     from compressed_kv_sparse_compressor_gb300.layer import DeviceLayer
     w = configs.C4
@@ -385,6 +399,13 @@ def run_decode(device, P):
         if i >= 3:
             times.append(e0.elapsed_time(e1) * 1e3)
     dl.sync()
+    if profile:
+        torch.cuda.profiler.start()
+        dl.compress_decode(hid, lens)
+        dl.indexer_topk(q_idx, lens, B, 1, topk)
+        dl.attention(q, raw, topk, lens, B, 1, out, commit_ring=True)
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
     us = statistics.median(times)
     # algorithmic bytes: weights + indexer rows scanned + gathered rows + q/out/raw
     wbytes = 2 * (2 * 2 * shape.head_dim + 2 * 2 * shape.idx_head_dim) * shape.d_model
