@@ -30,6 +30,10 @@ import torch  # noqa: E402
 from compressed_kv_sparse_compressor_gb300 import configs  # noqa: E402
 
 METRIC = "prefill tokens/s per layer"
+# dram__bytes_read.sum + dram__bytes_write.sum of one attention launch (4096 queries), from the ncu capture
+# in profiles/kernels_prefill_8192tok_chunk2_full.md; set to None when the kernel changes until re-captured
+ATTN_TRAFFIC = 557131520 + 483981056
+ATTN_TRAFFIC_SRC = "ncu, one 4096-query launch of the 8192-token case (same units per launch as C5)"
 UNIT = "tokens/s"
 
 
@@ -306,7 +310,8 @@ def roofline(kind, br, pf, P, src):
         peak = P["bf16_tflops"]
         return {"kernel": "sparse_swa_attention", "bound": "tensor", "achieved": round(per_launch / dur / 1e12, 2),
                 "peak": peak, "unit": "TFLOP/s", "frac": round(per_launch / dur / 1e12 / peak, 4),
-                "traffic": None, "peak_source": src, "units_per_launch": f"{C} queries"}
+                "traffic": ATTN_TRAFFIC, "traffic_source": ATTN_TRAFFIC_SRC, "peak_source": src,
+                "units_per_launch": f"{C} queries"}
     if kind == "indexer_topk":
         flops = sum(indexer_flops_chunk(shape, c * C, min(C, T - c * C)) for c in range(pf.n_chunks))
         per_launch = flops / n_launch
