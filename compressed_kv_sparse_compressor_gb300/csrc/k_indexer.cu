@@ -57,7 +57,7 @@ __device__ __forceinline__ void store_slice(float (*As)[SP], float (*Bs)[SP], co
     }
 }
 
-__global__ void __launch_bounds__(256) score_prefill_kernel(IndexerArgs a) {
+__global__ void __launch_bounds__(256, 2) score_prefill_kernel(IndexerArgs a) {
     const int j0 = blockIdx.y * SB, c0 = blockIdx.x * SB;
     const int jlast = min(j0 + SB, a.n_tok) - 1;
     const uint64_t vis_max = (a.pos0 + (uint64_t)jlast + 1) / 4;
