@@ -26,8 +26,9 @@ EXPORTS = (
     "ds4c_workspace_bytes", "ds4c_state_init", "ds4c_compress_prefill", "ds4c_compress_decode_step",
     "ds4c_indexer_topk", "ds4c_sparse_swa_attn", "ds4c_checkpoint_floats", "ds4c_checkpoint_gather",
     "ds4c_sync_status", "ds4c_status_string", "ds4c_last_cuda_error", "ds4c_attn_uses_tensor_cores",
-    "ds4c_indexer_topk_noalloc",
+    "ds4c_indexer_topk_noalloc", "ds4c_checkpoint_scatter", "ds4c_payload_header",
 )
+PAYLOAD_U32_FIELDS = 13
 NOALLOC_SCORE_FLOATS = 2 * 1024 * 1024
 
 
@@ -50,6 +51,12 @@ class LayerCfg(C.Structure):
 
 class LaneWeights(C.Structure):
     _fields_ = [("wkv", C.c_void_p), ("wgate", C.c_void_p), ("ape", C.c_void_p), ("norm", C.c_void_p)]
+
+
+class PayloadInfo(C.Structure):
+    _fields_ = [(n, C.c_uint32) for n in ("ctx_size", "prefill_chunk", "raw_cap", "raw_window", "comp_cap",
+                                           "token_count", "layer_count", "head_dim", "idx_head_dim", "vocab_size",
+                                           "live_raw_rows")]
 
 
 class LaneState(C.Structure):
@@ -86,6 +93,8 @@ def lib() -> C.CDLL:
         "ds4c_indexer_topk_noalloc": (st, [cfgp, lsp, P, C.POINTER(U64), U32, U32, P, P]),
         "ds4c_checkpoint_floats": (SZ, [cfgp, U64]),
         "ds4c_checkpoint_gather": (st, [cfgp, lsp, U32, U64, P, SZ, C.POINTER(SZ), P]),
+        "ds4c_checkpoint_scatter": (st, [cfgp, lsp, U32, U64, P, SZ, P]),
+        "ds4c_payload_header": (st, [C.POINTER(PayloadInfo), C.POINTER(C.c_uint32 * PAYLOAD_U32_FIELDS)]),
         "ds4c_sync_status": (st, [P]),
         "ds4c_status_string": (C.c_char_p, [C.c_int]),
         "ds4c_last_cuda_error": (C.c_char_p, []),
@@ -159,6 +168,17 @@ def ds4c_checkpoint_floats(cfg, pos):
 
 def ds4c_checkpoint_gather(cfg, state, seq, pos, dst, dst_floats, written, stream):
     return lib().ds4c_checkpoint_gather(C.byref(cfg), C.byref(state), seq, pos, dst, dst_floats, written, stream)
+
+
+def ds4c_checkpoint_scatter(cfg, state, seq, pos, src, src_floats, stream):
+    return lib().ds4c_checkpoint_scatter(C.byref(cfg), C.byref(state), seq, pos, src, src_floats, stream)
+
+
+def ds4c_payload_header(info):
+    """The 13 u32 fields of the DSV4 payload header for `info` (a PayloadInfo)."""
+    out = (C.c_uint32 * PAYLOAD_U32_FIELDS)()
+    check(lib().ds4c_payload_header(C.byref(info), C.byref(out)), "ds4c_payload_header")
+    return list(out)
 
 
 def ds4c_sync_status(stream):

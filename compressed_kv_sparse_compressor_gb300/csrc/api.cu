@@ -509,6 +509,71 @@ ds4c_status ds4c_checkpoint_gather(const ds4c_layer_cfg *cfg, const ds4c_layer_s
     return cuda_status(launch_gather(a, stream));
 }
 
+ds4c_status ds4c_checkpoint_scatter(const ds4c_layer_cfg *cfg, const ds4c_layer_state *st, uint32_t seq,
+                                    uint64_t pos, const float *src, size_t src_floats, cudaStream_t stream) {
+    ds4c_status s = check_cfg(cfg);
+    if (s != DS4C_OK) return s;
+    const ds4c_layer_cfg &c = *cfg;
+    if (!st || !st->raw || !src) return DS4C_ERR_NULL;
+    if (c.ratio != 0 && (s = check_lane_state(st->attn)) != DS4C_OK) return s;
+    if (c.ratio == 4 && (s = check_lane_state(st->idx)) != DS4C_OK) return s;
+    if (c.ratio != 0 && tc_attention(c) && !st->attn.comp_split) return DS4C_ERR_NULL;
+    if (c.ratio != 0 && pos / c.ratio > c.comp_cap) return DS4C_ERR_CAPACITY;
+    if (c.ratio == 4 && pos / 4 > c.idx_cap) return DS4C_ERR_CAPACITY;
+    const size_t need = ds4c_checkpoint_floats(cfg, pos);
+    if (src_floats < need) return DS4C_ERR_CAPACITY;
+    ScatterArgs a{};
+    a.src = src;
+    a.ring = st->raw + (size_t)seq * raw_stride(c);
+    a.D = c.head_dim;
+    a.S = c.swa;
+    a.pos = pos;
+    a.n_live = (int64_t)(pos < c.swa ? pos : c.swa);
+    int64_t o = a.n_live * a.D;
+    int n = 0;
+    float *comp_attn = nullptr;
+    int64_t n_comp = 0;
+    if (c.ratio != 0) {
+        const size_t fs = frontier_stride(c, true);
+        comp_attn = st->attn.comp + (size_t)seq * comp_stride(c, true);
+        n_comp = (int64_t)(pos / c.ratio);
+        a.seg[n++] = ScatterSeg{comp_attn, o, n_comp * c.head_dim};
+        o += a.seg[n - 1].n;
+        a.seg[n++] = ScatterSeg{st->attn.state_kv + (size_t)seq * fs, o, (int64_t)fs};
+        o += (int64_t)fs;
+        a.seg[n++] = ScatterSeg{st->attn.state_score + (size_t)seq * fs, o, (int64_t)fs};
+        o += (int64_t)fs;
+    }
+    if (c.ratio == 4) {
+        const size_t fs = frontier_stride(c, false);
+        a.seg[n++] = ScatterSeg{st->idx.comp + (size_t)seq * comp_stride(c, false), o, (int64_t)(pos / 4) * c.idx_head_dim};
+        o += a.seg[n - 1].n;
+        a.seg[n++] = ScatterSeg{st->idx.state_kv + (size_t)seq * fs, o, (int64_t)fs};
+        o += (int64_t)fs;
+        a.seg[n++] = ScatterSeg{st->idx.state_score + (size_t)seq * fs, o, (int64_t)fs};
+        o += (int64_t)fs;
+    }
+    a.n_seg = n;
+    if ((size_t)o != need) return DS4C_ERR_SHAPE;
+    cudaError_t e = launch_scatter(a, stream);
+    // the tensor-core attention's bf16 mirror of the restored compressed rows
+    if (e == cudaSuccess && c.ratio != 0 && tc_attention(c))
+        e = launch_split_rows(st->attn.comp_split + (size_t)seq * c.comp_cap * 2 * c.head_dim, comp_attn, n_comp,
+                              (int)c.head_dim, stream);
+    return cuda_status(e);
+}
+
+ds4c_status ds4c_payload_header(const ds4c_payload_info *info, uint32_t out[DS4C_PAYLOAD_U32_FIELDS]) {
+    if (!info || !out) return DS4C_ERR_NULL;
+    const uint32_t f[DS4C_PAYLOAD_U32_FIELDS] = {DS4C_PAYLOAD_MAGIC,        DS4C_PAYLOAD_VERSION,   info->ctx_size,
+                                                 info->prefill_chunk,      info->raw_cap,          info->raw_window,
+                                                 info->comp_cap,           info->token_count,      info->layer_count,
+                                                 info->head_dim,           info->idx_head_dim,     info->vocab_size,
+                                                 info->live_raw_rows};
+    for (unsigned i = 0; i < DS4C_PAYLOAD_U32_FIELDS; i++) out[i] = f[i];
+    return DS4C_OK;
+}
+
 const char *ds4c_last_cuda_error(void) { return cudaGetErrorName(t_last_cuda_error); }
 
 ds4c_status ds4c_sync_status(cudaStream_t stream) {

@@ -167,4 +167,17 @@ struct GatherArgs {
 };
 cudaError_t launch_gather(const GatherArgs &a, cudaStream_t s);
 
+// Restore (the gather's inverse): segment 0 writes the raw rows back to their
+// ring slots, the others are contiguous copies from src + src_off.
+struct ScatterSeg { float *dst; int64_t src_off; int64_t n; };
+struct ScatterArgs {
+    const float *src;
+    float *ring; int64_t D; int64_t S; uint64_t pos; int64_t n_live;
+    int n_seg;
+    ScatterSeg seg[8];
+};
+cudaError_t launch_scatter(const ScatterArgs &a, cudaStream_t s);
+// bf16 hi / lo of n_rows rows of D floats (the tensor-core attention's mirror)
+cudaError_t launch_split_rows(uint16_t *split, const float *rows, int64_t n_rows, int D, cudaStream_t s);
+
 }  // namespace ds4c

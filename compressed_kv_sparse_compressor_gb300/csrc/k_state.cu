@@ -1,6 +1,8 @@
 // State initialisation (K3), raw-ring commit (K7) and logical-order
 // checkpoint gather (K8).  All three are plain HBM copies / fills: coalesced
 // 16-byte accesses, grid-stride loops over a grid of a few waves of the SMs.
+#include <cuda_bf16.h>
+
 #include "ds4c_internal.cuh"
 
 namespace ds4c {
@@ -77,6 +79,50 @@ __global__ void gather_kernel(GatherArgs a, int vec) {
     }
 }
 
+// Restore of a checkpoint (the inverse of gather_kernel): destination row i of
+// the raw segment goes to slot (pos - n_live + i) % S; the other segments are
+// contiguous copies.  blockIdx.y picks the segment.
+__global__ void scatter_kernel(ScatterArgs a, int vec) {
+    const int s = blockIdx.y;
+    if (s > a.n_seg) return;
+    size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    size_t stride = (size_t)gridDim.x * blockDim.x;
+    if (s == 0) {
+        size_t n = (size_t)a.n_live * a.D;
+        uint64_t first = a.pos - (uint64_t)a.n_live;
+        for (size_t i = tid * (vec ? 4 : 1); i < n; i += stride * (vec ? 4 : 1)) {
+            size_t row = i / a.D, col = i % a.D;
+            size_t slot = (size_t)((first + row) % (uint64_t)a.S);
+            float *dst = a.ring + slot * a.D + col;
+            if (vec) *reinterpret_cast<float4 *>(dst) = *reinterpret_cast<const float4 *>(a.src + i);
+            else *dst = a.src[i];
+        }
+        return;
+    }
+    const ScatterSeg g = a.seg[s - 1];
+    const float *src = a.src + g.src_off;
+    if (vec) {
+        size_t n4 = (size_t)g.n / 4;
+        for (size_t i = tid; i < n4; i += stride)
+            reinterpret_cast<float4 *>(g.dst)[i] = reinterpret_cast<const float4 *>(src)[i];
+        for (size_t i = n4 * 4 + tid; i < (size_t)g.n; i += stride) g.dst[i] = src[i];
+    } else {
+        for (size_t i = tid; i < (size_t)g.n; i += stride) g.dst[i] = src[i];
+    }
+}
+
+// hi = bf16(x), lo = bf16(x - hi) of each element, into [row][2][D]
+__global__ void split_rows_kernel(uint16_t *__restrict__ split, const float *__restrict__ rows, int64_t n, int D) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / D, c = i % D;
+        const float x = rows[i];
+        const __nv_bfloat16 h = __float2bfloat16_rn(x);
+        const __nv_bfloat16 l = __float2bfloat16_rn(x - __bfloat162float(h));
+        split[(r * 2) * D + c] = *reinterpret_cast<const uint16_t *>(&h);
+        split[(r * 2 + 1) * D + c] = *reinterpret_cast<const uint16_t *>(&l);
+    }
+}
+
 int sm_count() {
     static int n = 0;
     if (n == 0) {
@@ -123,6 +169,31 @@ cudaError_t launch_gather(const GatherArgs &a, cudaStream_t s) {
     if (blocks < 1) blocks = 1;
     dim3 grid((unsigned)blocks, (unsigned)(a.n_seg + 1));
     gather_kernel<<<grid, 256, 0, s>>>(a, vec ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const ScatterArgs &a, cudaStream_t s) {
+    bool vec = ((uintptr_t)a.src & 15) == 0 && ((uintptr_t)a.ring & 15) == 0 && (a.D % 4) == 0;
+    for (int i = 0; i < a.n_seg; i++)
+        vec = vec && ((uintptr_t)a.seg[i].dst & 15) == 0 && (a.seg[i].src_off % 4) == 0;
+    int64_t biggest = a.n_live * a.D;
+    for (int i = 0; i < a.n_seg; i++) biggest = a.seg[i].n > biggest ? a.seg[i].n : biggest;
+    int64_t blocks = (biggest / 4 + 255) / 256;
+    int64_t cap = (int64_t)sm_count() * 4;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    dim3 grid((unsigned)blocks, (unsigned)(a.n_seg + 1));
+    scatter_kernel<<<grid, 256, 0, s>>>(a, vec ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_split_rows(uint16_t *split, const float *rows, int64_t n_rows, int D, cudaStream_t s) {
+    const int64_t n = n_rows * D;
+    if (n <= 0) return cudaSuccess;
+    int64_t blocks = (n + 255) / 256;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    split_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(split, rows, n, D);
     return cudaGetLastError();
 }
 

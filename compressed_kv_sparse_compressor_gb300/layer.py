@@ -113,6 +113,10 @@ class DeviceLayer:
                                              C.byref(written), _stream()), "ds4c_checkpoint_gather")
         return written.value
 
+    def checkpoint_scatter(self, seq: int, pos: int, src: torch.Tensor) -> None:
+        abi.check(abi.ds4c_checkpoint_scatter(self.cfg, self.state, seq, pos, _ptr(src), src.numel(), _stream()),
+                  "ds4c_checkpoint_scatter")
+
     def sync(self):
         abi.check(abi.ds4c_sync_status(_stream()), "ds4c_sync_status")
 

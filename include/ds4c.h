@@ -239,6 +239,37 @@ DS4C_API ds4c_status ds4c_checkpoint_gather(const ds4c_layer_cfg *cfg, const ds4
                                    uint32_t seq, uint64_t pos, float *dst, size_t dst_floats,
                                    size_t *written_h, cudaStream_t stream);
 
+/* Restore of a checkpoint into sequence `seq` of `state`: the inverse of
+ * ds4c_checkpoint_gather on a buffer in the same layout ([P1] §6: the raw rows,
+ * saved in logical position order, go back in order into the live ring, slot
+ * p % swa for position p; §7: the compressed rows and both lanes' frontier
+ * tensors, so that compression continues exactly from pos).  Rows of comp past
+ * the live count and ring slots past min(pos, swa) live rows are left as they
+ * are.  On the tensor-core attention path the attention lane's comp_split
+ * mirror of the restored rows is rebuilt as well.  src (device) holds
+ * ds4c_checkpoint_floats(cfg, pos) floats; fewer -> DS4C_ERR_CAPACITY. */
+DS4C_API ds4c_status ds4c_checkpoint_scatter(const ds4c_layer_cfg *cfg, const ds4c_layer_state *state,
+                                             uint32_t seq, uint64_t pos, const float *src, size_t src_floats,
+                                             cudaStream_t stream);
+
+/* The fixed header of the DSV4 session payload ([P1] §5): 13 u32 fields, in
+ * order: magic "DSV4" (0x34565344), payload version 2, saved context size,
+ * prefill chunk size, raw KV ring capacity, raw sliding-window length,
+ * compressed KV capacity, checkpoint token count, layer count, raw/head KV
+ * dimension, indexer head dimension, vocabulary size, live raw rows serialised
+ * in the body.  The body that follows it is, in order: the token ids, the
+ * next-token logits, per-layer compressed-row counts (attention, then ratio-4
+ * indexer; pos / ratio each), then the per-layer data ds4c_checkpoint_gather
+ * writes.  Host only. */
+#define DS4C_PAYLOAD_MAGIC 0x34565344u
+#define DS4C_PAYLOAD_VERSION 2u
+#define DS4C_PAYLOAD_U32_FIELDS 13u
+typedef struct {
+    uint32_t ctx_size, prefill_chunk, raw_cap, raw_window, comp_cap, token_count, layer_count, head_dim,
+        idx_head_dim, vocab_size, live_raw_rows;
+} ds4c_payload_info;
+DS4C_API ds4c_status ds4c_payload_header(const ds4c_payload_info *info, uint32_t out[DS4C_PAYLOAD_U32_FIELDS]);
+
 /* Synchronises `stream`, then reports (and clears) the device error word:
  * DS4C_ERR_DEVICE if a kernel raised it, DS4C_ERR_CUDA if the stream failed. */
 DS4C_API ds4c_status ds4c_sync_status(cudaStream_t stream);

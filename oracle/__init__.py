@@ -79,6 +79,7 @@ def lib():
             "orc_ring_commit": (None, [P, P, P, U64, I]),
             "orc_checkpoint_floats": (C.c_int64, [P, U64]),
             "orc_checkpoint_gather": (C.c_int64, [P, P, LaneS, LaneS, U64, P]),
+            "orc_checkpoint_scatter": (C.c_int64, [P, P, LaneS, LaneS, U64, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -324,6 +325,16 @@ def ring_commit(st: State, raw_new, pos0: int):
 def checkpoint_floats(L: Layer, pos: int) -> int:
     cfg = L.c()
     return lib().orc_checkpoint_floats(C.byref(cfg), pos)
+
+
+def checkpoint_scatter(st: State, pos: int, src: np.ndarray) -> None:
+    """Restore `st` from a checkpoint body of `pos` tokens (in place)."""
+    cfg = st.L.c()
+    n = checkpoint_floats(st.L, pos)
+    src = np.ascontiguousarray(src, dtype=np.float32)
+    assert src.size >= n
+    w = lib().orc_checkpoint_scatter(C.byref(cfg), _p(st.raw), st.attn.s(), st.idx.s(), pos, _p(src))
+    assert w == n
 
 
 def checkpoint_gather(st: State, pos: int) -> np.ndarray:

@@ -493,3 +493,31 @@ int64_t orc_checkpoint_gather(const orc_cfg *cfg, const float *ring, orc_lane_s 
     }
     return o;
 }
+
+/* Restore ("【#4】ds4.c を読み解く" §6-§7): the same body read back into the
+ * state -- raw rows in logical order to slot p % swa, then the compressed rows
+ * and frontier tensors of each lane.  Returns the number of floats read. */
+int64_t orc_checkpoint_scatter(const orc_cfg *cfg, float *ring, orc_lane_s as, orc_lane_s is, uint64_t pos,
+                               const float *src) {
+    const int D = cfg->head_dim, d = cfg->idx_head_dim, r = cfg->ratio, S = cfg->swa;
+    int64_t o = 0;
+    uint64_t n_live = pos < (uint64_t)S ? pos : (uint64_t)S;
+    for (uint64_t p = pos - n_live; p < pos; p++) {
+        memcpy(ring + (size_t)(p % (uint64_t)S) * D, src + o, sizeof(float) * (size_t)D);
+        o += D;
+    }
+    if (r != 0) {
+        const int coff = (r == 4) ? 2 : 1;
+        size_t nc = (size_t)(pos / (uint64_t)r) * D, nf = (size_t)(coff * r) * (coff * D);
+        memcpy(as.comp, src + o, sizeof(float) * nc); o += (int64_t)nc;
+        memcpy(as.state_kv, src + o, sizeof(float) * nf); o += (int64_t)nf;
+        memcpy(as.state_score, src + o, sizeof(float) * nf); o += (int64_t)nf;
+    }
+    if (r == 4) {
+        size_t nc = (size_t)(pos / 4) * d, nf = (size_t)8 * (2 * d);
+        memcpy(is.comp, src + o, sizeof(float) * nc); o += (int64_t)nc;
+        memcpy(is.state_kv, src + o, sizeof(float) * nf); o += (int64_t)nf;
+        memcpy(is.state_score, src + o, sizeof(float) * nf); o += (int64_t)nf;
+    }
+    return o;
+}

@@ -115,3 +115,18 @@ def test_host_validation_errors(L):
     written = C.c_size_t(0)
     assert abi.ds4c_checkpoint_gather(cfg, st, 0, 40, FAKE, n - 1, C.byref(written), None) == abi.DS4C_ERR_CAPACITY
     assert abi.status_string(abi.DS4C_ERR_CAPACITY).startswith("positions")
+
+
+def test_payload_header_matches_the_page_table():
+    """ds4c_payload_header writes the 13 fields in the order of the page's table."""
+    import json
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "payload_header.json")))
+    info = abi.PayloadInfo(*range(101, 112))      # distinct values: ctx_size = 101 .. live_raw_rows = 111
+    hdr = abi.ds4c_payload_header(info)
+    assert len(hdr) == g["u32_fields"] == abi.PAYLOAD_U32_FIELDS
+    assert hdr[0] == g["magic_u32"] == int.from_bytes(g["magic_ascii"].encode(), "little")
+    assert hdr[1] == g["version"]
+    names = [f[0] for f in abi.PayloadInfo._fields_]
+    for i, name in enumerate(g["fields"][2:], start=2):
+        assert hdr[i] == getattr(info, name), name
+    assert names == g["fields"][2:]

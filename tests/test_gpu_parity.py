@@ -206,3 +206,55 @@ def test_c2_full():
         sample = [0, 1, 127, 128, 1000, 2047, 4094, 4095]
         _run_chunk(dl, wa, wi, shape, w.seed, c * w.chunk, w.chunk, report, sample=sample)
     _gather_check(dl, w.n_tok)
+
+
+# ---------------------------------------------------------------------------
+# Checkpoint restore: gather -> scatter into a fresh state -> continue
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("ratio,heads,D", [(4, 64, 512), (128, 64, 512), (0, 64, 512), (4, 8, 128)])
+def test_checkpoint_restore_resumes_bit_exact(ratio, heads, D):
+    """Restored state equals the saved one on every live region (and the bf16
+    mirror is rebuilt), and continuing from it gives the uninterrupted run's
+    outputs bit for bit; the oracle's restore of the same body agrees."""
+    dtype = "bf16" if D == 512 else "f32"
+    shape = configs.LayerShape(d_model=512 if D == 512 else 256, head_dim=D, n_rot=64, idx_head_dim=128 if D == 512 else 64,
+                               n_heads=heads, ratio=ratio, top_k=16, dtype=dtype, w_std=0.04)
+    seed, T1, T2 = 41, 301, 170                       # T1 is mid-window for both ratios and wraps the ring
+    cap = (T1 + T2) // max(ratio, 1) + 1
+    icap = (T1 + T2) // 4 + 1
+    dl, wa, wi = device_layer(shape, comp_cap=cap, idx_cap=icap, seed=seed)
+    _run_chunk(dl, wa, wi, shape, seed, 0, T1, {}, check=False)
+    n = dl.checkpoint_floats(T1)
+    body = torch.empty(n, device="cuda")
+    dl.checkpoint_gather(0, T1, body)
+    dl.sync()
+    # restore into a fresh layer (same weights)
+    fresh, _, _ = device_layer(shape, comp_cap=cap, idx_cap=icap, seed=seed)
+    fresh.checkpoint_scatter(0, T1, body)
+    fresh.sync()
+    again = torch.empty(n, device="cuda")
+    fresh.checkpoint_gather(0, T1, again)
+    fresh.sync()
+    assert torch.equal(again, body)
+    if ratio and dl.attn_split is not None:
+        rows = T1 // ratio
+        assert torch.equal(fresh.attn_split[:, :rows], dl.attn_split[:, :rows])
+    # the oracle restores the same body to the same gather
+    st = orc.State(orc_layer(shape, cap, icap))
+    orc.state_init(st)
+    orc.checkpoint_scatter(st, T1, body.cpu().numpy())
+    np.testing.assert_array_equal(orc.checkpoint_gather(st, T1), body.cpu().numpy())
+    # continue both with the same chunk
+    tk_a, out_a = _run_chunk(dl, wa, wi, shape, seed, T1, T2, {}, check=False)
+    tk_b, out_b = _run_chunk(fresh, wa, wi, shape, seed, T1, T2, {}, check=False)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b)
+    if tk_a is not None:
+        assert torch.equal(tk_a, tk_b)
+    n2 = dl.checkpoint_floats(T1 + T2)
+    ga, gb = torch.empty(n2, device="cuda"), torch.empty(n2, device="cuda")
+    dl.checkpoint_gather(0, T1 + T2, ga)
+    fresh.checkpoint_gather(0, T1 + T2, gb)
+    dl.sync()
+    assert torch.equal(ga, gb)

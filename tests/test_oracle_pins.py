@@ -468,3 +468,40 @@ def test_ring_commit_and_gather_logical_order(orc):
         if ratio == 4:
             want += (p // 4) * 4 + 2 * 8 * 8
         assert orc.checkpoint_floats(L, p) == want
+
+
+@pytest.mark.parametrize("ratio", [0, 4, 128])
+def test_checkpoint_restore_resumes_exactly(orc, ratio):
+    """Gather at T1, restore into a fresh state, continue to T1 + T2: the state
+    equals the uninterrupted run's bit for bit ([P1] §6-§7: logical-order raw
+    rows and the frontier are what compression needs to continue)."""
+    shape = configs.LayerShape(d_model=32, head_dim=16, n_rot=8, idx_head_dim=8, n_heads=2, ratio=ratio,
+                               swa=16, top_k=4, dtype="f32", w_std=0.2)
+    T1, T2 = 37, 150                                   # T1 mid-window, past the ring; T2 wraps the ring
+    L = orc_layer(shape, comp_cap=64, idx_cap=64)
+    wa = lane_np(configs.lane_weights(shape, 9, 0, "attn"))
+    wi = lane_np(configs.lane_weights(shape, 9, 0, "idx"))
+    h = np_in(configs.hidden(shape, 9, T1 + T2))
+    _, _, raw = configs.queries(shape, 9, T1 + T2)
+    raw = raw.numpy()
+
+    def run(st, p0, n):
+        if ratio:
+            orc.compress(st, wa, wi, h[p0:p0 + n], p0)
+        orc.ring_commit(st, raw[p0:p0 + n], p0)
+
+    full = orc.State(L)
+    orc.state_init(full)
+    run(full, 0, T1)
+    run(full, T1, T2)
+
+    part = orc.State(L)
+    orc.state_init(part)
+    run(part, 0, T1)
+    body = orc.checkpoint_gather(part, T1)
+    fresh = orc.State(L)
+    orc.state_init(fresh)
+    orc.checkpoint_scatter(fresh, T1, body)
+    np.testing.assert_array_equal(orc.checkpoint_gather(fresh, T1), body)
+    run(fresh, T1, T2)
+    np.testing.assert_array_equal(orc.checkpoint_gather(fresh, T1 + T2), orc.checkpoint_gather(full, T1 + T2))
