@@ -257,11 +257,7 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         torch.cuda.profiler.stop()
     ms = t0.elapsed_time(t1) / args.steps
-    ms_t = torch.tensor([ms], device=device)
-    if world > 1:
-        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
-    value = world * n_tok / (ms_max / 1e3)
+    ms_max, value = aggregate(ms, n_tok, device)
     br = pf.breakdown()
 
     # roofline of the dominant call
@@ -319,6 +315,17 @@ def run_ours(args, rank, world, local_rank):
         "cpu_baseline": cpu,
     }
     return line
+
+
+def aggregate(ms_local: float, units_per_rank: int, device):
+    """Replicas: the step time is the maximum over ranks, the value the units all
+    ranks processed per second of that time.  Returns (ms_max, value)."""
+    world = torch.distributed.get_world_size() if torch.distributed.is_initialized() else 1
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(t.item())
+    return ms_max, world * units_per_rank / (ms_max / 1e3)
 
 
 def roofline(kind, br, pf, P, src):
