@@ -144,8 +144,8 @@ struct AttnTcArgs {
     int parts;                    // work items per query; > 1 splits the rows (decode)
     float *part_o, *part_ml;      // workspace for the partial outputs when parts > 1
 };
-// Work items per decode query: one per 128-row tile (the raw window plus the
-// compressed rows a query can see), at most 8.
+// Work items per decode query: one per two 128-row tiles (the raw window plus
+// the compressed rows a query can see), at most 8.
 int attn_tc_decode_parts(int ratio, int k, int comp_cap);
 bool attn_tc_supported(int H, int D, int S, int ratio, int k);
 cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *p, cudaStream_t s);

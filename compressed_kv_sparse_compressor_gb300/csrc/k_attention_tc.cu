@@ -993,9 +993,13 @@ cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, cudaStream_t s
 }  // namespace
 
 int attn_tc_decode_parts(int ratio, int k, int comp_cap) {
+    // about two tiles per work item: each item loads its query's Q and writes one
+    // partial, so halving the item count against one tile per item saves those
+    // fixed costs while a decode batch still spreads over the SMs
     const int rows = ratio == 4 ? (k < comp_cap ? k : comp_cap) : (ratio == 128 ? comp_cap : 0);
     const int tiles = 1 + (rows + ROWS - 1) / ROWS;
-    return tiles < 8 ? tiles : 8;
+    const int parts = (tiles + 1) / 2;
+    return parts < 8 ? parts : 8;
 }
 
 bool attn_tc_supported(int H, int D, int S, int ratio, int k) {

@@ -34,14 +34,20 @@ constexpr unsigned long long WAIT_NS = 4000000000ull;
 
 // Tile width BN: 256 for prefill chunks; 32 for decode-sized M, where the
 // weights are the traffic and more, narrower tiles spread them over the SMs.
-template <int BN>
+// AR: A rows a stage holds.  BM for prefill; 32 for M <= 32 ("thin" stages of
+// 8 KB, so twice as many stages are in flight): the M = 128 MMA then reads rows
+// 32..127 of A from whatever follows the stage -- finite or not, they only feed
+// accumulator rows that are never stored -- and a pad after the last stage keeps
+// those reads inside the allocation.
+template <int BN, int AR = BM>
 struct GT {
-    static constexpr int STAGES = BN >= 128 ? 4 : 8;
-    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int A_BYTES = AR * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = AR < BM ? (BN >= 128 ? 8 : 20) : (BN >= 128 ? 4 : 8);
+    static constexpr int PAD = (BM - AR) * BK * 2;
     static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + PAD + 1024 + 256;
     // instruction descriptor: kind::f16, A = B = bf16, D = f32, both K-major, M = 128, N = BN
     static constexpr uint32_t IDESC =
         (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
@@ -167,16 +173,16 @@ __device__ __forceinline__ void tile_coords(const TcParams &p, int tile, int &g,
     mt = o % p.m_tiles;
 }
 
-template <int BN>
+template <int BN, int AR>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
                const __grid_constant__ CUtensorMap mapB1, const __grid_constant__ CUtensorMap mapB2,
                const __grid_constant__ CUtensorMap mapB3, TcParams p) {
-    using G = GT<BN>;
+    using G = GT<BN, AR>;
     constexpr int STAGES = G::STAGES, A_BYTES = G::A_BYTES, STAGE_BYTES = G::STAGE_BYTES, TMEM_COLS = G::TMEM_COLS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES + G::PAD);
     uint64_t *full = bars, *empty = bars + STAGES, *acc_full = bars + 2 * STAGES, *acc_empty = bars + 2 * STAGES + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -362,9 +368,9 @@ __global__ void splitk_reduce_kernel(float *__restrict__ C, const float *__restr
     reinterpret_cast<float4 *>(C)[i] = acc;
 }
 
-template <int BN>
+template <int BN, int AR>
 cudaError_t launch_bn(const GemmArgs &a, cudaStream_t s) {
-    using G = GT<BN>;
+    using G = GT<BN, AR>;
     if (((uintptr_t)a.A & 15) != 0) return cudaErrorNotSupported;
     TcParams p{};
     p.M = a.M;
@@ -377,7 +383,7 @@ cudaError_t launch_bn(const GemmArgs &a, cudaStream_t s) {
         int out_tiles = 0;
         for (int g = 0; g < a.n_groups; g++) out_tiles += p.m_tiles * ((a.g[g].N + BN - 1) / BN);
         const int kb_count = (a.K + BK - 1) / BK;
-        while (ksplit * 2 <= a.max_ksplit && out_tiles * ksplit * 2 <= 4 * sm_count() && kb_count / (ksplit * 2) >= 4)
+        while (ksplit * 2 <= a.max_ksplit && out_tiles * ksplit * 2 <= 2 * sm_count() && kb_count / (ksplit * 2) >= 4)
             ksplit *= 2;
     }
     p.ksplit = ksplit;
@@ -404,10 +410,11 @@ cudaError_t launch_bn(const GemmArgs &a, cudaStream_t s) {
         }
     }
     p.tile_start[a.n_groups] = start;
-    cudaError_t e = ensure_dyn_smem(gemm_tc_kernel<BN>, G::SMEM_BYTES);
+    if (p.a_rows > AR) return cudaErrorInvalidValue;
+    cudaError_t e = ensure_dyn_smem(gemm_tc_kernel<BN, AR>, G::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int grid = start < sm_count() ? start : sm_count();
-    gemm_tc_kernel<BN><<<grid, THREADS, G::SMEM_BYTES, s>>>(mA, mB[0], mB[1], mB[2], mB[3], p);
+    gemm_tc_kernel<BN, AR><<<grid, THREADS, G::SMEM_BYTES, s>>>(mA, mB[0], mB[1], mB[2], mB[3], p);
     e = cudaGetLastError();
     if (e != cudaSuccess || ksplit == 1) return e;
     const int64_t n4 = (int64_t)a.M * a.part_ld / 4;
@@ -422,7 +429,10 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
         return cudaErrorNotSupported;
     if (((uintptr_t)a.A & 15) != 0) return cudaErrorNotSupported;
     // decode-sized M: narrow tiles, so the weight traffic spreads over many SMs
-    return a.M <= 256 ? launch_bn<32>(a, s) : launch_bn<256>(a, s);
+    // at most 32 rows: wide tiles (fewer re-reads of the activations per weight
+    // byte) over thin stages, split along K to cover the SMs
+    if (a.M <= 32) return launch_bn<128, 32>(a, s);
+    return a.M <= 256 ? launch_bn<32, BM>(a, s) : launch_bn<256, BM>(a, s);
 }
 
 unsigned int gemm_tc_read_clear_error() {
