@@ -361,27 +361,61 @@ def roofline(kind, br, pf, P, src):
 
 
 def run_e2e(pf, args, device):
+    """The prefill through the public API from pinned host memory: per chunk, the
+    inputs go up on one copy stream, the chunk runs on the compute stream once
+    they have landed, and its outputs come back on a second copy stream, so the
+    copies of neighbouring chunks overlap the compute (as a serving loop would)."""
     host_in = [t.cpu().pin_memory() for t in pf.inputs()]
     host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in pf.outputs()]
+    dev_in, dev_out = pf.inputs(), pf.outputs()
+    s_up, s_comp, s_down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    dl = pf.dl
     steps = max(1, min(args.steps, 2))
+
+    def one_step():
+        with torch.cuda.stream(s_comp):
+            dl.state_init()
+        for c in range(pf.n_chunks):
+            p0, n = c * pf.chunk, min(pf.chunk, pf.T - c * pf.chunk)
+            sl = slice(p0, p0 + n)
+            with torch.cuda.stream(s_up):
+                for d, h in zip(dev_in, host_in):
+                    d[sl].copy_(h[sl], non_blocking=True)
+                landed = torch.cuda.Event()
+                landed.record(s_up)
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(landed)
+                dl.compress_prefill(pf.h[sl], p0)
+                dl.indexer_topk(pf.q_idx[sl], [p0], 1, n, pf.topk[sl])
+                dl.attention(pf.q[sl], pf.raw[sl], pf.topk[sl], [p0], 1, n, pf.out[sl], commit_ring=True)
+                done = torch.cuda.Event()
+                done.record(s_comp)
+            with torch.cuda.stream(s_down):
+                s_down.wait_event(done)
+                host_out[0][sl].copy_(dev_out[0][sl], non_blocking=True)     # out
+                host_out[1][sl].copy_(dev_out[1][sl], non_blocking=True)     # topk
+        with torch.cuda.stream(s_comp):
+            dl.checkpoint_gather(0, pf.T, pf.ck)
+            done = torch.cuda.Event()
+            done.record(s_comp)
+        with torch.cuda.stream(s_down):
+            s_down.wait_event(done)
+            host_out[2].copy_(dev_out[2], non_blocking=True)                 # checkpoint
+        torch.cuda.synchronize()        # a step ends when its last output is on the host
+
+    one_step()                      # warm-up of the streams and the pinned buffers
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
     for _ in range(steps):
-        for d, h in zip(pf.inputs(), host_in):
-            d.copy_(h, non_blocking=True)
-        pf.step()
-        for h, d in zip(host_out, pf.outputs()):
-            h.copy_(d, non_blocking=True)
-    e1.record()
+        one_step()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+    ms = (time.perf_counter() - t0) * 1e3 / steps
+    dl.sync()
     bi = sum(t.numel() * t.element_size() for t in host_in)
     bo = sum(t.numel() * t.element_size() for t in host_out)
     return {"value": round(pf.T / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-            "ms_per_step": round(ms, 3), "steps": steps}
+            "ms_per_step": round(ms, 3), "steps": steps,
+            "pipeline": "per chunk: upload, compute and download on three streams"}
 
 
 def run_decode(device, P, profile=False):
