@@ -399,6 +399,7 @@ ds4c_status ds4c_sparse_swa_attn(const ds4c_layer_cfg *cfg, const ds4c_layer_sta
         }
     }
     cudaError_t e;
+    bool ring_done = false;   // the decode combine wrote the ring slots
     if (tc_attention(c)) {
         if (c.ratio != 0 && !st->attn.comp_split) return DS4C_ERR_NULL;
         const WsLayout L = (n_seq == 1) ? ws_prefill(c, n_tok) : ws_decode(c, n_seq);
@@ -426,6 +427,8 @@ ds4c_status ds4c_sparse_swa_attn(const ds4c_layer_cfg *cfg, const ds4c_layer_sta
         a.parts = (n_seq > 1) ? L.parts : 1;
         a.part_o = reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + L.part_o_off);
         a.part_ml = reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + L.part_ml_off);
+        a.commit_ring = (commit_ring && a.parts > 1) ? 1 : 0;
+        ring_done = a.commit_ring != 0;
         e = launch_attention_tc(a, n_seq > 1 ? &dp : nullptr, stream);
     } else {
         AttnArgs a{};
@@ -447,7 +450,7 @@ ds4c_status ds4c_sparse_swa_attn(const ds4c_layer_cfg *cfg, const ds4c_layer_sta
         a.pos0 = pos_h[0];
         e = launch_attention(a, n_seq > 1 ? &dp : nullptr, stream);
     }
-    if (e == cudaSuccess && commit_ring)
+    if (e == cudaSuccess && commit_ring && !ring_done)
         e = launch_ring_commit(st->raw, raw_new, (int)c.head_dim, (int)c.swa, (int)n_seq, (int)n_tok, pos_h[0],
                                n_seq > 1 ? &dp : nullptr, stream);
     return cuda_status(e);

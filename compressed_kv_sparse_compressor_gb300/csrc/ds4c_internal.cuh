@@ -142,6 +142,7 @@ struct AttnTcArgs {
     int n_seq, n_tok, n_seq_state;
     uint64_t pos0;
     int parts;                    // work items per query; > 1 splits the rows (decode)
+    int commit_ring;              // parts > 1: the combine also writes raw_new[b] to ring slot pos_b % 128
     float *part_o, *part_ml;      // workspace for the partial outputs when parts > 1
 };
 // Work items per decode query: one per two 128-row tiles (the raw window plus

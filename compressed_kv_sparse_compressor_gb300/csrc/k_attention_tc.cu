@@ -878,10 +878,20 @@ __global__ void raw_split_kernel(uint16_t *__restrict__ mirror, const float *__r
 // Split rows: out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p over the
 // parts of a query (M = the largest reference of a non-empty part).
 __global__ void __launch_bounds__(128) attn_combine_kernel(float *__restrict__ out, const float *__restrict__ part_o,
-                                                           const float *__restrict__ part_ml, int H, int D, int parts) {
+                                                           const float *__restrict__ part_ml, int H, int D, int parts,
+                                                           float *__restrict__ ring, const float *__restrict__ raw_new,
+                                                           DecodePos dp) {
     __shared__ float w[8];
     __shared__ float inv_den;
     const int n = blockIdx.x / H, h = blockIdx.x % H;
+    // ring commit of the step (decode: query n is sequence n): the attention read the
+    // ring through the raw mirror, so the slot can take the new row now
+    if (ring && h == 0) {
+        float *dst = ring + ((size_t)n * ROWS + (size_t)(dp.pos[n] % ROWS)) * D;
+        const float *src = raw_new + (size_t)n * D;
+        for (int d = threadIdx.x * 4; d < D; d += blockDim.x * 4)
+            *reinterpret_cast<float4 *>(dst + d) = *reinterpret_cast<const float4 *>(src + d);
+    }
     if (threadIdx.x == 0) {
         float M = -INFINITY;
         for (int q = 0; q < parts; q++) {
@@ -986,7 +996,9 @@ cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, cudaStream_t s
     attn_tc_kernel<H, D><<<grid, THREADS, Lay::SMEM, s>>>(rh, rl, qm, om, p);
     e = cudaGetLastError();
     if (e != cudaSuccess || p.parts == 1) return e;
-    attn_combine_kernel<<<a.n_seq * a.n_tok * H, 128, 0, s>>>(a.out, p.part_o, p.part_ml, H, D, p.parts);
+    attn_combine_kernel<<<a.n_seq * a.n_tok * H, 128, 0, s>>>(a.out, p.part_o, p.part_ml, H, D, p.parts,
+                                                              a.commit_ring ? const_cast<float *>(a.ring) : nullptr,
+                                                              a.raw_new, p.dp);
     return cudaGetLastError();
 }
 

@@ -246,13 +246,26 @@ PFN_cuTensorMapEncodeTiled_v12000 idx_encode_fn() {
 }
 
 // ---------------------------------------------------------------------------
-// K5 top-k, one CTA per query, in two forms.  Prefill (thousands of queries):
-// 256 threads, the scores stay in global memory (each pass re-reads the row:
-// the first read comes from HBM, the later ones hit L2), so a CTA holds only
-// its counters and candidate buffer (32 KB) and several CTAs share an SM,
-// hiding each other's barrier and scan latencies.  Decode (one query per
-// sequence, a few dozen CTAs): 1024 threads with the row's keys resident in
-// shared memory, so each pass is short.
+// K5 top-k, one CTA per query: the k largest scores among the visible rows,
+// listed in ascending row order, equal scores going to the lower row.
+//
+// Keys are order-preserving u32 images of the scores.  Main path, two reads
+// of the score row:
+//   1. a 4096-bin histogram of the top 12 key bits (shared atomics); a suffix
+//      scan over it gives the bin b* that holds the k-th largest key;
+//   2. rows in bins above b* are selected outright (one bitmap word per 32
+//      rows, from a warp ballot); rows in b* are copied to a candidate list;
+//   3. two 1024-bin passes over the candidates resolve the low 20 bits: the
+//      k-th largest key K* and how many rows equal to K* are taken;
+//   4. candidates above K* join the bitmap, those equal to K* go to a second
+//      bitmap, and one in-order scan of both writes the list, taking the
+//      lowest rows of K* first.
+// When b* holds more rows than the candidate list (heavy ties), the CTA runs
+// a plain 4-bit radix select instead (private per-thread counters, 8 passes,
+// then an ordered compaction).
+// Prefill: 256 threads, the row stays in global memory (the second read hits
+// L2), several CTAs per SM.  Decode: 1024 threads, the keys resident in shared
+// memory.
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t order_key(float s) {
@@ -260,89 +273,111 @@ __device__ __forceinline__ uint32_t order_key(float s) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-constexpr int TK_BINS = 16;          // 4-bit radix digits, 8 passes
-constexpr int TK_CAND = 4096;        // survivors are compacted once they fit here
-constexpr int TK_UNR = 4;            // independent score loads in flight per thread
-// dynamic shared memory: counters [16][threads] | candidates [4096] | (resident keys [V])
-template <int TK_THREADS>
-constexpr size_t tk_fixed_smem() { return sizeof(uint32_t) * (TK_BINS * TK_THREADS + TK_CAND); }
+constexpr int TK_HBITS = 12;         // main path: bits of the first histogram
+constexpr int TK_HBINS = 1 << TK_HBITS;
+constexpr int TK_LBINS = 1024;       // main path: 10-bit candidate passes
+constexpr int TK_CAND = 2048;        // main path: candidate list (key, row)
+constexpr int TK_BINS = 16;          // radix path: 4-bit digits
+constexpr int TK_RCAND = 4096;       // radix path: survivors compacted once they fit
+constexpr int TK_UNR = 8;            // independent score loads in flight per thread
 constexpr int TK_PREFILL = 256, TK_DECODE = 1024;
 
-template <int TK_THREADS, bool RESIDENT>
-__global__ void __launch_bounds__(TK_THREADS) topk_kernel(IndexerArgs a, DecodePos dp) {
-    constexpr int TK_WARPS = TK_THREADS / 32;
-    extern __shared__ uint32_t sm_tk[];
-    uint32_t *cnt = sm_tk;                              // cnt[bin * threads + tid], private per thread
-    uint32_t *cand = sm_tk + TK_BINS * TK_THREADS;
-    uint32_t *keys = cand + TK_CAND;                    // RESIDENT only
+// Dynamic shared memory in u32 words:
+//   bins [max(4096, 16 T)] | candidate keys [2048] | candidate rows [2048] |
+//   selected bitmap [wcap] | equal-key bitmap [wcap] | resident keys [vmax]
+// The radix path reuses the bins as its per-thread counters and the candidate
+// lists as its 4096-key survivor buffer.
+template <int T>
+__host__ __device__ constexpr int tk_bin_words() { return TK_HBINS > TK_BINS * T ? TK_HBINS : TK_BINS * T; }
+template <int T>
+size_t tk_smem(uint64_t vmax, bool resident) {
+    const uint64_t wcap = (vmax + 31) / 32;
+    return sizeof(uint32_t) * ((size_t)tk_bin_words<T>() + 2 * TK_CAND + 2 * wcap + (resident ? vmax : 0));
+}
+static_assert(2 * TK_CAND >= TK_RCAND, "radix survivors fit the candidate lists");
+
+// Suffix crossing over bins[0, nbins) (nbins a multiple of T, at least T),
+// counted from the top bin down: the bin holding the need-th largest element
+// (res[0]) and that element's rank inside the bin (res[1], 1 = the bin's
+// largest).  Needs need >= 1 and at most the bins' total.  Ends on a barrier.
+template <int T>
+__device__ __forceinline__ void tk_crossing(const uint32_t *bins, int nbins, uint32_t need, uint32_t *warp_sum,
+                                            uint32_t *res) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = nbins / T;
+    const int hi = nbins - tid * per;                       // this thread's bins: [hi - per, hi)
+    uint32_t local = 0;
+    for (int b = hi - 1; b >= hi - per; b--) local += bins[b];
+    uint32_t incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    for (int w = 0; w < warp; w++) incl += warp_sum[w];
+    const uint32_t excl = incl - local;
+    if (excl < need && incl >= need) {
+        uint32_t r = need - excl;
+        for (int b = hi - 1; b >= hi - per; b--) {
+            const uint32_t h = bins[b];
+            if (h >= r) {
+                res[0] = (uint32_t)b;
+                res[1] = r;
+                break;
+            }
+            r -= h;
+        }
+    }
+    __syncthreads();
+}
+
+// Radix path: 4 bits per pass from the top give K* and how many rows equal to
+// K* to keep; once the keys that still match the resolved prefix fit the
+// survivor buffer, later passes scan only those.  Then each warp owns a
+// contiguous range of rows and one exchange of per-warp counts gives every
+// warp its output offset.  cnt: [16][T] words, cand: [4096] words.
+template <int T, typename KeyAt>
+__device__ void tk_radix(int V, int k, int32_t *out, KeyAt key_at, uint32_t *cnt, uint32_t *cand) {
+    constexpr int NW = T / 32;
     __shared__ uint32_t tot[TK_BINS];
     __shared__ uint32_t sh_prefix, sh_match, sh_ncand;
     __shared__ int sh_remaining, sh_compacted;
-    __shared__ int sh_gt[TK_WARPS], sh_eq[TK_WARPS];
+    __shared__ int sh_gt[NW], sh_eq[NW];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int q = blockIdx.x;
-    const uint64_t pos = (a.n_seq == 1) ? a.pos0 + (uint64_t)q : dp.pos[q];
-    const int V = (int)((pos + 1) / 4);
-    const int k = a.k;
-    int32_t *out = a.topk + (size_t)q * k;
-    if (V <= k) {
-        for (int i = tid; i < k; i += TK_THREADS) out[i] = (i < V) ? i : -1;
-        return;
-    }
-    const float *s = a.scores + (size_t)q * a.lds;
-    if (RESIDENT) {
-        for (int base = 0; base < V; base += TK_THREADS * TK_UNR) {
-            float v[TK_UNR];
-#pragma unroll
-            for (int u = 0; u < TK_UNR; u++) {
-                const int i = base + u * TK_THREADS + tid;
-                if (i < V) v[u] = __ldcs(s + i);
-            }
-#pragma unroll
-            for (int u = 0; u < TK_UNR; u++) {
-                const int i = base + u * TK_THREADS + tid;
-                if (i < V) keys[i] = order_key(v[u]);
-            }
-        }
-    }
-    // key of visible row i
-    auto key_at = [&](int i) -> uint32_t { return RESIDENT ? keys[i] : order_key(__ldg(s + i)); };
     if (tid == 0) { sh_prefix = 0; sh_remaining = k; sh_compacted = 0; sh_ncand = 0; }
     __syncthreads();
-    // Radix select, 4 bits per pass from the top: the key K* of the k-th largest
-    // element and how many elements equal to K* to keep.  Counters are private
-    // to each thread (no atomics); once the keys that still match the resolved
-    // prefix fit in the candidate buffer, later passes scan only those.
     for (int shift = 28; shift >= 0; shift -= 4) {
 #pragma unroll
-        for (int d = 0; d < TK_BINS; d++) cnt[d * TK_THREADS + tid] = 0;
+        for (int d = 0; d < TK_BINS; d++) cnt[d * T + tid] = 0;
         const uint32_t prefix = sh_prefix;
         const uint32_t hmask = (shift == 28) ? 0u : (0xffffffffu << (shift + 4));
         if (sh_compacted) {
             const int n = (int)sh_ncand;
-            for (int i = tid; i < n; i += TK_THREADS) {
+            for (int i = tid; i < n; i += T) {
                 const uint32_t key = cand[i];
-                if ((key & hmask) == prefix) cnt[((key >> shift) & 15u) * TK_THREADS + tid] += 1u;
+                if ((key & hmask) == prefix) cnt[((key >> shift) & 15u) * T + tid] += 1u;
             }
         } else {
-            for (int base = 0; base < V; base += TK_THREADS * TK_UNR) {
+            for (int base = 0; base < V; base += T * TK_UNR) {
                 uint32_t kv[TK_UNR];
 #pragma unroll
                 for (int u = 0; u < TK_UNR; u++) {
-                    const int i = base + u * TK_THREADS + tid;
+                    const int i = base + u * T + tid;
                     kv[u] = (i < V) ? key_at(i) : 0u;
                 }
 #pragma unroll
                 for (int u = 0; u < TK_UNR; u++) {
-                    const int i = base + u * TK_THREADS + tid;
-                    if (i < V && (kv[u] & hmask) == prefix) cnt[((kv[u] >> shift) & 15u) * TK_THREADS + tid] += 1u;
+                    const int i = base + u * T + tid;
+                    if (i < V && (kv[u] & hmask) == prefix) cnt[((kv[u] >> shift) & 15u) * T + tid] += 1u;
                 }
             }
         }
         __syncthreads();
-        for (int bin = warp; bin < TK_BINS; bin += TK_WARPS) {
+        for (int bin = warp; bin < TK_BINS; bin += NW) {
             uint32_t v = 0;
-            for (int j = lane; j < TK_THREADS; j += 32) v += cnt[bin * TK_THREADS + j];
+            for (int j = lane; j < T; j += 32) v += cnt[bin * T + j];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
             if (lane == 0) tot[bin] = v;
@@ -361,10 +396,9 @@ __global__ void __launch_bounds__(TK_THREADS) topk_kernel(IndexerArgs a, DecodeP
             sh_match = tot[bin];
         }
         __syncthreads();
-        if (!sh_compacted && shift > 0 && sh_match <= (uint32_t)TK_CAND) {
-            // collect the keys that match the prefix resolved so far
+        if (!sh_compacted && shift > 0 && sh_match <= (uint32_t)TK_RCAND) {
             const uint32_t np = sh_prefix, nm = 0xffffffffu << shift;
-            for (int base = warp * 32; base < V; base += TK_THREADS) {
+            for (int base = warp * 32; base < V; base += T) {
                 const int c = base + lane;
                 const uint32_t key = (c < V) ? key_at(c) : 0u;
                 const bool hit = c < V && (key & nm) == np;
@@ -381,10 +415,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_kernel(IndexerArgs a, DecodeP
     }
     const uint32_t kstar = sh_prefix;
     const int remaining = sh_remaining;
-    // Ordered selection: keep key > K*, and the first `remaining` (by index) of
-    // key == K*.  Each warp owns a contiguous range of indices; one exchange of
-    // per-warp counts gives every warp its output offset.
-    const int per = ((V + TK_WARPS - 1) / TK_WARPS + 31) & ~31;
+    const int per = ((V + NW - 1) / NW + 31) & ~31;
     const int w0 = warp * per, w1 = min(V, w0 + per);
     int gt_w = 0, eq_w = 0;
     for (int base = w0; base < w1; base += 32) {
@@ -417,6 +448,216 @@ __global__ void __launch_bounds__(TK_THREADS) topk_kernel(IndexerArgs a, DecodeP
     }
 }
 
+// Query q: visible rows V = (pos + 1) / 4; fewer than k + 1 rows lists them all
+// and pads with -1.
+__device__ __forceinline__ bool tk_trivial(const IndexerArgs &a, int V, int32_t *out, int T) {
+    if (V > a.k) return false;
+    for (int i = threadIdx.x; i < a.k; i += T) out[i] = (i < V) ? i : -1;
+    return true;
+}
+
+template <int T, bool RESIDENT>
+__global__ void __launch_bounds__(T) topk_kernel(IndexerArgs a, DecodePos dp, int wcap) {
+    constexpr int NW = T / 32;
+    extern __shared__ uint32_t sm_tk[];
+    uint32_t *bins = sm_tk;
+    uint32_t *ckey = bins + tk_bin_words<T>();
+    uint32_t *crow = ckey + TK_CAND;
+    uint32_t *sel = crow + TK_CAND;
+    uint32_t *eqm = sel + wcap;
+    uint32_t *keys = eqm + wcap;                         // RESIDENT only
+    __shared__ uint32_t warp_a[NW], warp_b[NW], res[2], sh_nc;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int q = blockIdx.x;
+    const uint64_t pos = (a.n_seq == 1) ? a.pos0 + (uint64_t)q : dp.pos[q];
+    const int V = (int)((pos + 1) / 4);
+    const int k = a.k;
+    int32_t *out = a.topk + (size_t)q * k;
+    if (tk_trivial(a, V, out, T)) return;
+    const float *s = a.scores + (size_t)q * a.lds;
+    const int W = (V + 31) / 32;
+    for (int i = tid; i < TK_HBINS; i += T) bins[i] = 0;
+    for (int i = tid; i < W; i += T) eqm[i] = 0;
+    if (tid == 0) sh_nc = 0;
+    __syncthreads();
+    // 1. histogram of the top 12 key bits (resident: the keys land in shared memory)
+    constexpr int SH1 = 32 - TK_HBITS;
+    for (int base = 0; base < V; base += T * TK_UNR) {
+        float v[TK_UNR];
+#pragma unroll
+        for (int u = 0; u < TK_UNR; u++) {
+            const int i = base + u * T + tid;
+            v[u] = (i < V) ? (RESIDENT ? __ldcs(s + i) : __ldg(s + i)) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < TK_UNR; u++) {
+            const int i = base + u * T + tid;
+            if (i < V) {
+                const uint32_t key = order_key(v[u]);
+                if (RESIDENT) keys[i] = key;
+                atomicAdd(&bins[key >> SH1], 1u);
+            }
+        }
+    }
+    __syncthreads();
+    auto key_at = [&](int i) -> uint32_t { return RESIDENT ? keys[i] : order_key(__ldg(s + i)); };
+    tk_crossing<T>(bins, TK_HBINS, (uint32_t)k, warp_a, res);
+    const uint32_t bstar = res[0], rank1 = res[1];
+    const int nc = (int)bins[bstar];
+    if (nc > TK_CAND) {                                  // heavy ties in b*: plain radix select
+        __syncthreads();
+        tk_radix<T>(V, k, out, key_at, bins, ckey);
+        return;
+    }
+    // 2. rows above b* are selected, rows in b* become candidates; a warp's 32
+    //    rows are consecutive and 32-aligned, so its ballot is one bitmap word
+    for (int base = 0; base < V; base += T * TK_UNR) {
+        uint32_t kv[TK_UNR];
+#pragma unroll
+        for (int u = 0; u < TK_UNR; u++) {
+            const int i = base + u * T + tid;
+            kv[u] = (i < V) ? (RESIDENT ? keys[i] : order_key(__ldcs(s + i))) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < TK_UNR; u++) {
+            const int row0 = base + u * T + warp * 32;
+            if (row0 >= V) continue;                         // the whole warp is past the end
+            const int i = row0 + lane;
+            const bool in = i < V;
+            const uint32_t b = kv[u] >> SH1;
+            const unsigned above = __ballot_sync(0xffffffffu, in && b > bstar);
+            const bool hit = in && b == bstar;
+            const unsigned cm = __ballot_sync(0xffffffffu, hit);
+            if (lane == 0) sel[row0 >> 5] = above;
+            if (cm) {
+                uint32_t off = 0;
+                if (lane == 0) off = atomicAdd(&sh_nc, (uint32_t)__popc(cm));
+                off = __shfl_sync(0xffffffffu, off, 0);
+                if (hit) {
+                    const uint32_t o = off + __popc(cm & ((1u << lane) - 1u));
+                    ckey[o] = kv[u];
+                    crow[o] = (uint32_t)i;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    // 3. the low 20 bits among the candidates, 10 at a time
+    for (int i = tid; i < TK_LBINS; i += T) bins[i] = 0;
+    __syncthreads();
+    for (int j = tid; j < nc; j += T) atomicAdd(&bins[(ckey[j] >> 10) & 1023u], 1u);
+    __syncthreads();
+    tk_crossing<T>(bins, TK_LBINS, rank1, warp_a, res);
+    const uint32_t b1 = res[0], rank2 = res[1];
+    for (int i = tid; i < TK_LBINS; i += T) bins[i] = 0;
+    __syncthreads();
+    for (int j = tid; j < nc; j += T) {
+        const uint32_t key = ckey[j];
+        if (((key >> 10) & 1023u) == b1) atomicAdd(&bins[key & 1023u], 1u);
+    }
+    __syncthreads();
+    tk_crossing<T>(bins, TK_LBINS, rank2, warp_a, res);
+    const uint32_t kstar = (bstar << 20) | (b1 << 10) | res[0];
+    const uint32_t take_eq = res[1];                     // rows equal to K* to take, lowest first
+    // 4. candidates above K* join the selection, those equal to K* are marked apart
+    for (int j = tid; j < nc; j += T) {
+        const uint32_t key = ckey[j], r = crow[j];
+        if (key > kstar) atomicOr(&sel[r >> 5], 1u << (r & 31u));
+        else if (key == kstar) atomicOr(&eqm[r >> 5], 1u << (r & 31u));
+    }
+    __syncthreads();
+    // 5. in row order: each thread owns a run of bitmap words; an exclusive scan
+    //    of the per-thread counts gives its output offset and the equal-key rank
+    const int per = (W + T - 1) / T;
+    const int w0 = min(W, tid * per), w1 = min(W, w0 + per);
+    uint32_t cs = 0, ce = 0;
+    for (int w = w0; w < w1; w++) {
+        cs += __popc(sel[w]);
+        ce += __popc(eqm[w]);
+    }
+    uint32_t is = cs, ie = ce;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t vs = __shfl_up_sync(0xffffffffu, is, o), ve = __shfl_up_sync(0xffffffffu, ie, o);
+        if (lane >= o) { is += vs; ie += ve; }
+    }
+    if (lane == 31) { warp_a[warp] = is; warp_b[warp] = ie; }
+    __syncthreads();
+    for (int w = 0; w < warp; w++) { is += warp_a[w]; ie += warp_b[w]; }
+    uint32_t eq_before = ie - ce;
+    uint32_t dst = (is - cs) + min(eq_before, take_eq);
+    for (int w = w0; w < w1; w++) {
+        const uint32_t e_all = eqm[w];
+        uint32_t e = 0;
+        if (eq_before < take_eq) {
+            uint32_t want = take_eq - eq_before;
+            uint32_t rest = e_all;
+            while (rest && want) {                       // the lowest `want` equal rows of the word
+                const uint32_t lb = rest & (0u - rest);
+                e |= lb;
+                rest ^= lb;
+                want--;
+            }
+        }
+        eq_before += __popc(e_all);
+        uint32_t m = sel[w] | e;
+        while (m) {
+            out[dst++] = w * 32 + (__ffs(m) - 1);
+            m &= m - 1u;
+        }
+    }
+}
+
+// Radix path alone, for rows whose bitmaps would not fit shared memory.
+template <int T, bool RESIDENT>
+__global__ void __launch_bounds__(T) topk_radix_kernel(IndexerArgs a, DecodePos dp) {
+    extern __shared__ uint32_t sm_tk[];
+    uint32_t *cnt = sm_tk;
+    uint32_t *cand = cnt + TK_BINS * T;
+    uint32_t *keys = cand + TK_RCAND;                    // RESIDENT only
+    const int q = blockIdx.x;
+    const uint64_t pos = (a.n_seq == 1) ? a.pos0 + (uint64_t)q : dp.pos[q];
+    const int V = (int)((pos + 1) / 4);
+    int32_t *out = a.topk + (size_t)q * a.k;
+    if (tk_trivial(a, V, out, T)) return;
+    const float *s = a.scores + (size_t)q * a.lds;
+    if (RESIDENT) {
+        for (int i = threadIdx.x; i < V; i += T) keys[i] = order_key(__ldcs(s + i));
+        __syncthreads();
+    }
+    auto key_at = [&](int i) -> uint32_t { return RESIDENT ? keys[i] : order_key(__ldg(s + i)); };
+    tk_radix<T>(V, a.k, out, key_at, cnt, cand);
+}
+template <int T>
+size_t tk_radix_smem(uint64_t vmax, bool resident) {
+    return sizeof(uint32_t) * ((size_t)TK_BINS * T + TK_RCAND + (resident ? vmax : 0));
+}
+
+// Launch the top-k over n_q queries: the main path with its keys resident
+// when allowed and they fit, else in global memory, else the radix path.
+template <int T>
+cudaError_t launch_topk(const IndexerArgs &a, const DecodePos &dp, int n_q, uint64_t vmax, bool allow_resident,
+                        cudaStream_t s) {
+    constexpr size_t LIMIT = 200 * 1024;
+    if (vmax == 0) vmax = 1;
+    const int wcap = (int)((vmax + 31) / 32);
+    cudaError_t e;
+    if (allow_resident && tk_smem<T>(vmax, true) <= LIMIT) {
+        const size_t smem = tk_smem<T>(vmax, true);
+        if ((e = ensure_dyn_smem(topk_kernel<T, true>, smem)) != cudaSuccess) return e;
+        topk_kernel<T, true><<<n_q, T, smem, s>>>(a, dp, wcap);
+    } else if (tk_smem<T>(vmax, false) <= LIMIT) {
+        const size_t smem = tk_smem<T>(vmax, false);
+        if ((e = ensure_dyn_smem(topk_kernel<T, false>, smem)) != cudaSuccess) return e;
+        topk_kernel<T, false><<<n_q, T, smem, s>>>(a, dp, wcap);
+    } else {
+        const size_t smem = tk_radix_smem<T>(vmax, false);
+        if ((e = ensure_dyn_smem(topk_radix_kernel<T, false>, smem)) != cudaSuccess) return e;
+        topk_radix_kernel<T, false><<<n_q, T, smem, s>>>(a, dp);
+    }
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_indexer_prefill(const IndexerArgs &a, cudaStream_t s) {
@@ -428,12 +669,8 @@ cudaError_t launch_indexer_prefill(const IndexerArgs &a, cudaStream_t s) {
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    constexpr size_t smem = tk_fixed_smem<TK_PREFILL>();
-    cudaError_t e = ensure_dyn_smem(topk_kernel<TK_PREFILL, false>, smem);
-    if (e != cudaSuccess) return e;
     DecodePos dp{};
-    topk_kernel<TK_PREFILL, false><<<a.n_tok, TK_PREFILL, smem, s>>>(a, dp);
-    return cudaGetLastError();
+    return launch_topk<TK_PREFILL>(a, dp, a.n_tok, vis_max, false, s);
 }
 
 cudaError_t launch_indexer_decode(const IndexerArgs &a, const DecodePos &p, cudaStream_t s) {
@@ -486,17 +723,7 @@ cudaError_t launch_indexer_decode(const IndexerArgs &a, const DecodePos &p, cuda
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    const size_t smem = tk_fixed_smem<TK_DECODE>() + sizeof(uint32_t) * (size_t)(vis_max > 0 ? vis_max : 1);
-    if (smem <= (size_t)200 * 1024) {
-        e = ensure_dyn_smem(topk_kernel<TK_DECODE, true>, smem);
-        if (e != cudaSuccess) return e;
-        topk_kernel<TK_DECODE, true><<<a.n_seq, TK_DECODE, smem, s>>>(a, p);
-    } else {            // the keys do not fit: read them from the score rows each pass
-        e = ensure_dyn_smem(topk_kernel<TK_DECODE, false>, tk_fixed_smem<TK_DECODE>());
-        if (e != cudaSuccess) return e;
-        topk_kernel<TK_DECODE, false><<<a.n_seq, TK_DECODE, tk_fixed_smem<TK_DECODE>(), s>>>(a, p);
-    }
-    return cudaGetLastError();
+    return launch_topk<TK_DECODE>(a, p, a.n_seq, vis_max, true, s);
 }
 
 unsigned int idx_read_clear_error() {

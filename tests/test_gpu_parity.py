@@ -258,3 +258,78 @@ def test_checkpoint_restore_resumes_bit_exact(ratio, heads, D):
     fresh.checkpoint_gather(0, T1 + T2, gb)
     dl.sync()
     assert torch.equal(ga, gb)
+
+
+# ---------------------------------------------------------------------------
+# Top-k on crafted index rows: heavy ties (the radix path), a few distinct
+# scores (ties inside the boundary bin), signed zeros, V around k and across
+# the bitmap word boundaries; scores and lists bit-exact against the oracle
+# ---------------------------------------------------------------------------
+
+_TK_SHAPE = configs.LayerShape(d_model=256, head_dim=128, n_rot=64, idx_head_dim=64, n_heads=8, ratio=4, top_k=512,
+                               dtype="f32")
+_TK_CAP = 8200
+
+
+def _crafted_rows(kind, n, d, rng):
+    if kind in ("random", "zero_query"):
+        return rng.standard_normal((n, d)).astype(np.float32)
+    if kind == "all_equal":
+        return np.tile(rng.integers(-3, 4, d).astype(np.float32), (n, 1))
+    if kind == "few_values":
+        base = rng.integers(-3, 4, (5, d)).astype(np.float32)
+        return base[rng.integers(0, 5, n)]
+    if kind == "signed_zero":
+        r = np.zeros((n, d), np.float32)
+        r[:, 0] = rng.choice(np.array([-0.0, 0.0, 1.0, -1.0, 2.0], np.float32), n)
+        return r
+    raise ValueError(kind)
+
+
+def _crafted_queries(kind, n, d, rng):
+    if kind == "zero_query":
+        return np.zeros((n, d), np.float32)
+    if kind == "random":
+        return rng.standard_normal((n, d)).astype(np.float32)
+    return rng.integers(-2, 3, (n, d)).astype(np.float32)    # integer scores: ties stay exact
+
+
+@pytest.mark.parametrize("kind", ["random", "all_equal", "few_values", "signed_zero", "zero_query"])
+def test_topk_crafted_rows_prefill(kind):
+    shape = _TK_SHAPE
+    d, k = shape.idx_head_dim, shape.top_k
+    rng = np.random.default_rng(["random", "all_equal", "few_values", "signed_zero", "zero_query"].index(kind) + 70)
+    dl, _, _ = device_layer(shape, comp_cap=16, idx_cap=_TK_CAP, seed=5, max_rows=64)
+    dl.idx_comp[0] = torch.from_numpy(_crafted_rows(kind, _TK_CAP, d, rng)).cuda()
+    st = download(dl)
+    # V = (pos + 1) / 4 runs over k - 1 .. k + 4, 4094 .. 4098 and 8189 .. 8193
+    for pos0, T in ((4 * k - 5, 24), (4 * 4096 - 6, 16), (4 * 8190 - 3, 12)):
+        q_idx = _crafted_queries(kind, T, d, rng)
+        V = (pos0 + T) // 4
+        topk = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+        scores = torch.full((T, V), float("nan"), device="cuda")
+        dl.indexer_topk(torch.from_numpy(q_idx).cuda(), [pos0], 1, T, topk, scores, V)
+        dl.sync()
+        check_indexer_sampled(st, q_idx, [pos0 + j for j in range(T)], topk.cpu().numpy(), scores.cpu().numpy(),
+                              range(T))
+
+
+@pytest.mark.parametrize("kind", ["random", "all_equal", "few_values"])
+def test_topk_crafted_rows_decode(kind):
+    shape = _TK_SHAPE
+    d, k = shape.idx_head_dim, shape.top_k
+    rng = np.random.default_rng(["random", "all_equal", "few_values"].index(kind) + 90)
+    lens = [4 * k - 5, 4 * k + 3, 4095, 16383, 16390, 32770]       # V = 511, 513, 1024, 4096, 4097, 8192
+    B = len(lens)
+    dl, _, _ = device_layer(shape, comp_cap=16, idx_cap=_TK_CAP, n_seq=B, seed=5, max_rows=64)
+    for b in range(B):
+        dl.idx_comp[b] = torch.from_numpy(_crafted_rows(kind, _TK_CAP, d, rng)).cuda()
+    q_idx = _crafted_queries(kind, B, d, rng)
+    vmax = max((p + 1) // 4 for p in lens)
+    topk = torch.full((B, k), -7, dtype=torch.int32, device="cuda")
+    scores = torch.full((B, vmax), float("nan"), device="cuda")
+    dl.indexer_topk(torch.from_numpy(q_idx).cuda(), lens, B, 1, topk, scores, vmax)
+    dl.sync()
+    for b in range(B):
+        check_indexer_sampled(download(dl, b), q_idx[b:b + 1], [lens[b]], topk[b:b + 1].cpu().numpy(),
+                              scores[b:b + 1].cpu().numpy(), [0])
