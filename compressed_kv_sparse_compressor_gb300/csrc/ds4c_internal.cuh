@@ -31,6 +31,32 @@ inline cudaError_t ensure_dyn_smem(F *func, size_t bytes) {
     return e;
 }
 
+// Programmatic dependent launch.  Kernels launched by launch_pdl may be
+// scheduled while the previous kernel of the stream is still finishing, so
+// every such kernel calls pdl_wait() in each CTA before its first access to
+// global memory (and before any early return): it returns once the previous
+// kernel has completed and its writes are visible, which also orders every
+// earlier kernel.  pdl_launch_dependents() lets the next kernel be scheduled.
+// Under an ordinary launch both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // ----------------------------------------------------------------------------
 // Projection GEMM: C[g][m][n] = sum_k A[m][k] * B[g][n][k], fp32 out.
 // ----------------------------------------------------------------------------

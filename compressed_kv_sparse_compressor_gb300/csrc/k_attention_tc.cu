@@ -410,6 +410,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();
+    pdl_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -853,6 +855,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
 __global__ void raw_split_kernel(uint16_t *__restrict__ mirror, const float *__restrict__ ring,
                                  const float *__restrict__ raw_new, int D, int n_seq, int n_tok, uint64_t pos0,
                                  DecodePos dp) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int u = blockIdx.x;
     const float *src = nullptr;
     if (n_seq == 1) {
@@ -883,6 +887,8 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(float *__restrict__ o
                                                            DecodePos dp) {
     __shared__ float w[8];
     __shared__ float inv_den;
+    pdl_wait();
+    pdl_launch_dependents();
     const int n = blockIdx.x / H, h = blockIdx.x % H;
     // ring commit of the step (decode: query n is sequence n): the attention read the
     // ring through the raw mirror, so the slot can take the new row now
@@ -993,13 +999,11 @@ cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, cudaStream_t s
     if (e != cudaSuccess) return e;
     const int items = a.n_seq * a.n_tok * p.parts;
     const int grid = items < sm_count() ? items : sm_count();
-    attn_tc_kernel<H, D><<<grid, THREADS, Lay::SMEM, s>>>(rh, rl, qm, om, p);
-    e = cudaGetLastError();
+    e = launch_pdl(attn_tc_kernel<H, D>, dim3(grid), dim3(THREADS), Lay::SMEM, s, rh, rl, qm, om, p);
     if (e != cudaSuccess || p.parts == 1) return e;
-    attn_combine_kernel<<<a.n_seq * a.n_tok * H, 128, 0, s>>>(a.out, p.part_o, p.part_ml, H, D, p.parts,
-                                                              a.commit_ring ? const_cast<float *>(a.ring) : nullptr,
-                                                              a.raw_new, p.dp);
-    return cudaGetLastError();
+    return launch_pdl(attn_combine_kernel, dim3(a.n_seq * a.n_tok * H), dim3(128), 0, s, a.out,
+                      (const float *)p.part_o, (const float *)p.part_ml, H, D, p.parts,
+                      a.commit_ring ? const_cast<float *>(a.ring) : nullptr, a.raw_new, p.dp);
 }
 
 }  // namespace
@@ -1026,8 +1030,8 @@ cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *dp, cudaSt
     DecodePos dd{};
     if (a.n_seq > 1) dd = *dp;
     const int raw_rows = (a.n_seq == 1) ? ROWS + a.n_tok : a.n_seq * ROWS;
-    raw_split_kernel<<<raw_rows, 128, 0, s>>>(a.raw_mirror, a.ring, a.raw_new, a.D, a.n_seq, a.n_tok, a.pos0, dd);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(raw_split_kernel, dim3(raw_rows), dim3(128), 0, s, a.raw_mirror, a.ring, a.raw_new, a.D,
+                               a.n_seq, a.n_tok, a.pos0, dd);
     if (e != cudaSuccess) return e;
     TcAttnParams p{};
     p.out = a.out;

@@ -370,6 +370,8 @@ __global__ void commit_kernel(CompressArgs a, int lane_id, DecodePos dp, int dec
 template <int GA, int GI>
 __global__ void __launch_bounds__(128) compress_decode_r4_kernel(CompressArgs a, DecodePos dp) {
     __shared__ float red[32];
+    pdl_wait();
+    pdl_launch_dependents();
     const int seq = blockIdx.x, lane_id = blockIdx.y;
     if (lane_id == 0) pool_r4<GA>(a, 0, dp, 1, (threadIdx.x / GA == 0) ? seq : a.n_seg, red);
     else pool_r4<GI>(a, 1, dp, 1, (threadIdx.x / GI == 0) ? seq : a.n_seg, red);
@@ -432,8 +434,7 @@ cudaError_t launch_compress_decode(const CompressArgs &a, const DecodePos &p, in
         const dim3 grid((unsigned)n_seq, 2);
 #define DS4C_CDEC(A, I)                                                              \
         if (ga == A && gi == I) {                                                   \
-            compress_decode_r4_kernel<A, I><<<grid, 128, 0, s>>>(a, p);             \
-            return cudaGetLastError();                                              \
+            return launch_pdl(compress_decode_r4_kernel<A, I>, grid, dim3(128), 0, s, a, p); \
         }
         DS4C_CDEC(128, 32)
         DS4C_CDEC(128, 16)

@@ -215,6 +215,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     __syncthreads();
     fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();
+    pdl_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -358,6 +360,8 @@ int sm_count() {
 // over the whole [M][ldc] block the groups write into.
 __global__ void splitk_reduce_kernel(float *__restrict__ C, const float *__restrict__ part, int64_t n4, int64_t stride,
                                      int ksplit) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n4) return;
     float4 acc = reinterpret_cast<const float4 *>(part)[i];
@@ -414,12 +418,11 @@ cudaError_t launch_bn(const GemmArgs &a, cudaStream_t s) {
     cudaError_t e = ensure_dyn_smem(gemm_tc_kernel<BN, AR>, G::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int grid = start < sm_count() ? start : sm_count();
-    gemm_tc_kernel<BN, AR><<<grid, THREADS, G::SMEM_BYTES, s>>>(mA, mB[0], mB[1], mB[2], mB[3], p);
-    e = cudaGetLastError();
+    e = launch_pdl(gemm_tc_kernel<BN, AR>, dim3(grid), dim3(THREADS), G::SMEM_BYTES, s, mA, mB[0], mB[1], mB[2], mB[3], p);
     if (e != cudaSuccess || ksplit == 1) return e;
     const int64_t n4 = (int64_t)a.M * a.part_ld / 4;
-    splitk_reduce_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(a.c_base, a.part, n4, p.part_stride, ksplit);
-    return cudaGetLastError();
+    return launch_pdl(splitk_reduce_kernel, dim3((unsigned)((n4 + 255) / 256)), dim3(256), 0, s, a.c_base,
+                      (const float *)a.part, n4, p.part_stride, ksplit);
 }
 
 }  // namespace

@@ -25,20 +25,23 @@ namespace {
 
 // ---------------------------------------------------------------------------
 // K4 prefill: n_tok queries of one sequence against every visible row.  128 x
-// 128 (query x row) tile per 256-thread block, 8 x 8 outputs per thread, d
-// consumed in 16-wide slices in index order (so each output is exactly the
-// in-order fmaf chain), slices double-buffered in shared memory (k-major, so
-// a thread reads its 8 queries / 8 rows of one k as two 16-byte loads).
-// Tiles wholly past the visibility triangle are skipped.
+// 128 (query x row) tile per 128-thread block, 8 queries x 16 rows per thread,
+// d consumed in 16-wide slices in index order (so each output is exactly the
+// in-order fmaf chain), slices double-buffered in shared memory, k-major.
+// Shared-memory delivery (32 floats per clock per SM) against the FMA pipe
+// (128 per clock) sets the register tile: 24 operands per 128 FMAs per k.  A
+// thread's rows are tx*4 + 32g + (0..3), g < 4, so the eight threads of a
+// quarter-warp read one 128-byte line of the row slice and share the query
+// values.  Tiles wholly past the visibility triangle are skipped.
 // ---------------------------------------------------------------------------
-constexpr int SB = 128, SK = 16, SP = SB + 4;
+constexpr int SB = 128, SK = 16, SP = SB + 4, ST = 128;
 
-// 128 rows x 16 k of q and of the index rows: 512 float4 each, 2 per thread
-__device__ __forceinline__ void fetch_slice(float4 (&qv)[2], float4 (&rv)[2], const IndexerArgs &a, int j0, int c0,
+// 128 queries x 16 d and 128 rows x 16 d: 512 float4 each, 4 per thread
+__device__ __forceinline__ void fetch_slice(float4 (&qv)[4], float4 (&rv)[4], const IndexerArgs &a, int j0, int c0,
                                             uint64_t vis_max, int i0) {
 #pragma unroll
-    for (int h = 0; h < 2; h++) {
-        const int f = threadIdx.x + 256 * h;
+    for (int h = 0; h < 4; h++) {
+        const int f = threadIdx.x + ST * h;
         const int r = f >> 2, k4 = (f & 3) * 4;
         const int j = j0 + r, c = c0 + r;
         qv[h] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -47,30 +50,30 @@ __device__ __forceinline__ void fetch_slice(float4 (&qv)[2], float4 (&rv)[2], co
         if ((uint64_t)c < vis_max) rv[h] = *reinterpret_cast<const float4 *>(a.rows + (size_t)c * a.d + i0 + k4);
     }
 }
-__device__ __forceinline__ void store_slice(float (*As)[SP], float (*Bs)[SP], const float4 (&qv)[2], const float4 (&rv)[2]) {
+__device__ __forceinline__ void store_slice(float (*As)[SP], float (*Bs)[SP], const float4 (&qv)[4], const float4 (&rv)[4]) {
 #pragma unroll
-    for (int h = 0; h < 2; h++) {
-        const int f = threadIdx.x + 256 * h;
+    for (int h = 0; h < 4; h++) {
+        const int f = threadIdx.x + ST * h;
         const int r = f >> 2, k4 = (f & 3) * 4;
         As[k4 + 0][r] = qv[h].x; As[k4 + 1][r] = qv[h].y; As[k4 + 2][r] = qv[h].z; As[k4 + 3][r] = qv[h].w;
         Bs[k4 + 0][r] = rv[h].x; Bs[k4 + 1][r] = rv[h].y; Bs[k4 + 2][r] = rv[h].z; Bs[k4 + 3][r] = rv[h].w;
     }
 }
 
-__global__ void __launch_bounds__(256, 2) score_prefill_kernel(IndexerArgs a) {
+__global__ void __launch_bounds__(ST, 2) score_prefill_kernel(IndexerArgs a) {
     const int j0 = blockIdx.y * SB, c0 = blockIdx.x * SB;
     const int jlast = min(j0 + SB, a.n_tok) - 1;
     const uint64_t vis_max = (a.pos0 + (uint64_t)jlast + 1) / 4;
     if ((uint64_t)c0 >= vis_max) return;
     __shared__ __align__(16) float As[2][SK][SP];
     __shared__ __align__(16) float Bs[2][SK][SP];
-    const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-    float acc[8][8];
+    const int tx = threadIdx.x % 8, ty = threadIdx.x / 8;
+    float acc[8][16];
 #pragma unroll
     for (int i = 0; i < 8; i++)
 #pragma unroll
-        for (int k = 0; k < 8; k++) acc[i][k] = 0.f;
-    float4 qv[2], rv[2];
+        for (int n = 0; n < 16; n++) acc[i][n] = 0.f;
+    float4 qv[4], rv[4];
     fetch_slice(qv, rv, a, j0, c0, vis_max, 0);
     store_slice(As[0], Bs[0], qv, rv);
     __syncthreads();
@@ -82,32 +85,39 @@ __global__ void __launch_bounds__(256, 2) score_prefill_kernel(IndexerArgs a) {
         for (int kk = 0; kk < SK; kk++) {
             const float4 a0 = *reinterpret_cast<const float4 *>(&As[cur][kk][ty * 8]);
             const float4 a1 = *reinterpret_cast<const float4 *>(&As[cur][kk][ty * 8 + 4]);
-            const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[cur][kk][tx * 8]);
-            const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[cur][kk][tx * 8 + 4]);
+            float rb[16];
+#pragma unroll
+            for (int g = 0; g < 4; g++) {
+                const float4 b = *reinterpret_cast<const float4 *>(&Bs[cur][kk][32 * g + tx * 4]);
+                rb[4 * g + 0] = b.x; rb[4 * g + 1] = b.y; rb[4 * g + 2] = b.z; rb[4 * g + 3] = b.w;
+            }
             const float qa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float rb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
             for (int i = 0; i < 8; i++)
 #pragma unroll
-                for (int k = 0; k < 8; k++) acc[i][k] = __fmaf_rn(qa[i], rb[k], acc[i][k]);
+                for (int n = 0; n < 16; n++) acc[i][n] = __fmaf_rn(qa[i], rb[n], acc[i][n]);
         }
         if (sl + 1 < nslices) store_slice(As[cur ^ 1], Bs[cur ^ 1], qv, rv);
         __syncthreads();
     }
+    const bool vec = (a.lds % 4) == 0;
 #pragma unroll
     for (int i = 0; i < 8; i++) {
         const int j = j0 + ty * 8 + i;
         if (j >= a.n_tok) continue;
         const uint64_t vis = (a.pos0 + (uint64_t)j + 1) / 4;
         float *dst = a.scores + (size_t)j * a.lds;
-        const int cb = c0 + tx * 8;
-        if ((uint64_t)cb + 8 <= vis && (a.lds % 4) == 0) {
-            *reinterpret_cast<float4 *>(dst + cb) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-            *reinterpret_cast<float4 *>(dst + cb + 4) = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
-        } else {
 #pragma unroll
-            for (int k = 0; k < 8; k++)
-                if ((uint64_t)(cb + k) < vis) dst[cb + k] = acc[i][k];
+        for (int g = 0; g < 4; g++) {
+            const int cb = c0 + 32 * g + tx * 4;
+            if (vec && (uint64_t)cb + 4 <= vis) {
+                *reinterpret_cast<float4 *>(dst + cb) =
+                    make_float4(acc[i][4 * g], acc[i][4 * g + 1], acc[i][4 * g + 2], acc[i][4 * g + 3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; e++)
+                    if ((uint64_t)(cb + e) < vis) dst[cb + e] = acc[i][4 * g + e];
+            }
         }
     }
 }
@@ -121,6 +131,8 @@ __global__ void __launch_bounds__(256, 2) score_prefill_kernel(IndexerArgs a) {
 template <int DD>
 __global__ void __launch_bounds__(128) score_decode_kernel(IndexerArgs a, DecodePos dp) {
     __shared__ float qs[DD];
+    pdl_wait();
+    pdl_launch_dependents();
     const int b = blockIdx.y;
     const uint64_t vis = (dp.pos[b] + 1) / 4;
     const int c = blockIdx.x * 128 + threadIdx.x;
@@ -169,6 +181,8 @@ __global__ void __launch_bounds__(128) score_decode_tma_kernel(const __grid_cons
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~(uintptr_t)1023);
     __shared__ uint64_t bar;
     __shared__ float qs[DD];
+    pdl_wait();
+    pdl_launch_dependents();
     const int b = blockIdx.y;
     const uint64_t vis = (dp.pos[b] + 1) / 4;
     const int c0 = blockIdx.x * 128;
@@ -467,6 +481,8 @@ __global__ void __launch_bounds__(T) topk_kernel(IndexerArgs a, DecodePos dp, in
     uint32_t *eqm = sel + wcap;
     uint32_t *keys = eqm + wcap;                         // RESIDENT only
     __shared__ uint32_t warp_a[NW], warp_b[NW], res[2], sh_nc;
+    pdl_wait();
+    pdl_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int q = blockIdx.x;
     const uint64_t pos = (a.n_seq == 1) ? a.pos0 + (uint64_t)q : dp.pos[q];
@@ -615,6 +631,8 @@ __global__ void __launch_bounds__(T) topk_radix_kernel(IndexerArgs a, DecodePos 
     uint32_t *cnt = sm_tk;
     uint32_t *cand = cnt + TK_BINS * T;
     uint32_t *keys = cand + TK_RCAND;                    // RESIDENT only
+    pdl_wait();
+    pdl_launch_dependents();
     const int q = blockIdx.x;
     const uint64_t pos = (a.n_seq == 1) ? a.pos0 + (uint64_t)q : dp.pos[q];
     const int V = (int)((pos + 1) / 4);
@@ -645,17 +663,16 @@ cudaError_t launch_topk(const IndexerArgs &a, const DecodePos &dp, int n_q, uint
     if (allow_resident && tk_smem<T>(vmax, true) <= LIMIT) {
         const size_t smem = tk_smem<T>(vmax, true);
         if ((e = ensure_dyn_smem(topk_kernel<T, true>, smem)) != cudaSuccess) return e;
-        topk_kernel<T, true><<<n_q, T, smem, s>>>(a, dp, wcap);
+        return launch_pdl(topk_kernel<T, true>, dim3(n_q), dim3(T), smem, s, a, dp, wcap);
     } else if (tk_smem<T>(vmax, false) <= LIMIT) {
         const size_t smem = tk_smem<T>(vmax, false);
         if ((e = ensure_dyn_smem(topk_kernel<T, false>, smem)) != cudaSuccess) return e;
-        topk_kernel<T, false><<<n_q, T, smem, s>>>(a, dp, wcap);
+        return launch_pdl(topk_kernel<T, false>, dim3(n_q), dim3(T), smem, s, a, dp, wcap);
     } else {
         const size_t smem = tk_radix_smem<T>(vmax, false);
         if ((e = ensure_dyn_smem(topk_radix_kernel<T, false>, smem)) != cudaSuccess) return e;
-        topk_radix_kernel<T, false><<<n_q, T, smem, s>>>(a, dp);
+        return launch_pdl(topk_radix_kernel<T, false>, dim3(n_q), dim3(T), smem, s, a, dp);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace
@@ -665,7 +682,7 @@ cudaError_t launch_indexer_prefill(const IndexerArgs &a, cudaStream_t s) {
     if (a.n_tok <= 0) return cudaSuccess;
     if (vis_max > 0) {
         dim3 grid((unsigned)((vis_max + SB - 1) / SB), (unsigned)((a.n_tok + SB - 1) / SB));
-        score_prefill_kernel<<<grid, 256, 0, s>>>(a);
+        score_prefill_kernel<<<grid, ST, 0, s>>>(a);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -699,7 +716,8 @@ cudaError_t launch_indexer_decode(const IndexerArgs &a, const DecodePos &p, cuda
     case dd:                                                                                                 \
         e = ensure_dyn_smem(score_decode_tma_kernel<dd>, smem);                                              \
         if (e != cudaSuccess) return e;                                                                      \
-        score_decode_tma_kernel<dd><<<grid, 128, smem, s>>>(rm, a, p, (int)idx_cap);                          \
+        e = launch_pdl(score_decode_tma_kernel<dd>, grid, dim3(128), smem, s, rm, a, p, (int)idx_cap);       \
+        if (e != cudaSuccess) return e;                                                                      \
         break;
         switch (a.d) {
             DS4C_SCORE_TMA(32)
@@ -714,10 +732,10 @@ cudaError_t launch_indexer_decode(const IndexerArgs &a, const DecodePos &p, cuda
     } else if (vis_max > 0) {
         dim3 grid((unsigned)((vis_max + 127) / 128), (unsigned)a.n_seq);
         switch (a.d) {
-            case 64: score_decode_kernel<64><<<grid, 128, 0, s>>>(a, p); break;
-            case 128: score_decode_kernel<128><<<grid, 128, 0, s>>>(a, p); break;
-            case 256: score_decode_kernel<256><<<grid, 128, 0, s>>>(a, p); break;
-            case 512: score_decode_kernel<512><<<grid, 128, 0, s>>>(a, p); break;
+            case 64: e = launch_pdl(score_decode_kernel<64>, grid, dim3(128), 0, s, a, p); break;
+            case 128: e = launch_pdl(score_decode_kernel<128>, grid, dim3(128), 0, s, a, p); break;
+            case 256: e = launch_pdl(score_decode_kernel<256>, grid, dim3(128), 0, s, a, p); break;
+            case 512: e = launch_pdl(score_decode_kernel<512>, grid, dim3(128), 0, s, a, p); break;
             default: return cudaErrorInvalidValue;
         }
         e = cudaGetLastError();
