@@ -32,7 +32,7 @@ from compressed_kv_sparse_compressor_gb300 import configs  # noqa: E402
 METRIC = "prefill tokens/s per layer"
 # dram__bytes_read.sum + dram__bytes_write.sum of one attention launch (4096 queries), from the ncu capture
 # in profiles/kernels_prefill_8192tok_chunk2_full.md; set to None when the kernel changes until re-captured
-ATTN_TRAFFIC = 557460224 + 483186432   # dram__bytes_read.sum + dram__bytes_write.sum, one launch
+ATTN_TRAFFIC = 558503424 + 483813632   # dram__bytes_read.sum + dram__bytes_write.sum, one launch
 ATTN_TRAFFIC_SRC = "ncu, one 4096-query launch of the 8192-token case (same units per launch as C5)"
 UNIT = "tokens/s"
 
@@ -370,7 +370,7 @@ def run_e2e(pf, args, device):
     dev_in, dev_out = pf.inputs(), pf.outputs()
     s_up, s_comp, s_down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     dl = pf.dl
-    steps = max(1, min(args.steps, 2))
+    steps = max(1, min(args.steps, 3))
 
     def one_step():
         with torch.cuda.stream(s_comp):
@@ -405,16 +405,19 @@ def run_e2e(pf, args, device):
 
     one_step()                      # warm-up of the streams and the pinned buffers
     torch.cuda.synchronize()
+    each = []
     t0 = time.perf_counter()
     for _ in range(steps):
-        one_step()
+        t1 = time.perf_counter()
+        one_step()                  # ends with a device synchronize
+        each.append((time.perf_counter() - t1) * 1e3)
     torch.cuda.synchronize()
     ms = (time.perf_counter() - t0) * 1e3 / steps
     dl.sync()
     bi = sum(t.numel() * t.element_size() for t in host_in)
     bo = sum(t.numel() * t.element_size() for t in host_out)
     return {"value": round(pf.T / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-            "ms_per_step": round(ms, 3), "steps": steps,
+            "ms_per_step": round(ms, 3), "ms_each_step": [round(x, 1) for x in each], "steps": steps,
             "pipeline": "per chunk: upload, compute and download on three streams"}
 
 

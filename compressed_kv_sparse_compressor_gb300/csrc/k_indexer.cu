@@ -32,7 +32,10 @@ namespace {
 // (128 per clock) sets the register tile: 24 operands per 128 FMAs per k.  A
 // thread's rows are tx*4 + 32g + (0..3), g < 4, so the eight threads of a
 // quarter-warp read one 128-byte line of the row slice and share the query
-// values.  Tiles wholly past the visibility triangle are skipped.
+// values.  The FMAs are packed (fma.rn.f32x2: two independent round-to-nearest
+// fmas, one per lane half) over pairs of rows, which halves the issue slots
+// the chain takes; each output is still its own in-order fmaf chain.  Tiles
+// wholly past the visibility triangle are skipped.
 // ---------------------------------------------------------------------------
 constexpr int SB = 128, SK = 16, SP = SB + 4, ST = 128;
 
@@ -60,6 +63,16 @@ __device__ __forceinline__ void store_slice(float (*As)[SP], float (*Bs)[SP], co
     }
 }
 
+// two floats as the halves of one 64-bit register pair, and back
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
 __global__ void __launch_bounds__(ST, 2) score_prefill_kernel(IndexerArgs a) {
     const int j0 = blockIdx.y * SB, c0 = blockIdx.x * SB;
     const int jlast = min(j0 + SB, a.n_tok) - 1;
@@ -68,11 +81,11 @@ __global__ void __launch_bounds__(ST, 2) score_prefill_kernel(IndexerArgs a) {
     __shared__ __align__(16) float As[2][SK][SP];
     __shared__ __align__(16) float Bs[2][SK][SP];
     const int tx = threadIdx.x % 8, ty = threadIdx.x / 8;
-    float acc[8][16];
+    uint64_t acc2[8][8];          // rows (2m, 2m+1) of query i, one packed pair
 #pragma unroll
     for (int i = 0; i < 8; i++)
 #pragma unroll
-        for (int n = 0; n < 16; n++) acc[i][n] = 0.f;
+        for (int m = 0; m < 8; m++) acc2[i][m] = 0ull;
     float4 qv[4], rv[4];
     fetch_slice(qv, rv, a, j0, c0, vis_max, 0);
     store_slice(As[0], Bs[0], qv, rv);
@@ -85,21 +98,29 @@ __global__ void __launch_bounds__(ST, 2) score_prefill_kernel(IndexerArgs a) {
         for (int kk = 0; kk < SK; kk++) {
             const float4 a0 = *reinterpret_cast<const float4 *>(&As[cur][kk][ty * 8]);
             const float4 a1 = *reinterpret_cast<const float4 *>(&As[cur][kk][ty * 8 + 4]);
-            float rb[16];
+            uint64_t rr[8];
 #pragma unroll
             for (int g = 0; g < 4; g++) {
                 const float4 b = *reinterpret_cast<const float4 *>(&Bs[cur][kk][32 * g + tx * 4]);
-                rb[4 * g + 0] = b.x; rb[4 * g + 1] = b.y; rb[4 * g + 2] = b.z; rb[4 * g + 3] = b.w;
+                rr[2 * g] = pack2(b.x, b.y);
+                rr[2 * g + 1] = pack2(b.z, b.w);
             }
             const float qa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-            for (int i = 0; i < 8; i++)
+            for (int i = 0; i < 8; i++) {
+                const uint64_t qq = pack2(qa[i], qa[i]);
 #pragma unroll
-                for (int n = 0; n < 16; n++) acc[i][n] = __fmaf_rn(qa[i], rb[n], acc[i][n]);
+                for (int m = 0; m < 8; m++) asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[i][m]) : "l"(qq), "l"(rr[m]));
+            }
         }
         if (sl + 1 < nslices) store_slice(As[cur ^ 1], Bs[cur ^ 1], qv, rv);
         __syncthreads();
     }
+    float acc[8][16];
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+#pragma unroll
+        for (int m = 0; m < 8; m++) unpack2(acc2[i][m], acc[i][2 * m], acc[i][2 * m + 1]);
     const bool vec = (a.lds % 4) == 0;
 #pragma unroll
     for (int i = 0; i < 8; i++) {
