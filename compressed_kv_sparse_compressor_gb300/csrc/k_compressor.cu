@@ -209,6 +209,8 @@ __device__ __forceinline__ void pool_r4(const CompressArgs &a, int lane_id, cons
 template <int G>
 __global__ void __launch_bounds__(128) compress_r4_kernel(CompressArgs a, int lane_id, DecodePos dp, int decode) {
     __shared__ float red[32];
+    pdl_wait();
+    pdl_launch_dependents();
     pool_r4<G>(a, lane_id, dp, decode, blockIdx.x * (128 / G) + threadIdx.x / G, red);
 }
 
@@ -219,6 +221,8 @@ __global__ void __launch_bounds__(G * 4) compress_r128_kernel(CompressArgs a, in
     constexpr int NS = 4;
     __shared__ float4 part[3][NS][G];
     __shared__ float red[32];
+    pdl_wait();
+    pdl_launch_dependents();
     const LaneArgs L = a.lane[lane_id];
     const int W = L.Dl;
     const int split = threadIdx.x / G;
@@ -354,6 +358,8 @@ __device__ __forceinline__ void commit_col(const CompressArgs &a, int lane_id, c
 }
 
 __global__ void commit_kernel(CompressArgs a, int lane_id, DecodePos dp, int decode) {
+    pdl_wait();
+    pdl_launch_dependents();
     const LaneArgs &L = a.lane[lane_id];
     const int W = (a.ratio == 4 ? 2 : 1) * L.Dl;
     const int col = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
@@ -387,29 +393,26 @@ cudaError_t pool_lane(const CompressArgs &a, int lane, const DecodePos &dp, int 
         int G = Dl / 4;
         int blocks = (n_tasks * G + 127) / 128;
         switch (G) {
-            case 16: compress_r4_kernel<16><<<blocks, 128, 0, s>>>(a, lane, dp, decode); break;
-            case 32: compress_r4_kernel<32><<<blocks, 128, 0, s>>>(a, lane, dp, decode); break;
-            case 64: compress_r4_kernel<64><<<blocks, 128, 0, s>>>(a, lane, dp, decode); break;
-            case 128: compress_r4_kernel<128><<<blocks, 128, 0, s>>>(a, lane, dp, decode); break;
-            default: return cudaErrorInvalidValue;
-        }
-    } else {
-        switch (Dl / 4) {
-            case 16: compress_r128_kernel<16><<<n_tasks, 64, 0, s>>>(a, lane, dp, decode); break;
-            case 32: compress_r128_kernel<32><<<n_tasks, 128, 0, s>>>(a, lane, dp, decode); break;
-            case 64: compress_r128_kernel<64><<<n_tasks, 256, 0, s>>>(a, lane, dp, decode); break;
-            case 128: compress_r128_kernel<128><<<n_tasks, 512, 0, s>>>(a, lane, dp, decode); break;
+            case 16: return launch_pdl(compress_r4_kernel<16>, dim3(blocks), dim3(128), 0, s, a, lane, dp, decode);
+            case 32: return launch_pdl(compress_r4_kernel<32>, dim3(blocks), dim3(128), 0, s, a, lane, dp, decode);
+            case 64: return launch_pdl(compress_r4_kernel<64>, dim3(blocks), dim3(128), 0, s, a, lane, dp, decode);
+            case 128: return launch_pdl(compress_r4_kernel<128>, dim3(blocks), dim3(128), 0, s, a, lane, dp, decode);
             default: return cudaErrorInvalidValue;
         }
     }
-    return cudaGetLastError();
+    switch (Dl / 4) {
+        case 16: return launch_pdl(compress_r128_kernel<16>, dim3(n_tasks), dim3(64), 0, s, a, lane, dp, decode);
+        case 32: return launch_pdl(compress_r128_kernel<32>, dim3(n_tasks), dim3(128), 0, s, a, lane, dp, decode);
+        case 64: return launch_pdl(compress_r128_kernel<64>, dim3(n_tasks), dim3(256), 0, s, a, lane, dp, decode);
+        case 128: return launch_pdl(compress_r128_kernel<128>, dim3(n_tasks), dim3(512), 0, s, a, lane, dp, decode);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t commit_lane(const CompressArgs &a, int lane, const DecodePos &dp, int decode, int n_seg, cudaStream_t s) {
     const int W = (a.ratio == 4 ? 2 : 1) * a.lane[lane].Dl;
     dim3 grid((W / 4 + 127) / 128, decode ? n_seg : 1);
-    commit_kernel<<<grid, 128, 0, s>>>(a, lane, dp, decode);
-    return cudaGetLastError();
+    return launch_pdl(commit_kernel, grid, dim3(128), 0, s, a, lane, dp, decode);
 }
 
 }  // namespace

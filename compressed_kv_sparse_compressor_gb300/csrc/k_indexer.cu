@@ -74,6 +74,8 @@ __device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi) {
 }
 
 __global__ void __launch_bounds__(ST, 2) score_prefill_kernel(IndexerArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int j0 = blockIdx.y * SB, c0 = blockIdx.x * SB;
     const int jlast = min(j0 + SB, a.n_tok) - 1;
     const uint64_t vis_max = (a.pos0 + (uint64_t)jlast + 1) / 4;
@@ -314,7 +316,7 @@ constexpr int TK_LBINS = 1024;       // main path: 10-bit candidate passes
 constexpr int TK_CAND = 2048;        // main path: candidate list (key, row)
 constexpr int TK_BINS = 16;          // radix path: 4-bit digits
 constexpr int TK_RCAND = 4096;       // radix path: survivors compacted once they fit
-constexpr int TK_UNR = 8;            // independent score loads in flight per thread
+constexpr int TK_UNR = 16;           // independent score loads in flight per thread
 constexpr int TK_PREFILL = 256, TK_DECODE = 1024;
 
 // Dynamic shared memory in u32 words:
@@ -703,8 +705,7 @@ cudaError_t launch_indexer_prefill(const IndexerArgs &a, cudaStream_t s) {
     if (a.n_tok <= 0) return cudaSuccess;
     if (vis_max > 0) {
         dim3 grid((unsigned)((vis_max + SB - 1) / SB), (unsigned)((a.n_tok + SB - 1) / SB));
-        score_prefill_kernel<<<grid, ST, 0, s>>>(a);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_pdl(score_prefill_kernel, grid, dim3(ST), 0, s, a);
         if (e != cudaSuccess) return e;
     }
     DecodePos dp{};

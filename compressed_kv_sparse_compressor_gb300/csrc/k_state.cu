@@ -26,6 +26,8 @@ __global__ void fill_kernel(float *__restrict__ p, size_t n, float v) {
 // last min(n_tok, S) rows of the chunk.  Decode: one row per sequence.
 __global__ void ring_commit_kernel(float *__restrict__ ring, const float *__restrict__ raw_new, int D, int S,
                                    int n_seq, int n_tok, uint64_t pos0, DecodePos dp) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int r = blockIdx.x;                  // row within the committed set
     uint64_t p;
     const float *src;
@@ -153,8 +155,7 @@ cudaError_t launch_ring_commit(float *ring, const float *raw_new, int D, int S, 
     int threads = D / 4 < 128 ? D / 4 : 128;
     DecodePos dp{};
     if (n_seq > 1) dp = *p;
-    ring_commit_kernel<<<rows, threads, 0, s>>>(ring, raw_new, D, S, n_seq, n_tok, pos0, dp);
-    return cudaGetLastError();
+    return launch_pdl(ring_commit_kernel, dim3(rows), dim3(threads), 0, s, ring, raw_new, D, S, n_seq, n_tok, pos0, dp);
 }
 
 cudaError_t launch_gather(const GatherArgs &a, cudaStream_t s) {
