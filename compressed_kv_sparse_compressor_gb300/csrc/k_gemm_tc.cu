@@ -381,14 +381,27 @@ cudaError_t launch_bn(const GemmArgs &a, cudaStream_t s) {
     p.K = a.K;
     p.m_tiles = (a.M + BM - 1) / BM;
     p.n_groups = a.n_groups;
-    // split K when the output tiles alone leave most SMs idle and a partial buffer is given
+    // split K when a partial buffer is given: the split count with the shortest
+    // critical path, rounds of work units over the SMs times the time of one unit
+    // (its k-blocks plus about two k-blocks of tile setup and partial epilogue);
+    // ties go to fewer splits; every split gets at least 4 k-blocks, none is empty
     int ksplit = 1;
     if (a.part && a.c_base) {
         int out_tiles = 0;
         for (int g = 0; g < a.n_groups; g++) out_tiles += p.m_tiles * ((a.g[g].N + BN - 1) / BN);
         const int kb_count = (a.K + BK - 1) / BK;
-        while (ksplit * 2 <= a.max_ksplit && out_tiles * ksplit * 2 <= 2 * sm_count() && kb_count / (ksplit * 2) >= 4)
-            ksplit *= 2;
+        const int sms = sm_count();
+        constexpr int UNIT_COST = 2;
+        long best = (long)((out_tiles + sms - 1) / sms) * (kb_count + UNIT_COST);
+        for (int k = 2; k <= a.max_ksplit; k++) {
+            const int kb_per = (kb_count + k - 1) / k;
+            if (kb_per < 4 || (k - 1) * kb_per >= kb_count) continue;
+            const long cost = (long)((out_tiles * k + sms - 1) / sms) * (kb_per + UNIT_COST);
+            if (cost < best) {
+                best = cost;
+                ksplit = k;
+            }
+        }
     }
     p.ksplit = ksplit;
     p.part_stride = (int64_t)a.M * a.part_ld;
