@@ -312,7 +312,6 @@ __device__ __forceinline__ uint32_t order_key(float s) {
 
 constexpr int TK_HBITS = 12;         // main path: bits of the first histogram
 constexpr int TK_HBINS = 1 << TK_HBITS;
-constexpr int TK_LBINS = 1024;       // main path: 10-bit candidate passes
 constexpr int TK_CAND = 2048;        // main path: candidate list (key, row)
 constexpr int TK_BINS = 16;          // radix path: 4-bit digits
 constexpr int TK_RCAND = 4096;       // radix path: survivors compacted once they fit
@@ -485,6 +484,84 @@ __device__ void tk_radix(int V, int k, int32_t *out, KeyAt key_at, uint32_t *cnt
     }
 }
 
+// One histogram pass over the candidate keys ckey[0, nc): bins of key bits
+// [lo, lo + nbits) among the keys whose bits above them equal `match` (every
+// key when `all`), then the crossing for the need-th largest (res[0] = bin,
+// res[1] = rank in the bin).  Ends on a barrier.
+template <int T>
+__device__ __forceinline__ void tk_cand_pass(uint32_t *bins, const uint32_t *ckey, int nc, int nbits, int lo, bool all,
+                                             uint32_t match, uint32_t need, uint32_t *warp_a, uint32_t *res) {
+    const int nb = 1 << nbits;
+    for (int i = threadIdx.x; i < nb; i += T) bins[i] = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < nc; j += T) {
+        const uint32_t key = ckey[j];
+        if (all || (key >> (lo + nbits)) == match) atomicAdd(&bins[(key >> lo) & (uint32_t)(nb - 1)], 1u);
+    }
+    __syncthreads();
+    tk_crossing<T>(bins, nb, need, warp_a, res);
+}
+
+// Candidates above K* join the selection bitmap, those equal to K* go to the
+// equal-key bitmap.  Ends on a barrier.
+template <int T>
+__device__ __forceinline__ void tk_mark(const uint32_t *ckey, const uint32_t *crow, int nc, uint32_t kstar, uint32_t *sel,
+                                        uint32_t *eqm) {
+    for (int j = threadIdx.x; j < nc; j += T) {
+        const uint32_t key = ckey[j], r = crow[j];
+        if (key > kstar) atomicOr(&sel[r >> 5], 1u << (r & 31u));
+        else if (key == kstar) atomicOr(&eqm[r >> 5], 1u << (r & 31u));
+    }
+    __syncthreads();
+}
+
+// The list in row order: the selected rows plus the first take_eq rows equal
+// to K*.  Each thread owns a run of bitmap words; an exclusive scan of the
+// per-thread counts gives its output offset and the equal-key rank.
+template <int T>
+__device__ __forceinline__ void tk_emit(const uint32_t *sel, const uint32_t *eqm, int W, uint32_t take_eq, int32_t *out,
+                                        uint32_t *warp_a, uint32_t *warp_b) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (W + T - 1) / T;
+    const int w0 = min(W, tid * per), w1 = min(W, w0 + per);
+    uint32_t cs = 0, ce = 0;
+    for (int w = w0; w < w1; w++) {
+        cs += __popc(sel[w]);
+        ce += __popc(eqm[w]);
+    }
+    uint32_t is = cs, ie = ce;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t vs = __shfl_up_sync(0xffffffffu, is, o), ve = __shfl_up_sync(0xffffffffu, ie, o);
+        if (lane >= o) { is += vs; ie += ve; }
+    }
+    if (lane == 31) { warp_a[warp] = is; warp_b[warp] = ie; }
+    __syncthreads();
+    for (int w = 0; w < warp; w++) { is += warp_a[w]; ie += warp_b[w]; }
+    uint32_t eq_before = ie - ce;
+    uint32_t dst = (is - cs) + min(eq_before, take_eq);
+    for (int w = w0; w < w1; w++) {
+        const uint32_t e_all = eqm[w];
+        uint32_t e = 0;
+        if (eq_before < take_eq) {
+            uint32_t want = take_eq - eq_before;
+            uint32_t rest = e_all;
+            while (rest && want) {                       // the lowest `want` equal rows of the word
+                const uint32_t lb = rest & (0u - rest);
+                e |= lb;
+                rest ^= lb;
+                want--;
+            }
+        }
+        eq_before += __popc(e_all);
+        uint32_t m = sel[w] | e;
+        while (m) {
+            out[dst++] = w * 32 + (__ffs(m) - 1);
+            m &= m - 1u;
+        }
+    }
+}
+
 // Query q: visible rows V = (pos + 1) / 4; fewer than k + 1 rows lists them all
 // and pads with -1.
 __device__ __forceinline__ bool tk_trivial(const IndexerArgs &a, int V, int32_t *out, int T) {
@@ -581,70 +658,16 @@ __global__ void __launch_bounds__(T) topk_kernel(IndexerArgs a, DecodePos dp, in
         }
     }
     __syncthreads();
-    // 3. the low 20 bits among the candidates, 10 at a time
-    for (int i = tid; i < TK_LBINS; i += T) bins[i] = 0;
-    __syncthreads();
-    for (int j = tid; j < nc; j += T) atomicAdd(&bins[(ckey[j] >> 10) & 1023u], 1u);
-    __syncthreads();
-    tk_crossing<T>(bins, TK_LBINS, rank1, warp_a, res);
+    // 3. the low 20 bits among the candidates (all in b*), 10 at a time
+    tk_cand_pass<T>(bins, ckey, nc, 10, 10, true, 0u, rank1, warp_a, res);
     const uint32_t b1 = res[0], rank2 = res[1];
-    for (int i = tid; i < TK_LBINS; i += T) bins[i] = 0;
-    __syncthreads();
-    for (int j = tid; j < nc; j += T) {
-        const uint32_t key = ckey[j];
-        if (((key >> 10) & 1023u) == b1) atomicAdd(&bins[key & 1023u], 1u);
-    }
-    __syncthreads();
-    tk_crossing<T>(bins, TK_LBINS, rank2, warp_a, res);
+    tk_cand_pass<T>(bins, ckey, nc, 10, 0, false, (bstar << 10) | b1, rank2, warp_a, res);
     const uint32_t kstar = (bstar << 20) | (b1 << 10) | res[0];
     const uint32_t take_eq = res[1];                     // rows equal to K* to take, lowest first
     // 4. candidates above K* join the selection, those equal to K* are marked apart
-    for (int j = tid; j < nc; j += T) {
-        const uint32_t key = ckey[j], r = crow[j];
-        if (key > kstar) atomicOr(&sel[r >> 5], 1u << (r & 31u));
-        else if (key == kstar) atomicOr(&eqm[r >> 5], 1u << (r & 31u));
-    }
-    __syncthreads();
-    // 5. in row order: each thread owns a run of bitmap words; an exclusive scan
-    //    of the per-thread counts gives its output offset and the equal-key rank
-    const int per = (W + T - 1) / T;
-    const int w0 = min(W, tid * per), w1 = min(W, w0 + per);
-    uint32_t cs = 0, ce = 0;
-    for (int w = w0; w < w1; w++) {
-        cs += __popc(sel[w]);
-        ce += __popc(eqm[w]);
-    }
-    uint32_t is = cs, ie = ce;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t vs = __shfl_up_sync(0xffffffffu, is, o), ve = __shfl_up_sync(0xffffffffu, ie, o);
-        if (lane >= o) { is += vs; ie += ve; }
-    }
-    if (lane == 31) { warp_a[warp] = is; warp_b[warp] = ie; }
-    __syncthreads();
-    for (int w = 0; w < warp; w++) { is += warp_a[w]; ie += warp_b[w]; }
-    uint32_t eq_before = ie - ce;
-    uint32_t dst = (is - cs) + min(eq_before, take_eq);
-    for (int w = w0; w < w1; w++) {
-        const uint32_t e_all = eqm[w];
-        uint32_t e = 0;
-        if (eq_before < take_eq) {
-            uint32_t want = take_eq - eq_before;
-            uint32_t rest = e_all;
-            while (rest && want) {                       // the lowest `want` equal rows of the word
-                const uint32_t lb = rest & (0u - rest);
-                e |= lb;
-                rest ^= lb;
-                want--;
-            }
-        }
-        eq_before += __popc(e_all);
-        uint32_t m = sel[w] | e;
-        while (m) {
-            out[dst++] = w * 32 + (__ffs(m) - 1);
-            m &= m - 1u;
-        }
-    }
+    tk_mark<T>(ckey, crow, nc, kstar, sel, eqm);
+    // 5. in row order
+    tk_emit<T>(sel, eqm, W, take_eq, out, warp_a, warp_b);
 }
 
 // Radix path alone, for rows whose bitmaps would not fit shared memory.

@@ -262,8 +262,9 @@ def test_checkpoint_restore_resumes_bit_exact(ratio, heads, D):
 
 # ---------------------------------------------------------------------------
 # Top-k on crafted index rows: heavy ties (the radix path), a few distinct
-# scores (ties inside the boundary bin), signed zeros, V around k and across
-# the bitmap word boundaries; scores and lists bit-exact against the oracle
+# scores (ties inside the boundary bin), signed zeros, a few strided stretches
+# of high rows, V around k and across the bitmap word boundaries; scores and
+# lists bit-exact against the oracle
 # ---------------------------------------------------------------------------
 
 _TK_SHAPE = configs.LayerShape(d_model=256, head_dim=128, n_rot=64, idx_head_dim=64, n_heads=8, ratio=4, top_k=512,
@@ -283,6 +284,13 @@ def _crafted_rows(kind, n, d, rng):
         r = np.zeros((n, d), np.float32)
         r[:, 0] = rng.choice(np.array([-0.0, 0.0, 1.0, -1.0, 2.0], np.float32), n)
         return r
+    if kind == "skewed":
+        # high rows in eight short stretches, fewer than k of them in all
+        r = rng.standard_normal((n, d)).astype(np.float32)
+        for st in range(8):
+            r[st * 1024 + 8:st * 1024 + 120] += 4.0
+            r[st * 512 + 4:st * 512 + 28] += 4.0
+        return r
     raise ValueError(kind)
 
 
@@ -291,14 +299,19 @@ def _crafted_queries(kind, n, d, rng):
         return np.zeros((n, d), np.float32)
     if kind == "random":
         return rng.standard_normal((n, d)).astype(np.float32)
+    if kind == "skewed":
+        return rng.integers(0, 3, (n, d)).astype(np.float32)  # non-negative: the raised rows score high
     return rng.integers(-2, 3, (n, d)).astype(np.float32)    # integer scores: ties stay exact
 
 
-@pytest.mark.parametrize("kind", ["random", "all_equal", "few_values", "signed_zero", "zero_query"])
+_TK_KINDS = ["random", "all_equal", "few_values", "signed_zero", "zero_query", "skewed"]
+
+
+@pytest.mark.parametrize("kind", _TK_KINDS)
 def test_topk_crafted_rows_prefill(kind):
     shape = _TK_SHAPE
     d, k = shape.idx_head_dim, shape.top_k
-    rng = np.random.default_rng(["random", "all_equal", "few_values", "signed_zero", "zero_query"].index(kind) + 70)
+    rng = np.random.default_rng(_TK_KINDS.index(kind) + 70)
     dl, _, _ = device_layer(shape, comp_cap=16, idx_cap=_TK_CAP, seed=5, max_rows=64)
     dl.idx_comp[0] = torch.from_numpy(_crafted_rows(kind, _TK_CAP, d, rng)).cuda()
     st = download(dl)
