@@ -26,7 +26,7 @@ EXPORTS = (
     "ds4c_workspace_bytes", "ds4c_state_init", "ds4c_compress_prefill", "ds4c_compress_decode_step",
     "ds4c_indexer_topk", "ds4c_sparse_swa_attn", "ds4c_checkpoint_floats", "ds4c_checkpoint_gather",
     "ds4c_sync_status", "ds4c_status_string", "ds4c_last_cuda_error", "ds4c_attn_uses_tensor_cores",
-    "ds4c_indexer_topk_noalloc", "ds4c_checkpoint_scatter", "ds4c_payload_header",
+    "ds4c_indexer_topk_noalloc", "ds4c_checkpoint_scatter", "ds4c_payload_header", "ds4c_fma_probe",
 )
 PAYLOAD_U32_FIELDS = 13
 NOALLOC_SCORE_FLOATS = 2 * 1024 * 1024
@@ -95,6 +95,7 @@ def lib() -> C.CDLL:
         "ds4c_checkpoint_gather": (st, [cfgp, lsp, U32, U64, P, SZ, C.POINTER(SZ), P]),
         "ds4c_checkpoint_scatter": (st, [cfgp, lsp, U32, U64, P, SZ, P]),
         "ds4c_payload_header": (st, [C.POINTER(PayloadInfo), C.POINTER(C.c_uint32 * PAYLOAD_U32_FIELDS)]),
+        "ds4c_fma_probe": (st, [U32, U32, P, C.POINTER(C.c_double), P]),
         "ds4c_sync_status": (st, [P]),
         "ds4c_status_string": (C.c_char_p, [C.c_int]),
         "ds4c_last_cuda_error": (C.c_char_p, []),
@@ -179,6 +180,13 @@ def ds4c_payload_header(info):
     out = (C.c_uint32 * PAYLOAD_U32_FIELDS)()
     check(lib().ds4c_payload_header(C.byref(info), C.byref(out)), "ds4c_payload_header")
     return list(out)
+
+
+def ds4c_fma_probe(blocks, iters, out_ptr, stream):
+    """Launch the fp32 FMA-rate probe; returns (status, flops of the launch)."""
+    fl = C.c_double(0.0)
+    s = lib().ds4c_fma_probe(blocks, iters, out_ptr, C.byref(fl), stream)
+    return s, fl.value
 
 
 def ds4c_sync_status(stream):

@@ -235,6 +235,14 @@ size_t ds4c_workspace_bytes(const ds4c_layer_cfg *cfg, uint32_t max_tok, uint32_
     return a > b ? a : b;
 }
 
+ds4c_status ds4c_fma_probe(uint32_t blocks, uint32_t iters, float *out, double *flops_h, cudaStream_t stream) {
+    if (!out || !flops_h) return DS4C_ERR_NULL;
+    if (blocks == 0 || iters == 0 || iters > (1u << 24)) return DS4C_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(out) & 3u) != 0) return DS4C_ERR_SHAPE;
+    *flops_h = fma_probe_flops(blocks, iters);
+    return cuda_status(launch_fma_probe(blocks, iters, out, stream));
+}
+
 int ds4c_attn_uses_tensor_cores(const ds4c_layer_cfg *cfg) {
     if (check_cfg(cfg) != DS4C_OK) return 0;
     return tc_attention(*cfg) ? 1 : 0;

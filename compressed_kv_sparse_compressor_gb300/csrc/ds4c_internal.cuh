@@ -31,6 +31,11 @@ inline cudaError_t ensure_dyn_smem(F *func, size_t bytes) {
     return e;
 }
 
+// FP32 FMA-rate probe (the ALU roofline's denominator): flops of one launch
+// of `blocks` 256-thread CTAs running `iters` rounds, and the launch itself.
+double fma_probe_flops(uint32_t blocks, uint32_t iters);
+cudaError_t launch_fma_probe(uint32_t blocks, uint32_t iters, float *out, cudaStream_t s);
+
 // Programmatic dependent launch.  Kernels launched by launch_pdl may be
 // scheduled while the previous kernel of the stream is still finishing, so
 // every such kernel calls pdl_wait() in each CTA before its first access to

@@ -270,6 +270,17 @@ typedef struct {
 } ds4c_payload_info;
 DS4C_API ds4c_status ds4c_payload_header(const ds4c_payload_info *info, uint32_t out[DS4C_PAYLOAD_U32_FIELDS]);
 
+/* Measurement helper, not a step of the path: the fp32 FMA rate of the GPU,
+ * the denominator of the indexer score's roofline (an in-order fp32 fmaf chain
+ * per output on the CUDA cores).  Launches `blocks` CTAs of 256 threads, each
+ * thread running independent fmaf chains for `iters` rounds in registers and
+ * storing one float to out[blocks * 256] (device, caller-owned, 4-byte
+ * aligned); *flops_h (host) receives the launch's flop count.  The caller
+ * times the launch on `stream`.  DS4C_ERR_NULL / DS4C_ERR_SHAPE (blocks or
+ * iters zero, iters above 2^24, misaligned out) before any launch. */
+DS4C_API ds4c_status ds4c_fma_probe(uint32_t blocks, uint32_t iters, float *out, double *flops_h,
+                                    cudaStream_t stream);
+
 /* Synchronises `stream`, then reports (and clears) the device error word:
  * DS4C_ERR_DEVICE if a kernel raised it, DS4C_ERR_CUDA if the stream failed. */
 DS4C_API ds4c_status ds4c_sync_status(cudaStream_t stream);
