@@ -49,9 +49,9 @@ namespace {
 constexpr int ROWS = 128;
 constexpr int SLOT = 8192;            // [64 rows][64 d] bf16
 constexpr int PAIR = 2 * SLOT;
-constexpr int RING = 3;
+constexpr int RING = 4;
 constexpr int THREADS = 192;
-constexpr int MAX_LIST = 1024;
+constexpr int MAX_LIST = 512;
 constexpr float TAU = 8.0f;           // log2 units
 constexpr unsigned long long WAIT_NS = 4000000000ull;
 
@@ -67,15 +67,20 @@ struct L {
     static constexpr int OFF_X = OFF_Q + DC * QCH;
     static constexpr int OFF_PHI = OFF_X + RING * PAIR;
     static constexpr int OFF_PLO = OFF_PHI + PB;
+    // the all-ones A operand of the denominator MMA: one 8 x 8 bf16 core matrix
+    // that the descriptor repeats over every row group and k step (strides 0)
     static constexpr int OFF_ONES = OFF_PLO + PB;
-    static constexpr int OFF_LIST = OFF_ONES + 4096;
-    static constexpr int OFF_RED = OFF_LIST + 4 * MAX_LIST;
-    static constexpr int OFF_MREF = OFF_RED + 4 * 4 * H;
-    static constexpr int OFF_ALPHA = OFF_MREF + 4 * H;
-    static constexpr int OFF_FLAG = OFF_ALPHA + 4 * H;
+    static constexpr int OFF_LIST = OFF_ONES + 128;
+    // per head: the tile maximum as an order-preserving key, then (same word)
+    // the rescale factor of the new reference
+    static constexpr int OFF_TMAX = OFF_LIST + 4 * MAX_LIST;
+    static constexpr int OFF_MREF = OFF_TMAX + 4 * H;
+    static constexpr int OFF_FLAG = OFF_MREF + 4 * H;
     static constexpr int OFF_BAR = OFF_FLAG + 64;
     static constexpr int N_BAR = 2 * RING + 10;
-    static constexpr int SMEM = OFF_BAR + 8 * N_BAR + 16 + 1024;
+    // the dynamic shared memory starts 1024-byte aligned (checked at entry), as
+    // the 128-byte swizzle atoms of Q, the ring and P need
+    static constexpr int SMEM = OFF_BAR + 8 * N_BAR + 16;
     // TMEM columns
     static constexpr int T_S = 0;                      // two S^T buffers of H columns
     static constexpr int T_O = 2 * H;                  // DB blocks of H columns
@@ -242,6 +247,15 @@ __device__ __forceinline__ void tmem_store(uint32_t taddr, const float (&v)[H]) 
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// order-preserving u32 image of a float (for atomicMax) and back
+__device__ __forceinline__ uint32_t max_key(float x) {
+    const uint32_t u = __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_max(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -365,15 +379,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                const __grid_constant__ CUtensorMap qMap, const __grid_constant__ CUtensorMap oMap,
                const TcAttnParams p) {
     using Lay = L<H, D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if ((smem_u32(smem_raw) & 1023u) != 0) {            // the layout has no room to realign
+        if (threadIdx.x == 0) atomicOr(&g_attn_tc_err, 4u);
+        return;
+    }
+    uint8_t *sm = smem_raw;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Lay::OFF_BAR);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + Lay::N_BAR);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *list = reinterpret_cast<int *>(sm + Lay::OFF_LIST);
-    float *red = reinterpret_cast<float *>(sm + Lay::OFF_RED);
+    uint32_t *tmax = reinterpret_cast<uint32_t *>(sm + Lay::OFF_TMAX);
+    float *alpha_s = reinterpret_cast<float *>(sm + Lay::OFF_TMAX);
     float *mref_s = reinterpret_cast<float *>(sm + Lay::OFF_MREF);
-    float *alpha_s = reinterpret_cast<float *>(sm + Lay::OFF_ALPHA);
     volatile int *flags = reinterpret_cast<volatile int *>(sm + Lay::OFF_FLAG);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
@@ -397,7 +415,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     // the all-ones A operand of the denominator MMA (4 KB, layout-free)
-    for (int i = threadIdx.x; i < 4096 / 4; i += THREADS)
+    for (int i = threadIdx.x; i < 128 / 4; i += THREADS)
         reinterpret_cast<uint32_t *>(sm + Lay::OFF_ONES)[i] = 0x3F803F80u;
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -582,7 +600,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             // denominator: L += ones * P (hi and lo)
             const uint32_t d_l = tmem + Lay::T_L;
             for (int kk = 0; kk < ROWS / 16; kk++) {
-                const uint64_t a1 = make_desc(ones, 128, 256, 0);
+                const uint64_t a1 = make_desc(ones, 0, 0, 0);
                 const uint64_t bh = make_desc(phi + kk * 16 * 128, 8192, 1024, 2);
                 const uint64_t bl = make_desc(plo + kk * 16 * 128, 8192, 1024, 2);
                 mma(d_l, a1, bh, ID_L, (first && kk == 0) ? 0u : 1u);
@@ -740,10 +758,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                             m[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
                         }
                     }
-                    *reinterpret_cast<float2 *>(red + q4 * H + 2 * lane) = make_float2(m[0], m[1]);
+                    // the four warps' maxima meet in one key per head (the previous
+                    // tile's factors have been read by now: the vote barrier came after)
+                    if (tid < H) tmax[tid] = 0u;
+                    if (!soft_bar()) { ok = false; break; }
+                    atomicMax(&tmax[2 * lane], max_key(m[0]));
+                    atomicMax(&tmax[2 * lane + 1], max_key(m[1]));
                     if (!soft_bar()) { ok = false; break; }
                     if (tid < H) {
-                        const float mt = fmaxf(fmaxf(red[tid], red[H + tid]), fmaxf(red[2 * H + tid], red[3 * H + tid]));
+                        const float mt = key_max(tmax[tid]);
                         const float mo = mref_s[tid];
                         const float mn = fmaxf(mo, mt);
                         alpha_s[tid] = exp2f(mo - mn);
