@@ -17,7 +17,10 @@
 // query), compressed rows from the comp_split mirror the compressor maintains,
 // gathered by the row list (top-k on ratio-4 layers, every visible row on
 // ratio-128 layers) with 16-byte cp.async by the whole producer warp into the
-// same 128-byte-swizzled layout.  A tile is streamed twice through a 3-deep
+// same 128-byte-swizzled layout, lane pairs taking the two halves of one
+// 32-byte sector so that no sector is fetched twice (16 rows per instruction;
+// 32 rows of one 16-byte chunk each fetched every sector twice, and 4 whole
+// rows per instruction was slower still).  A tile is streamed twice through a 3-deep
 // ring of 16 KB slot pairs: by 64-wide d-chunks for S, by 64-row halves of
 // 128-wide d-blocks for O (the same bytes form the K-major A operand of the
 // first product and the MN-major A operand of the second).  Compressed rows
@@ -477,25 +480,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                     // 1024 chunks of 16 bytes, 32 per lane, in the 128-byte swizzle layout
                     const uint16_t *split = p.comp_split + lo * D;
                     if (!pv) {
+                        // lane pairs take the two halves of one 32-byte sector: an
+                        // instruction covers 16 rows x 32 bytes
 #pragma unroll
-                        for (int m = 0; m < 4; m++) {
-                            const int r = lane + 32 * m;
+                        for (int b = 0; b < 8; b++) {
+                            const int r = 16 * b + (lane >> 1);
                             const uint16_t *src = split + (size_t)row_of(tile, r) * 2 * D + 64 * a;
                             const uint32_t drow = dst + r * 128;
 #pragma unroll
-                            for (int u = 0; u < 8; u++) cp_async16(drow + ((u ^ (r & 7)) << 4), src + 8 * u);
+                            for (int sct = 0; sct < 4; sct++) {
+                                const int u = 2 * sct + (lane & 1);
+                                cp_async16(drow + ((u ^ (r & 7)) << 4), src + 8 * u);
+                            }
                         }
                     } else {
 #pragma unroll
-                        for (int m = 0; m < 2; m++) {
-                            const int rr = lane + 32 * m;
+                        for (int b = 0; b < 4; b++) {
+                            const int rr = 16 * b + (lane >> 1);
                             const uint16_t *src0 = split + (size_t)row_of(tile, 64 * hh + rr) * 2 * D + 128 * a;
 #pragma unroll
-                            for (int half = 0; half < 2; half++) {
-                                const uint32_t drow = dst + half * SLOT + rr * 128;
-#pragma unroll
-                                for (int u = 0; u < 8; u++)
-                                    cp_async16(drow + ((u ^ (rr & 7)) << 4), src0 + 64 * half + 8 * u);
+                            for (int sct = 0; sct < 8; sct++) {
+                                const int half = sct >> 2, u = 2 * (sct & 3) + (lane & 1);
+                                cp_async16(dst + half * SLOT + rr * 128 + ((u ^ (rr & 7)) << 4), src0 + 64 * half + 8 * u);
                             }
                         }
                     }
