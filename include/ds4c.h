@@ -128,9 +128,10 @@ typedef struct {
 } ds4c_layer_state;
 
 /* 1 when ds4c_sparse_swa_attn runs on the tensor cores for this shape
- * (ratio 0/4/128 with n_heads in {16, 32, 64}, head_dim in {128, 256, 512},
- * swa == 128), 0 when it runs on the CUDA cores.  On the tensor-core path the
- * attention lane's comp_split mirror must be allocated. */
+ * (ratio 0/4/128 with n_heads == 64, head_dim in {128, 256, 512}, swa == 128,
+ * and top_k <= 512 on ratio-4 layers), 0 when it runs on the CUDA cores.  On
+ * the tensor-core path the attention lane's comp_split mirror must be
+ * allocated. */
 DS4C_API int ds4c_attn_uses_tensor_cores(const ds4c_layer_cfg *cfg);
 
 /* Bytes of workspace that serves every call on `cfg` with prefill chunks of
