@@ -115,6 +115,12 @@ def test_host_validation_errors(L):
     written = C.c_size_t(0)
     assert abi.ds4c_checkpoint_gather(cfg, st, 0, 40, FAKE, n - 1, C.byref(written), None) == abi.DS4C_ERR_CAPACITY
     assert abi.status_string(abi.DS4C_ERR_CAPACITY).startswith("positions")
+    # the FMA-rate probe validates before launching
+    assert abi.ds4c_fma_probe(8, 16, None, None)[0] == abi.DS4C_ERR_NULL
+    assert abi.ds4c_fma_probe(0, 16, FAKE, None)[0] == abi.DS4C_ERR_SHAPE
+    assert abi.ds4c_fma_probe(8, 0, FAKE, None)[0] == abi.DS4C_ERR_SHAPE
+    assert abi.ds4c_fma_probe(8, (1 << 24) + 1, FAKE, None)[0] == abi.DS4C_ERR_SHAPE
+    assert abi.ds4c_fma_probe(8, 16, FAKE + 2, None)[0] == abi.DS4C_ERR_SHAPE
 
 
 def test_payload_header_matches_the_page_table():
