@@ -584,7 +584,9 @@ __global__ void __launch_bounds__(T) topk_kernel(IndexerArgs a, DecodePos dp, in
     pdl_wait();
     pdl_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int q = blockIdx.x;
+    // prefill takes the queries last first: the score rows written last are the
+    // ones still in L2
+    const int q = (a.n_seq == 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
     const uint64_t pos = (a.n_seq == 1) ? a.pos0 + (uint64_t)q : dp.pos[q];
     const int V = (int)((pos + 1) / 4);
     const int k = a.k;
