@@ -56,6 +56,9 @@ def test_invalid_configs_are_rejected(L):
     assert abi.ds4c_workspace_bytes(_cfg(base), 64) > 0
     big = _cfg(configs.C5.layer, 32768, 32768)
     assert abi.ds4c_attn_uses_tensor_cores(big) == 1 and abi.ds4c_attn_uses_tensor_cores(_cfg(base)) == 0
+    # the tensor-core path holds a row list of at most 512 entries; larger top-k runs on the CUDA cores
+    wide = _cfg(configs.LayerShape(**{**configs.C5.layer.__dict__, "top_k": 1024}), 32768, 32768)
+    assert abi.ds4c_attn_uses_tensor_cores(wide) == 0
     assert abi.ds4c_workspace_bytes(big, 4096, 32) >= abi.ds4c_workspace_bytes(big, 4096)
     for bad in (dict(ratio=3), dict(head_dim=96), dict(n_heads=12), dict(n_rot=6), dict(d_model=100),
                 dict(idx_head_dim=48), dict(swa=0), dict(top_k=0)):
