@@ -141,13 +141,17 @@ def test_ragged_chunks(ratio, heads):
 # Decode: B sequences, one token each at staggered positions
 # ---------------------------------------------------------------------------
 
-def test_decode_small():
-    shape = configs.LayerShape(d_model=512, head_dim=512, n_rot=64, idx_head_dim=128, n_heads=64, ratio=4,
+@pytest.mark.parametrize("ratio,base", [(4, 60), (128, 380), (0, 200)])
+def test_decode_small(ratio, base):
+    shape = configs.LayerShape(d_model=512, head_dim=512, n_rot=64, idx_head_dim=128, n_heads=64, ratio=ratio,
                                top_k=16, dtype="bf16", w_std=0.04)
     seed, B = 31, 8
-    lens = [60 + b for b in range(B)]                    # every stagger class, some emit this step
-    cap = max(lens) // 4 + 2
-    dl, wa, wi = device_layer(shape, comp_cap=cap, idx_cap=cap, n_seq=B, seed=seed, max_rows=128)
+    # every stagger class; ratio 4: some emit this step; ratio 128: 382 + 1 ends a window
+    # (383 = 3*128 - 1), the others sit mid-window over 2 visible rows; ratio 0: a wrapped ring
+    lens = [base + b for b in range(B)]
+    cap = max(lens) // max(ratio, 1) + 2
+    icap = max(lens) // 4 + 2
+    dl, wa, wi = device_layer(shape, comp_cap=cap, idx_cap=icap, n_seq=B, seed=seed, max_rows=128)
     for b in range(B):
         view = dl.seq_view(b)
         saved = dl.state
@@ -166,10 +170,12 @@ def test_decode_small():
     q_idx = torch.cat([x[1] for x in qs]).cuda()
     raw = torch.cat([x[2] for x in qs]).cuda()
     dl.compress_decode(hid, lens)
-    topk = torch.empty(B, shape.top_k, dtype=torch.int32, device="cuda")
-    vmax = (max(lens) + 1) // 4
-    scores = torch.full((B, vmax), float("nan"), device="cuda")
-    dl.indexer_topk(q_idx, lens, B, 1, topk, scores, vmax)
+    topk = scores = None
+    if ratio == 4:
+        topk = torch.empty(B, shape.top_k, dtype=torch.int32, device="cuda")
+        vmax = (max(lens) + 1) // 4
+        scores = torch.full((B, vmax), float("nan"), device="cuda")
+        dl.indexer_topk(q_idx, lens, B, 1, topk, scores, vmax)
     out = torch.empty(B, shape.n_heads, shape.head_dim, device="cuda")
     after_compress = [None] * B
     torch.cuda.synchronize()
@@ -177,20 +183,26 @@ def test_decode_small():
     dl.attention(q, raw, topk, lens, B, 1, out, commit_ring=True)
     dl.sync()
     for b in range(B):
-        check_compress(befores[b], after_compress[b], wa, wi, hid[b:b + 1].cpu(), lens[b])
-        check_indexer_sampled(after_compress[b], q_idx[b:b + 1].cpu().numpy(), [lens[b]],
-                              topk[b:b + 1].cpu().numpy(), scores[b:b + 1].cpu().numpy(), [0])
+        if ratio:
+            check_compress(befores[b], after_compress[b], wa, wi, hid[b:b + 1].cpu(), lens[b])
+        if ratio == 4:
+            check_indexer_sampled(after_compress[b], q_idx[b:b + 1].cpu().numpy(), [lens[b]],
+                                  topk[b:b + 1].cpu().numpy(), scores[b:b + 1].cpu().numpy(), [0])
         check_attention_sampled(after_compress[b], q[b:b + 1].cpu().numpy(), raw[b:b + 1].cpu().numpy(),
-                                topk[b:b + 1].cpu().numpy(), out[b:b + 1].cpu().numpy(), lens[b], [0])
+                                None if topk is None else topk[b:b + 1].cpu().numpy(), out[b:b + 1].cpu().numpy(),
+                                lens[b], [0])
         np.testing.assert_array_equal(dl.raw[b, lens[b] % shape.swa].cpu().numpy(), raw[b].cpu().numpy())
+    if not ratio:
+        return
     # decode(t) equals prefill's t-th step: a fresh one-shot prefill of len+1 tokens
     for b in (0, 3):
-        ref, _, _ = device_layer(shape, comp_cap=cap, idx_cap=cap, seed=seed)
+        ref, _, _ = device_layer(shape, comp_cap=cap, idx_cap=icap, seed=seed)
         ref.compress_prefill(configs.hidden(shape, seed, lens[b] + 1, layer=b).cuda(), 0)
         torch.cuda.synchronize()
         torch.testing.assert_close(dl.attn_comp[b], ref.attn_comp[0], rtol=RTOL, atol=ATOL)
         torch.testing.assert_close(dl.attn_kv[b], ref.attn_kv[0], rtol=RTOL, atol=ATOL)
-        torch.testing.assert_close(dl.idx_comp[b], ref.idx_comp[0], rtol=RTOL, atol=ATOL)
+        if ratio == 4:
+            torch.testing.assert_close(dl.idx_comp[b], ref.idx_comp[0], rtol=RTOL, atol=ATOL)
 
 
 # ---------------------------------------------------------------------------
