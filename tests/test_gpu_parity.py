@@ -119,11 +119,14 @@ def test_c1_chain_against_oracle_end_to_end():
 # Multi-tile shapes with ragged tails (D=512, d=128, 64 heads)
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("ratio,heads", [(0, 64), (4, 64), (128, 64), (4, 32)])
-def test_ragged_chunks(ratio, heads):
-    """heads = 64: tensor-core attention; heads = 32: CUDA-core attention."""
-    shape = configs.LayerShape(d_model=512, head_dim=512, n_rot=64, idx_head_dim=128, n_heads=heads, ratio=ratio,
-                               top_k=16, dtype="bf16", w_std=0.04)
+@pytest.mark.parametrize("ratio,heads,D", [(0, 64, 512), (4, 64, 512), (128, 64, 512), (4, 32, 512),
+                                           (4, 64, 128), (4, 64, 256), (128, 64, 256)])
+def test_ragged_chunks(ratio, heads, D):
+    """heads = 64: tensor-core attention (head_dim 512, 256 or 128: at 128 the one
+    128-wide d-block holds the RoPE dims, so no block is FP8-exact); heads = 32:
+    CUDA-core attention."""
+    shape = configs.LayerShape(d_model=512, head_dim=D, n_rot=64, idx_head_dim=128 if D >= 256 else 64,
+                               n_heads=heads, ratio=ratio, top_k=16, dtype="bf16", w_std=0.04)
     seed = 21
     T_total = 300 if ratio != 128 else 700
     cap = T_total // max(ratio, 1) + 1
