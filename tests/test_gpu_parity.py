@@ -361,3 +361,28 @@ def test_topk_crafted_rows_decode(kind):
     for b in range(B):
         check_indexer_sampled(download(dl, b), q_idx[b:b + 1], [lens[b]], topk[b:b + 1].cpu().numpy(),
                               scores[b:b + 1].cpu().numpy(), [0])
+
+
+@pytest.mark.parametrize("kind", ["random", "few_values"])
+def test_topk_decode_long_rows(kind):
+    """Decode top-k over 28.9K-40960 visible rows, where the keys no longer fit
+    shared memory and each pass reads the score row again (few_values also
+    overflows the candidate list, so the radix path runs on 1024 threads)."""
+    shape = _TK_SHAPE
+    d, k = shape.idx_head_dim, shape.top_k
+    cap = 40960
+    rng = np.random.default_rng(["random", "few_values"].index(kind) + 110)
+    lens = [4 * 28900 - 1, 4 * 30001 + 1, 4 * cap - 1]              # V = 28900, 30001, 40960
+    B = len(lens)
+    dl, _, _ = device_layer(shape, comp_cap=16, idx_cap=cap, n_seq=B, seed=5, max_rows=64)
+    for b in range(B):
+        dl.idx_comp[b] = torch.from_numpy(_crafted_rows(kind, cap, d, rng)).cuda()
+    q_idx = _crafted_queries(kind, B, d, rng)
+    vmax = max((p + 1) // 4 for p in lens)
+    topk = torch.full((B, k), -7, dtype=torch.int32, device="cuda")
+    scores = torch.full((B, vmax), float("nan"), device="cuda")
+    dl.indexer_topk(torch.from_numpy(q_idx).cuda(), lens, B, 1, topk, scores, vmax)
+    dl.sync()
+    for b in range(B):
+        check_indexer_sampled(download(dl, b), q_idx[b:b + 1], [lens[b]], topk[b:b + 1].cpu().numpy(),
+                              scores[b:b + 1].cpu().numpy(), [0])
