@@ -672,35 +672,9 @@ __global__ void __launch_bounds__(T) topk_kernel(IndexerArgs a, DecodePos dp, in
     tk_emit<T>(sel, eqm, W, take_eq, out, warp_a, warp_b);
 }
 
-// Radix path alone, for rows whose bitmaps would not fit shared memory.
-template <int T, bool RESIDENT>
-__global__ void __launch_bounds__(T) topk_radix_kernel(IndexerArgs a, DecodePos dp) {
-    extern __shared__ uint32_t sm_tk[];
-    uint32_t *cnt = sm_tk;
-    uint32_t *cand = cnt + TK_BINS * T;
-    uint32_t *keys = cand + TK_RCAND;                    // RESIDENT only
-    pdl_wait();
-    pdl_launch_dependents();
-    const int q = blockIdx.x;
-    const uint64_t pos = (a.n_seq == 1) ? a.pos0 + (uint64_t)q : dp.pos[q];
-    const int V = (int)((pos + 1) / 4);
-    int32_t *out = a.topk + (size_t)q * a.k;
-    if (tk_trivial(a, V, out, T)) return;
-    const float *s = a.scores + (size_t)q * a.lds;
-    if (RESIDENT) {
-        for (int i = threadIdx.x; i < V; i += T) keys[i] = order_key(__ldcs(s + i));
-        __syncthreads();
-    }
-    auto key_at = [&](int i) -> uint32_t { return RESIDENT ? keys[i] : order_key(__ldg(s + i)); };
-    tk_radix<T>(V, a.k, out, key_at, cnt, cand);
-}
-template <int T>
-size_t tk_radix_smem(uint64_t vmax, bool resident) {
-    return sizeof(uint32_t) * ((size_t)TK_BINS * T + TK_RCAND + (resident ? vmax : 0));
-}
-
-// Launch the top-k over n_q queries: the main path with its keys resident
-// when allowed and they fit, else in global memory, else the radix path.
+// Launch the top-k over n_q queries: the keys resident in shared memory when
+// allowed and they fit, else read from the score rows each pass.  (At the
+// largest index capacity the non-resident form needs 92 KB with 1024 threads.)
 template <int T>
 cudaError_t launch_topk(const IndexerArgs &a, const DecodePos &dp, int n_q, uint64_t vmax, bool allow_resident,
                         cudaStream_t s) {
@@ -716,11 +690,8 @@ cudaError_t launch_topk(const IndexerArgs &a, const DecodePos &dp, int n_q, uint
         const size_t smem = tk_smem<T>(vmax, false);
         if ((e = ensure_dyn_smem(topk_kernel<T, false>, smem)) != cudaSuccess) return e;
         return launch_pdl(topk_kernel<T, false>, dim3(n_q), dim3(T), smem, s, a, dp, wcap);
-    } else {
-        const size_t smem = tk_radix_smem<T>(vmax, false);
-        if ((e = ensure_dyn_smem(topk_radix_kernel<T, false>, smem)) != cudaSuccess) return e;
-        return launch_pdl(topk_radix_kernel<T, false>, dim3(n_q), dim3(T), smem, s, a, dp);
     }
+    return cudaErrorNotSupported;
 }
 
 }  // namespace
