@@ -386,6 +386,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
     using Lay = L<H, D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if ((smem_u32(smem_raw) & 1023u) != 0) {            // the layout has no room to realign
+        pdl_wait();                                      // keep the launch chain ordered
         if (threadIdx.x == 0) atomicOr(&g_attn_tc_err, 4u);
         return;
     }
