@@ -32,7 +32,7 @@ from compressed_kv_sparse_compressor_gb300 import configs  # noqa: E402
 METRIC = "prefill tokens/s per layer"
 # dram__bytes_read.sum + dram__bytes_write.sum of one attention launch (4096 queries), from the ncu capture
 # in profiles/kernels_prefill_8192tok_chunk2_full.md; set to None when the kernel changes until re-captured
-ATTN_TRAFFIC = 557589248 + 482480896   # dram__bytes_read.sum + dram__bytes_write.sum, one launch
+ATTN_TRAFFIC = 556861952 + 482737664   # dram__bytes_read.sum + dram__bytes_write.sum, one launch
 ATTN_TRAFFIC_SRC = "ncu, one 4096-query launch of the 8192-token case (same units per launch as C5)"
 UNIT = "tokens/s"
 
