@@ -13,6 +13,10 @@ namespace {
 bool pow2_width(uint32_t w) { return w == 64 || w == 128 || w == 256 || w == 512; }
 bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
+}  // namespace
+
+namespace ds4c {
+
 ds4c_status check_cfg(const ds4c_layer_cfg *c) {
     if (!c) return DS4C_ERR_NULL;
     if (c->ratio != 0 && c->ratio != 4 && c->ratio != 128) return DS4C_ERR_SHAPE;
@@ -34,6 +38,18 @@ ds4c_status check_cfg(const ds4c_layer_cfg *c) {
     }
     return DS4C_OK;
 }
+
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+ds4c_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return DS4C_OK;
+    t_last_cuda_error = e;
+    return DS4C_ERR_CUDA;
+}
+
+}  // namespace ds4c
+
+namespace {
 
 // Projection width of one lane (kv and score each): coff * Dl.
 int proj_width(const ds4c_layer_cfg &c, bool attn) { return coff_of(c) * lane_width(c, attn); }
@@ -103,14 +119,6 @@ RopeTable rope_table(const ds4c_layer_cfg &c) {
     for (uint32_t i = 0; i < c.n_rot / 2; i++)
         t.inv_freq[i] = (float)pow((double)c.rope_base, -2.0 * (double)i / (double)c.n_rot);
     return t;
-}
-
-thread_local cudaError_t t_last_cuda_error = cudaSuccess;
-
-ds4c_status cuda_status(cudaError_t e) {
-    if (e == cudaSuccess) return DS4C_OK;
-    t_last_cuda_error = e;
-    return DS4C_ERR_CUDA;
 }
 
 ds4c_status check_lane_state(const ds4c_lane_state &s) {

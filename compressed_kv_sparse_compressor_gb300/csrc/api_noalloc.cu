@@ -30,7 +30,10 @@ float *g_scores_dev[kMaxDevices] = {};
 std::mutex g_scores_mu;
 
 // Device address of the array on the current device.  The first call on each
-// device looks it up with that device current; later calls reuse it.
+// device looks it up with that device current; later calls reuse it.  The
+// cached address belongs to the CUDA context of that first call: after a
+// cudaDeviceReset of that device the module is loaded anew and the address
+// is stale, so this entry point must not be used across a device reset.
 cudaError_t scores_on_current_device(float **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -54,10 +57,10 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 extern "C" ds4c_status ds4c_indexer_topk_noalloc(const ds4c_layer_cfg *cfg, const ds4c_layer_state *st,
                                                  const float *q_idx, const uint64_t *pos_h, uint32_t n_seq,
                                                  uint32_t n_tok, int32_t *topk, cudaStream_t stream) {
-    if (!cfg) return DS4C_ERR_NULL;
-    const ds4c_layer_cfg &c = *cfg;
     // the same shape rules as ds4c_indexer_topk
-    if (ds4c_workspace_bytes(cfg, 1, 0) == 0) return DS4C_ERR_SHAPE;
+    ds4c_status s = check_cfg(cfg);
+    if (s != DS4C_OK) return s;
+    const ds4c_layer_cfg &c = *cfg;
     if (c.ratio != 4) return DS4C_ERR_SHAPE;
     if (n_seq == 0 || n_tok == 0) return DS4C_ERR_SHAPE;
     if (n_seq > 1 && n_tok > 1) return DS4C_ERR_UNSUPPORTED;
@@ -81,7 +84,8 @@ extern "C" ds4c_status ds4c_indexer_topk_noalloc(const ds4c_layer_cfg *cfg, cons
     const uint64_t rows = (uint64_t)n_seq * n_tok;
     if (rows * (lds > 0 ? lds : 4) > (uint64_t)DS4C_NOALLOC_SCORE_FLOATS) return DS4C_ERR_CAPACITY;
     float *scores = nullptr;
-    if (scores_on_current_device(&scores) != cudaSuccess) return DS4C_ERR_CUDA;
+    cudaError_t e = scores_on_current_device(&scores);
+    if (e != cudaSuccess) return cuda_status(e);
     IndexerArgs a{};
     a.q = q_idx;
     a.rows = st->idx.comp;
@@ -94,6 +98,6 @@ extern "C" ds4c_status ds4c_indexer_topk_noalloc(const ds4c_layer_cfg *cfg, cons
     a.n_seq = (int)n_seq;
     a.n_tok = (int)n_tok;
     a.pos0 = pos_h[0];
-    cudaError_t e = (n_seq == 1) ? launch_indexer_prefill(a, stream) : launch_indexer_decode(a, dp, stream);
-    return e == cudaSuccess ? DS4C_OK : DS4C_ERR_CUDA;
+    e = (n_seq == 1) ? launch_indexer_prefill(a, stream) : launch_indexer_decode(a, dp, stream);
+    return cuda_status(e);
 }

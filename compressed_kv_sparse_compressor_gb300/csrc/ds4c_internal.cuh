@@ -14,6 +14,11 @@ constexpr int kMaxRot = 128;
 constexpr int kMaxDecodeSeq = 1024;
 constexpr uint32_t kMaxIdxCap = 40960;
 
+// Host validation of a layer configuration (DS4C_OK or the status every call returns for it).
+ds4c_status check_cfg(const ds4c_layer_cfg *c);
+// DS4C_OK for cudaSuccess; otherwise records e for ds4c_last_cuda_error and returns DS4C_ERR_CUDA.
+ds4c_status cuda_status(cudaError_t e);
+
 inline int lane_width(const ds4c_layer_cfg &c, bool attn) { return attn ? (int)c.head_dim : (int)c.idx_head_dim; }
 inline int coff_of(const ds4c_layer_cfg &c) { return c.ratio == 4 ? 2 : 1; }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

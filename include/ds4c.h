@@ -214,8 +214,9 @@ DS4C_API ds4c_status ds4c_sparse_swa_attn(const ds4c_layer_cfg *cfg, const ds4c_
  *     4096-token prefill chunk at 131072 context does not).
  *   - The array exists on every GPU that loads the library, until the process
  *     exits.  The first call on a device looks up the array's device address
- *     (with that device current); make that first call before any stream
- *     capture.
+ *     (with that device current) and keeps it; make that first call before any
+ *     stream capture.  The kept address does not survive cudaDeviceReset: do
+ *     not call this entry point on a device after resetting it.
  *   - Every call shares the array: calls whose kernels overlap on the GPU (on
  *     streams without ordering between them) race on it.  A call reads only
  *     scores it wrote itself, so no part of the array needs clearing.

@@ -139,3 +139,12 @@ def test_payload_header_matches_the_page_table():
     for i, name in enumerate(g["fields"][2:], start=2):
         assert hdr[i] == getattr(info, name), name
     assert names == g["fields"][2:]
+
+
+def test_noalloc_capacity_constant_matches_the_header():
+    """The binding's copy of DS4C_NOALLOC_SCORE_FLOATS is the header's value."""
+    import re
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "ds4c.h")).read()
+    m = re.search(r"#define\s+DS4C_NOALLOC_SCORE_FLOATS\s+\((\d+)u\s*\*\s*(\d+)u\s*\*\s*(\d+)u\)", hdr)
+    assert m, "DS4C_NOALLOC_SCORE_FLOATS not found in include/ds4c.h"
+    assert int(m.group(1)) * int(m.group(2)) * int(m.group(3)) == abi.NOALLOC_SCORE_FLOATS

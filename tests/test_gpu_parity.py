@@ -386,3 +386,60 @@ def test_topk_decode_long_rows(kind):
     for b in range(B):
         check_indexer_sampled(download(dl, b), q_idx[b:b + 1], [lens[b]], topk[b:b + 1].cpu().numpy(),
                               scores[b:b + 1].cpu().numpy(), [0])
+
+
+def _chain_layer(n_seq, d):
+    """Rows and queries built from vectors on which the in-order fused chain differs
+    from the reversed chain, the unfused chain and a dot rounded once; each vector is
+    zero-padded after its last dimension (which leaves every chain's value as it is)."""
+    from fp_exact import distinguishing_pairs
+    pairs = [p for w in (4, 6, 8) for p in distinguishing_pairs(6, w, seed=300 + w)]
+    rows = np.zeros((len(pairs), d), np.float32)
+    qs = np.zeros((len(pairs), d), np.float32)
+    for i, (q, r, _) in enumerate(pairs):
+        rows[i, :len(r)] = r
+        qs[i, :len(q)] = q
+    return pairs, rows, qs
+
+
+def test_index_score_chain_vectors_prefill_and_decode():
+    """The GPU scores are the in-order binary32 fmaf chain, computed here in exact
+    arithmetic, on vectors where the other plausible evaluation orders differ."""
+    from fp_exact import fma_chain
+    shape = _TK_SHAPE
+    d = shape.idx_head_dim
+    pairs, rows, qs = _chain_layer(1, d)
+    n = len(pairs)
+    cap = 64
+    rng = np.random.default_rng(400)
+    full = np.concatenate([rows, rng.standard_normal((cap - n, d)).astype(np.float32)])
+    want = np.array([[fma_chain(qs[j], full[c]) for c in range(cap)] for j in range(n)], np.float32)
+    for j in range(n):
+        assert want[j, j] == pairs[j][2]
+    # prefill form: n queries of one sequence, all at positions that see every row
+    dl, _, _ = device_layer(shape, comp_cap=16, idx_cap=cap, seed=5, max_rows=64)
+    dl.idx_comp[0] = torch.from_numpy(full).cuda()
+    pos0 = 4 * cap - 1
+    topk = torch.full((n, shape.top_k), -7, dtype=torch.int32, device="cuda")
+    scores = torch.full((n, cap), float("nan"), device="cuda")
+    dl.indexer_topk(torch.from_numpy(qs).cuda(), [pos0], 1, n, topk, scores, cap)
+    dl.sync()
+    np.testing.assert_array_equal(scores.cpu().numpy(), want)
+    st = download(dl)
+    check_indexer_sampled(st, qs, [pos0 + j for j in range(n)], topk.cpu().numpy(), scores.cpu().numpy(), range(n))
+    # decode form: one query per sequence (TMA-staged score), every sequence holding the same rows
+    B = n
+    dd, _, _ = device_layer(shape, comp_cap=16, idx_cap=cap, n_seq=B, seed=5, max_rows=64)
+    for b in range(B):
+        dd.idx_comp[b] = torch.from_numpy(full).cuda()
+    lens = [4 * cap - 1 - (b % 3) for b in range(B)]
+    topk = torch.full((B, shape.top_k), -7, dtype=torch.int32, device="cuda")
+    scores = torch.full((B, cap), float("nan"), device="cuda")
+    dd.indexer_topk(torch.from_numpy(qs).cuda(), lens, B, 1, topk, scores, cap)
+    dd.sync()
+    sc = scores.cpu().numpy()
+    for b in range(B):
+        V = (lens[b] + 1) // 4
+        np.testing.assert_array_equal(sc[b, :V], want[b, :V], err_msg=f"decode scores sequence {b}")
+        check_indexer_sampled(download(dd, b), qs[b:b + 1], [lens[b]], topk[b:b + 1].cpu().numpy(), sc[b:b + 1],
+                              [0])

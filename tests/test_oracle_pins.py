@@ -338,6 +338,46 @@ def test_index_score_error_bound(orc):
             assert np.float32(s) == s
 
 
+def test_round_f32_rule():
+    """The exact-rounding helper itself: ties to even, subnormal quantum, exact values kept."""
+    from fractions import Fraction as Fr
+
+    from fp_exact import round_f32
+    u = Fr(1, 1 << 24)                                   # half an ulp of 1.0
+    assert round_f32(1 + u) == np.float32(1.0)            # tie -> even significand
+    assert round_f32(1 + 3 * u) == np.float32(1.0) + np.float32(2.0 ** -22)
+    assert round_f32(1 + u + Fr(1, 1 << 60)) == np.float32(1.0) + np.float32(2.0 ** -23)
+    assert round_f32(-(1 + 3 * u)) == -(np.float32(1.0) + np.float32(2.0 ** -22))
+    assert round_f32(Fr(1, 1 << 150)) == 0.0             # half the smallest subnormal -> 0 (even)
+    assert round_f32(Fr(3, 1 << 150)) == np.float32(2.0 ** -148)
+    rng = np.random.default_rng(12)
+    for x in rng.standard_normal(500).astype(np.float32):
+        assert round_f32(Fr(float(x))) == x
+    for x in rng.standard_normal(500):                     # doubles: numpy's cast rounds to nearest even too
+        assert round_f32(Fr(float(x))) == np.float32(x)
+
+
+def test_index_score_is_the_in_order_fused_chain(orc):
+    """The indexer score is s = fmaf(q[i], row[i], s) for i = 0..d-1 in binary32
+    (the reading that makes the top-k bit-exact).  On crafted vectors the in-order
+    fused chain, the reversed chain, the unfused chain, the exact dot rounded once
+    and a double accumulation give different binary32 results; the oracle must give
+    the first, computed here in exact rational arithmetic."""
+    from fp_exact import distinguishing_pairs
+    for d in (4, 6, 8):
+        for q, r, want in distinguishing_pairs(6, d, seed=300 + d):
+            got = np.float32(orc.index_score(q, r))
+            assert got == want, (d, q.tolist(), r.tolist(), float(got), float(want))
+            # zero padding after the last dimension leaves the chain's value unchanged
+            qp = np.concatenate([q, np.zeros(128 - d, np.float32)])
+            rp = np.concatenate([r, rng_pad(128 - d)])
+            assert np.float32(orc.index_score(qp, rp)) == want
+
+
+def rng_pad(n):
+    return np.random.default_rng(n).standard_normal(n).astype(np.float32)
+
+
 def test_topk_brute_force(orc):
     rng = np.random.default_rng(6)
     for trial in range(300):
