@@ -27,6 +27,7 @@ EXPORTS = (
     "ds4c_indexer_topk", "ds4c_sparse_swa_attn", "ds4c_checkpoint_floats", "ds4c_checkpoint_gather",
     "ds4c_sync_status", "ds4c_status_string", "ds4c_last_cuda_error", "ds4c_attn_uses_tensor_cores",
     "ds4c_indexer_topk_noalloc", "ds4c_checkpoint_scatter", "ds4c_payload_header", "ds4c_fma_probe",
+    "ds4c_payload_bytes", "ds4c_payload_write", "ds4c_payload_read",
 )
 PAYLOAD_U32_FIELDS = 13
 NOALLOC_SCORE_FLOATS = 2 * 1024 * 1024
@@ -95,6 +96,10 @@ def lib() -> C.CDLL:
         "ds4c_checkpoint_gather": (st, [cfgp, lsp, U32, U64, P, SZ, C.POINTER(SZ), P]),
         "ds4c_checkpoint_scatter": (st, [cfgp, lsp, U32, U64, P, SZ, P]),
         "ds4c_payload_header": (st, [C.POINTER(PayloadInfo), C.POINTER(C.c_uint32 * PAYLOAD_U32_FIELDS)]),
+        "ds4c_payload_bytes": (SZ, [cfgp, U32, U64, U32]),
+        "ds4c_payload_write": (st, [C.POINTER(PayloadInfo), cfgp, lsp, U32, U32, P, P, P, SZ, C.POINTER(SZ), P]),
+        "ds4c_payload_read": (st, [C.POINTER(PayloadInfo), cfgp, lsp, U32, U32, P, SZ, P, SZ, P,
+                                   C.POINTER(U32), P]),
         "ds4c_fma_probe": (st, [U32, U32, P, C.POINTER(C.c_double), P]),
         "ds4c_sync_status": (st, [P]),
         "ds4c_status_string": (C.c_char_p, [C.c_int]),
@@ -180,6 +185,39 @@ def ds4c_payload_header(info):
     out = (C.c_uint32 * PAYLOAD_U32_FIELDS)()
     check(lib().ds4c_payload_header(C.byref(info), C.byref(out)), "ds4c_payload_header")
     return list(out)
+
+
+def _stack(cfgs, states=None):
+    ca = (LayerCfg * len(cfgs))(*cfgs)
+    sa = None if states is None else (LayerState * len(states))(*states)
+    return ca, sa
+
+
+def ds4c_payload_bytes(cfgs, pos, vocab_size):
+    ca, _ = _stack(cfgs)
+    return lib().ds4c_payload_bytes(ca, len(cfgs), pos, vocab_size)
+
+
+def ds4c_payload_write(info, cfgs, states, seq, tokens_h, logits_h, dst, dst_bytes, stream):
+    """tokens_h / logits_h: host numpy arrays (uint32 / float32).  Returns (status, bytes written)."""
+    ca, sa = _stack(cfgs, states)
+    w = C.c_size_t(0)
+    tp = tokens_h.ctypes.data_as(C.c_void_p) if tokens_h is not None and tokens_h.size else None
+    lp = logits_h.ctypes.data_as(C.c_void_p) if logits_h is not None and logits_h.size else None
+    s = lib().ds4c_payload_write(C.byref(info), ca, sa, len(cfgs), seq, tp, lp, dst, dst_bytes, C.byref(w), stream)
+    return s, w.value
+
+
+def ds4c_payload_read(expect, cfgs, states, seq, src, src_bytes, tokens_h, logits_h, stream):
+    """tokens_h / logits_h: writable host numpy arrays.  Returns (status, token count)."""
+    ca, sa = _stack(cfgs, states)
+    n = C.c_uint32(0)
+    tp = tokens_h.ctypes.data_as(C.c_void_p) if tokens_h is not None and tokens_h.size else None
+    lp = logits_h.ctypes.data_as(C.c_void_p) if logits_h is not None and logits_h.size else None
+    cap = 0 if tokens_h is None else tokens_h.size
+    s = lib().ds4c_payload_read(C.byref(expect), ca, sa, len(cfgs), seq, src, src_bytes, tp, cap, lp, C.byref(n),
+                                stream)
+    return s, n.value
 
 
 def ds4c_fma_probe(blocks, iters, out_ptr, stream):

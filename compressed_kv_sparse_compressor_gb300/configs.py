@@ -101,6 +101,17 @@ C5 = Workload(
 
 ALL = {w.name: w for w in (C1, C2, C3, C4, C5)}
 
+# The Pro variant's layer table ("Metal グラフと圧縮 KV の実装を読む" §1: layers 0-1 at
+# ratio 128 instead of uncompressed, then even layers ratio 4, odd layers ratio 128) on
+# the same layer shapes as the Flash stack, 8192 tokens per layer in two chunks.
+PRO = Workload(
+    name="pro8_T8192_bf16",
+    layer=LayerShape(d_model=4096, head_dim=512, n_rot=64, idx_head_dim=128, n_heads=64,
+                     ratio=4),
+    ratios=(128, 128, 4, 128, 4, 128, 4, 128),
+    n_tok=8192, chunk=4096, seed=6,
+    note="Pro-style 8-layer stack, 8192-token prefill in 4096-token chunks")
+
 
 def comp_caps(shape: LayerShape, max_tokens: int):
     """Rows the compressed arrays must hold after ``max_tokens`` tokens."""

@@ -272,6 +272,49 @@ typedef struct {
 } ds4c_payload_info;
 DS4C_API ds4c_status ds4c_payload_header(const ds4c_payload_info *info, uint32_t out[DS4C_PAYLOAD_U32_FIELDS]);
 
+/* Bytes of the DSV4 payload ([P1] §5) of a stack of n_layers layers (cfgs[l],
+ * layer order) after pos tokens with a vocabulary of vocab_size logits:
+ * 4 * (13 + pos + vocab_size + 2 * n_layers) + 4 * sum over layers of
+ * ds4c_checkpoint_floats(cfgs[l], pos).  0 for an invalid cfg or n_layers == 0. */
+DS4C_API size_t ds4c_payload_bytes(const ds4c_layer_cfg *cfgs, uint32_t n_layers, uint64_t pos, uint32_t vocab_size);
+
+/* Writes sequence `seq` of a layer stack as one DSV4 payload into the device
+ * buffer dst ([P1] §5 body order; §6 raw rows in logical position order; §7 the
+ * frontier tensors): the header of `info` (info->token_count is the checkpoint
+ * position pos, info->layer_count == n_layers, info->live_raw_rows ==
+ * min(pos, raw_window)), the pos token ids tokens_h (host), the vocab_size logits
+ * logits_h (host; both come from outside this path), the attention row counts
+ * pos / ratio (0 on ratio-0 layers) and the indexer row counts pos / 4 (ratio-4
+ * layers, else 0) as u32 per layer, then for each layer in order the body
+ * ds4c_checkpoint_gather writes.  cfgs[l] / states[l] describe layer l: every
+ * layer's swa must equal raw_window and raw_cap, its head_dim the header's, a
+ * ratio-4 layer's idx_head_dim the header's, and its comp_cap must not exceed
+ * the header's comp_cap (else DS4C_ERR_SHAPE).  dst must be 16-byte aligned
+ * and hold ds4c_payload_bytes bytes (else DS4C_ERR_CAPACITY); *written_h (host,
+ * optional) receives that count.  The host fields are staged before the call
+ * returns; the copies and kernels run on `stream`. */
+DS4C_API ds4c_status ds4c_payload_write(const ds4c_payload_info *info, const ds4c_layer_cfg *cfgs,
+                                        const ds4c_layer_state *states, uint32_t n_layers, uint32_t seq,
+                                        const uint32_t *tokens_h, const float *logits_h, void *dst, size_t dst_bytes,
+                                        size_t *written_h, cudaStream_t stream);
+
+/* Restores sequence `seq` of a layer stack from a DSV4 payload in the device
+ * buffer src, the inverse of ds4c_payload_write.  The payload's header must
+ * match `expect` in every field but the token count and the live raw rows
+ * (a payload written for another runtime shape is refused with
+ * DS4C_ERR_SHAPE, as is a live-row count or a per-layer row count that
+ * disagrees with the token count); then each layer's body is scattered into
+ * states[l] (ds4c_checkpoint_scatter), the token ids are copied to tokens_h
+ * (host, room for tokens_cap ids, else DS4C_ERR_CAPACITY), the logits to
+ * logits_h (host, expect->vocab_size floats) and the token count to
+ * *token_count_h.  The header and the host fields are read synchronously
+ * (the call synchronises `stream` twice); nothing is written before every
+ * check has passed. */
+DS4C_API ds4c_status ds4c_payload_read(const ds4c_payload_info *expect, const ds4c_layer_cfg *cfgs,
+                                       const ds4c_layer_state *states, uint32_t n_layers, uint32_t seq,
+                                       const void *src, size_t src_bytes, uint32_t *tokens_h, size_t tokens_cap,
+                                       float *logits_h, uint32_t *token_count_h, cudaStream_t stream);
+
 /* Measurement helper, not a step of the path: the fp32 FMA rate of the GPU,
  * the denominator of the indexer score's roofline (an in-order fp32 fmaf chain
  * per output on the CUDA cores).  Launches `blocks` CTAs of 256 threads, each

@@ -80,6 +80,8 @@ def lib():
             "orc_checkpoint_floats": (C.c_int64, [P, U64]),
             "orc_checkpoint_gather": (C.c_int64, [P, P, LaneS, LaneS, U64, P]),
             "orc_checkpoint_scatter": (C.c_int64, [P, P, LaneS, LaneS, U64, P]),
+            "orc_payload_write": (C.c_int64, [P, I, P, P, P, P, P, P, P]),
+            "orc_payload_read": (C.c_int64, [P, I, P, P, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -344,3 +346,50 @@ def checkpoint_gather(st: State, pos: int) -> np.ndarray:
     w = lib().orc_checkpoint_gather(C.byref(cfg), _p(st.raw), st.attn.s(), st.idx.s(), pos, _p(dst))
     assert w == n
     return dst[:n]
+
+
+PAYLOAD_FIELDS = ("ctx_size", "prefill_chunk", "raw_cap", "raw_window", "comp_cap", "token_count", "layer_count",
+                  "head_dim", "idx_head_dim", "vocab_size", "live_raw_rows")
+
+
+def _stack_args(states):
+    n = len(states)
+    cfgs = (Cfg * n)(*[s.L.c() for s in states])
+    rings = (C.c_void_p * n)(*[s.raw.ctypes.data for s in states])
+    attn = (LaneS * n)(*[s.attn.s() for s in states])
+    idx = (LaneS * n)(*[s.idx.s() for s in states])
+    return cfgs, rings, attn, idx
+
+
+def payload_size(states, fields) -> int:
+    pos = fields[5]
+    return 4 * (13 + fields[5] + fields[9] + 2 * len(states)) + 4 * sum(checkpoint_floats(s.L, pos) for s in states)
+
+
+def payload_write(fields, states, tokens, logits) -> np.ndarray:
+    """DSV4 payload bytes of the layer stack ``states`` (one State per layer, same sequence)."""
+    f = np.ascontiguousarray(fields, dtype=np.uint32)
+    assert f.size == 11
+    tok = np.ascontiguousarray(tokens, dtype=np.uint32)
+    lg = _f32(logits)
+    assert tok.size == f[5] and lg.size == f[9]
+    out = np.zeros(payload_size(states, [int(x) for x in f]), dtype=np.uint8)
+    cfgs, rings, attn, idx = _stack_args(states)
+    n = lib().orc_payload_write(_p(f), len(states), cfgs, rings, attn, idx, _p(tok) if tok.size else None,
+                                _p(lg) if lg.size else None, _p(out))
+    assert n == out.size
+    return out
+
+
+def payload_read(buf, states, max_tokens: int, vocab: int):
+    """Restore ``states`` from payload bytes; returns (fields, tokens, logits)."""
+    buf = np.ascontiguousarray(buf, dtype=np.uint8)
+    n_tok = int(buf[28:32].view(np.uint32)[0])
+    assert n_tok <= max_tokens and int(buf[44:48].view(np.uint32)[0]) == vocab, "payload larger than the buffers"
+    f = np.zeros(11, dtype=np.uint32)
+    tok = np.zeros(max(max_tokens, 1), dtype=np.uint32)
+    lg = np.zeros(max(vocab, 1), dtype=np.float32)
+    cfgs, rings, attn, idx = _stack_args(states)
+    n = lib().orc_payload_read(_p(buf), len(states), cfgs, rings, attn, idx, _p(f), _p(tok), _p(lg))
+    assert n >= 0, "payload magic or version mismatch"
+    return f, tok[:f[5]], lg[:f[9]]

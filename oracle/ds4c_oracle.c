@@ -521,3 +521,97 @@ int64_t orc_checkpoint_scatter(const orc_cfg *cfg, float *ring, orc_lane_s as, o
     }
     return o;
 }
+
+/* ---------------------------------------------------------------------------
+ * DSV4 session payload of a layer stack ("【#4】ds4.c を読み解く" §5).
+ * Header: 13 u32 fields in the page's table order -- magic "DSV4" (the bytes
+ * 'D','S','V','4' read as a little-endian u32), payload version 2, then the 11
+ * fields of `fields` (saved context size, prefill chunk size, raw KV ring
+ * capacity, raw sliding-window length, compressed KV capacity, checkpoint
+ * token count, layer count, raw/head KV dimension, indexer head dimension,
+ * vocabulary size, live raw rows).  Body, in the page's order: u32 token ids
+ * [token_count], f32 logits [vocab_size], u32 compressed attention row counts
+ * [layer_count], u32 ratio-4 indexer row counts [layer_count], then per layer
+ * the raw SWA rows (logical order, §6), the attention compressed rows, the
+ * compressor frontier (§7), the indexer compressed rows and the indexer
+ * frontier (ratio-4 layers) -- READING: the page's list is written once per
+ * layer, layer by layer, which is the single-layer checkpoint body above.
+ * The checkpoint position is the token count.  Returns the bytes written.
+ * ------------------------------------------------------------------------- */
+static void put_u32(uint8_t *dst, int64_t *o, uint32_t v) {
+    dst[*o + 0] = (uint8_t)(v & 0xFFu);
+    dst[*o + 1] = (uint8_t)((v >> 8) & 0xFFu);
+    dst[*o + 2] = (uint8_t)((v >> 16) & 0xFFu);
+    dst[*o + 3] = (uint8_t)((v >> 24) & 0xFFu);
+    *o += 4;
+}
+
+static uint32_t get_u32(const uint8_t *src, int64_t *o) {
+    uint32_t v = (uint32_t)src[*o] | ((uint32_t)src[*o + 1] << 8) | ((uint32_t)src[*o + 2] << 16) |
+                 ((uint32_t)src[*o + 3] << 24);
+    *o += 4;
+    return v;
+}
+
+static void put_f32(uint8_t *dst, int64_t *o, float f) {
+    uint32_t v;
+    memcpy(&v, &f, sizeof v);
+    put_u32(dst, o, v);
+}
+
+static float get_f32(const uint8_t *src, int64_t *o) {
+    uint32_t v = get_u32(src, o);
+    float f;
+    memcpy(&f, &v, sizeof f);
+    return f;
+}
+
+int64_t orc_payload_write(const uint32_t *fields, int n_layers, const orc_cfg *cfgs, float *const *rings,
+                          const orc_lane_s *attn, const orc_lane_s *idx, const uint32_t *tokens,
+                          const float *logits, uint8_t *dst) {
+    const uint32_t magic = (uint32_t)'D' | ((uint32_t)'S' << 8) | ((uint32_t)'V' << 16) | ((uint32_t)'4' << 24);
+    const uint32_t token_count = fields[5], vocab = fields[9];
+    const uint64_t pos = token_count;
+    int64_t o = 0;
+    put_u32(dst, &o, magic);
+    put_u32(dst, &o, 2u);
+    for (int i = 0; i < 11; i++) put_u32(dst, &o, fields[i]);
+    for (uint32_t i = 0; i < token_count; i++) put_u32(dst, &o, tokens[i]);
+    for (uint32_t i = 0; i < vocab; i++) put_f32(dst, &o, logits[i]);
+    for (int l = 0; l < n_layers; l++) put_u32(dst, &o, cfgs[l].ratio ? (uint32_t)(pos / (uint64_t)cfgs[l].ratio) : 0u);
+    for (int l = 0; l < n_layers; l++) put_u32(dst, &o, cfgs[l].ratio == 4 ? (uint32_t)(pos / 4) : 0u);
+    for (int l = 0; l < n_layers; l++) {
+        int64_t n = orc_checkpoint_floats(&cfgs[l], pos);
+        float *body = (float *)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1));
+        orc_checkpoint_gather(&cfgs[l], rings[l], attn[l], idx[l], pos, body);
+        for (int64_t i = 0; i < n; i++) put_f32(dst, &o, body[i]);
+        free(body);
+    }
+    return o;
+}
+
+/* The inverse: the 11 fields after magic and version into fields_out, the
+ * token ids and logits out, each layer's body scattered into its state.
+ * Returns the bytes read, or -1 when the magic or the version differ. */
+int64_t orc_payload_read(const uint8_t *src, int n_layers, const orc_cfg *cfgs, float *const *rings,
+                         const orc_lane_s *attn, const orc_lane_s *idx, uint32_t *fields_out,
+                         uint32_t *tokens_out, float *logits_out) {
+    const uint32_t magic = (uint32_t)'D' | ((uint32_t)'S' << 8) | ((uint32_t)'V' << 16) | ((uint32_t)'4' << 24);
+    int64_t o = 0;
+    if (get_u32(src, &o) != magic) return -1;
+    if (get_u32(src, &o) != 2u) return -1;
+    for (int i = 0; i < 11; i++) fields_out[i] = get_u32(src, &o);
+    const uint32_t token_count = fields_out[5], vocab = fields_out[9];
+    const uint64_t pos = token_count;
+    for (uint32_t i = 0; i < token_count; i++) tokens_out[i] = get_u32(src, &o);
+    for (uint32_t i = 0; i < vocab; i++) logits_out[i] = get_f32(src, &o);
+    o += 8 * (int64_t)n_layers;                     /* the two count arrays follow from pos */
+    for (int l = 0; l < n_layers; l++) {
+        int64_t n = orc_checkpoint_floats(&cfgs[l], pos);
+        float *body = (float *)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1));
+        for (int64_t i = 0; i < n; i++) body[i] = get_f32(src, &o);
+        orc_checkpoint_scatter(&cfgs[l], rings[l], attn[l], idx[l], pos, body);
+        free(body);
+    }
+    return o;
+}

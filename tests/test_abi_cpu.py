@@ -6,6 +6,7 @@ import ctypes as C
 import os
 import re
 
+import numpy as np
 import pytest
 
 from compressed_kv_sparse_compressor_gb300 import abi, configs
@@ -148,3 +149,50 @@ def test_noalloc_capacity_constant_matches_the_header():
     m = re.search(r"#define\s+DS4C_NOALLOC_SCORE_FLOATS\s+\((\d+)u\s*\*\s*(\d+)u\s*\*\s*(\d+)u\)", hdr)
     assert m, "DS4C_NOALLOC_SCORE_FLOATS not found in include/ds4c.h"
     assert int(m.group(1)) * int(m.group(2)) * int(m.group(3)) == abi.NOALLOC_SCORE_FLOATS
+
+
+def test_payload_bytes_and_host_validation(L, orc):
+    """ds4c_payload_bytes matches the oracle's payload size; ds4c_payload_write / read
+    reject bad arguments on the host before touching the device."""
+    shapes = [configs.LayerShape(d_model=64, head_dim=128, n_rot=64, idx_head_dim=64, n_heads=8, ratio=r, top_k=8,
+                                 dtype="f32") for r in (0, 4, 128, 4)]
+    pos, vocab = 1000, 11
+    cfgs = []
+    for s in shapes:
+        cfgs.append(abi.LayerCfg(d_model=s.d_model, head_dim=s.head_dim, n_rot=s.n_rot, idx_head_dim=s.idx_head_dim,
+                                 n_heads=s.n_heads, ratio=s.ratio, swa=s.swa, top_k=s.top_k, comp_cap=300,
+                                 idx_cap=300, dtype=abi.DS4C_F32, rms_eps=s.rms_eps, attn_scale=s.attn_scale,
+                                 rope_base=s.rope_base))
+    states = [orc.State(orc_layer(s, comp_cap=300, idx_cap=300)) for s in shapes]
+    fields = [4096, 4096, 128, 128, 300, pos, 4, 128, 64, vocab, 128]
+    assert abi.ds4c_payload_bytes(cfgs, pos, vocab) == orc.payload_size(states, fields)
+    assert abi.ds4c_payload_bytes(cfgs[:0] + [abi.LayerCfg()], pos, vocab) == 0
+    info = abi.PayloadInfo(*fields)
+    st = [abi.LayerState() for _ in cfgs]
+    FAKE = 1 << 20
+    tok = np.zeros(pos, np.uint32)
+    lg = np.zeros(vocab, np.float32)
+    need = abi.ds4c_payload_bytes(cfgs, pos, vocab)
+    assert abi.ds4c_payload_write(info, cfgs, st, 0, tok, lg, None, need, None)[0] == abi.DS4C_ERR_NULL
+    assert abi.ds4c_payload_write(info, cfgs, st, 0, None, lg, FAKE, need, None)[0] == abi.DS4C_ERR_NULL
+    bad = abi.PayloadInfo(*fields)
+    bad.layer_count = 3
+    assert abi.ds4c_payload_write(bad, cfgs, st, 0, tok, lg, FAKE, need, None)[0] == abi.DS4C_ERR_SHAPE
+    bad = abi.PayloadInfo(*fields)
+    bad.head_dim = 256
+    assert abi.ds4c_payload_write(bad, cfgs, st, 0, tok, lg, FAKE, need, None)[0] == abi.DS4C_ERR_SHAPE
+    bad = abi.PayloadInfo(*fields)
+    bad.live_raw_rows = 127
+    assert abi.ds4c_payload_write(bad, cfgs, st, 0, tok, lg, FAKE, need, None)[0] == abi.DS4C_ERR_SHAPE
+    bad = abi.PayloadInfo(*fields)
+    bad.comp_cap = 299                               # a layer holds more rows than the header's capacity
+    assert abi.ds4c_payload_write(bad, cfgs, st, 0, tok, lg, FAKE, need, None)[0] == abi.DS4C_ERR_SHAPE
+    assert abi.ds4c_payload_write(info, cfgs, st, 0, tok, lg, FAKE + 4, need, None)[0] == abi.DS4C_ERR_SHAPE
+    assert abi.ds4c_payload_write(info, cfgs, st, 0, tok, lg, FAKE, need - 1, None)[0] == abi.DS4C_ERR_CAPACITY
+    big = abi.PayloadInfo(*fields)
+    big.token_count, big.live_raw_rows = 1300, 128   # 1300 / 4 = 325 rows > idx_cap 300
+    assert abi.ds4c_payload_write(big, cfgs, st, 0, np.zeros(1300, np.uint32), lg, FAKE, 1 << 30,
+                                  None)[0] == abi.DS4C_ERR_CAPACITY
+    assert abi.ds4c_payload_read(info, cfgs, st, 0, None, need, tok, lg, None)[0] == abi.DS4C_ERR_NULL
+    assert abi.ds4c_payload_read(info, cfgs, st, 0, FAKE + 4, need, tok, lg, None)[0] == abi.DS4C_ERR_SHAPE
+    assert abi.ds4c_payload_read(info, cfgs, st, 0, FAKE, 10, tok, lg, None)[0] == abi.DS4C_ERR_CAPACITY

@@ -545,3 +545,94 @@ def test_checkpoint_restore_resumes_exactly(orc, ratio):
     np.testing.assert_array_equal(orc.checkpoint_gather(fresh, T1), body)
     run(fresh, T1, T2)
     np.testing.assert_array_equal(orc.checkpoint_gather(fresh, T1 + T2), orc.checkpoint_gather(full, T1 + T2))
+
+
+# --------------------------------------------------------------------------
+# DSV4 payload of a layer stack ("【#4】ds4.c を読み解く" §5 body order)
+# --------------------------------------------------------------------------
+
+def _payload_stack(orc, ratios, pos, S=16, D=64, d=16):
+    states = []
+    for li, r in enumerate(ratios):
+        shape = configs.LayerShape(d_model=32, head_dim=D, n_rot=16, idx_head_dim=d, n_heads=8, ratio=r, swa=S,
+                                   top_k=4, dtype="f32")
+        L = orc_layer(shape, comp_cap=max(pos // max(r, 1), 1) + 3, idx_cap=pos // 4 + 3)
+        st = orc.State(L)
+        base = 10000.0 * (li + 1)
+        # every element tells where it lives: layer, tensor, row, column
+        st.raw[:] = base + 100.0 * np.arange(S)[:, None] + np.arange(D)[None, :] / 1000.0
+        for k, lane in enumerate((st.attn, st.idx)):
+            for j, arr in enumerate((lane.comp, lane.state_kv, lane.state_score)):
+                arr[:] = base + 1000.0 * (1 + 3 * k + j) + np.arange(arr.size).reshape(arr.shape) / 64.0
+        states.append(st)
+    return states
+
+
+def test_payload_layout_follows_the_page(orc):
+    """Bytes of the oracle's DSV4 payload against the page's header table and body
+    order, parsed here field by field (little-endian u32 / f32)."""
+    g = _golden("payload_header.json")
+    ratios, pos, S = (0, 4, 128, 4), 301, 16
+    states = _payload_stack(orc, ratios, pos, S=S)
+    D, d = 64, 16
+    vocab = 7
+    fields = dict(ctx_size=1024, prefill_chunk=4096, raw_cap=S, raw_window=S, comp_cap=200, token_count=pos,
+                  layer_count=len(ratios), head_dim=D, idx_head_dim=d, vocab_size=vocab, live_raw_rows=min(pos, S))
+    assert tuple(fields) == tuple(g["fields"][2:]) == orc.PAYLOAD_FIELDS
+    tokens = (np.arange(pos, dtype=np.uint32) * 7919 + 3) % 128000
+    logits = np.linspace(-3, 3, vocab).astype(np.float32)
+    buf = orc.payload_write([fields[k] for k in orc.PAYLOAD_FIELDS], states, tokens, logits)
+    u32 = buf.view("<u4")
+    f32 = buf.view("<f4")
+    assert buf[:4].tobytes() == g["magic_ascii"].encode() and u32[0] == g["magic_u32"]
+    assert u32[1] == g["version"]
+    for i, name in enumerate(g["fields"][2:], start=2):
+        assert u32[i] == fields[name], name
+    o = 13
+    np.testing.assert_array_equal(u32[o:o + pos], tokens); o += pos                      # token ids
+    np.testing.assert_array_equal(f32[o:o + vocab], logits); o += vocab                  # logits
+    np.testing.assert_array_equal(u32[o:o + len(ratios)], [pos // r if r else 0 for r in ratios]); o += len(ratios)
+    np.testing.assert_array_equal(u32[o:o + len(ratios)], [pos // 4 if r == 4 else 0 for r in ratios])
+    o += len(ratios)
+    for st, r in zip(states, ratios):
+        n_live = min(pos, S)
+        want = [st.raw[p % S] for p in range(pos - n_live, pos)]                        # raw rows, logical order
+        if r:
+            want += [st.attn.comp[:pos // r].ravel(), st.attn.state_kv.ravel(), st.attn.state_score.ravel()]
+        if r == 4:
+            want += [st.idx.comp[:pos // 4].ravel(), st.idx.state_kv.ravel(), st.idx.state_score.ravel()]
+        w = np.concatenate([np.ravel(x) for x in want]).astype(np.float32)
+        np.testing.assert_array_equal(f32[o:o + w.size], w)
+        o += w.size
+    assert 4 * o == buf.size
+
+
+def test_payload_round_trip_restores_every_layer(orc):
+    ratios, pos = (128, 4, 0, 4), 517
+    states = _payload_stack(orc, ratios, pos)
+    fields = [2048, 4096, 16, 16, 300, pos, len(ratios), 64, 16, 5, 16]
+    tokens = np.arange(pos, dtype=np.uint32)
+    logits = np.arange(5, dtype=np.float32) - 2.5
+    buf = orc.payload_write(fields, states, tokens, logits)
+    fresh = [orc.State(s.L) for s in states]
+    f, tk, lg = orc.payload_read(buf, fresh, pos, 5)
+    assert f.tolist() == fields
+    np.testing.assert_array_equal(tk, tokens)
+    np.testing.assert_array_equal(lg, logits)
+    for a, b in zip(states, fresh):
+        n_live = min(pos, a.L.swa)
+        for p in range(pos - n_live, pos):
+            np.testing.assert_array_equal(b.raw[p % a.L.swa], a.raw[p % a.L.swa])
+        if a.L.ratio:
+            np.testing.assert_array_equal(b.attn.comp[:pos // a.L.ratio], a.attn.comp[:pos // a.L.ratio])
+            np.testing.assert_array_equal(b.attn.state_kv, a.attn.state_kv)
+            np.testing.assert_array_equal(b.attn.state_score, a.attn.state_score)
+        if a.L.ratio == 4:
+            np.testing.assert_array_equal(b.idx.comp[:pos // 4], a.idx.comp[:pos // 4])
+            np.testing.assert_array_equal(b.idx.state_kv, a.idx.state_kv)
+            np.testing.assert_array_equal(b.idx.state_score, a.idx.state_score)
+    # a corrupted magic is refused
+    bad = buf.copy()
+    bad[0] ^= 1
+    with pytest.raises(AssertionError):
+        orc.payload_read(bad, [orc.State(s.L) for s in states], pos, 5)
