@@ -27,7 +27,7 @@ EXPORTS = (
     "ds4c_indexer_topk", "ds4c_sparse_swa_attn", "ds4c_checkpoint_floats", "ds4c_checkpoint_gather",
     "ds4c_sync_status", "ds4c_status_string", "ds4c_last_cuda_error", "ds4c_attn_uses_tensor_cores",
     "ds4c_indexer_topk_noalloc", "ds4c_checkpoint_scatter", "ds4c_payload_header", "ds4c_fma_probe",
-    "ds4c_payload_bytes", "ds4c_payload_write", "ds4c_payload_read",
+    "ds4c_payload_bytes", "ds4c_payload_write", "ds4c_payload_read", "ds4c_compress_prefill_timed",
 )
 PAYLOAD_U32_FIELDS = 13
 NOALLOC_SCORE_FLOATS = 2 * 1024 * 1024
@@ -88,6 +88,7 @@ def lib() -> C.CDLL:
         "ds4c_attn_uses_tensor_cores": (C.c_int, [cfgp]),
         "ds4c_state_init": (st, [cfgp, lsp, U32, P]),
         "ds4c_compress_prefill": (st, [cfgp, lwp, lwp, lsp, P, U32, U64, P, SZ, P]),
+        "ds4c_compress_prefill_timed": (st, [cfgp, lwp, lwp, lsp, P, U32, U64, P, SZ, P, P]),
         "ds4c_compress_decode_step": (st, [cfgp, lwp, lwp, lsp, P, C.POINTER(U64), U32, P, SZ, P]),
         "ds4c_indexer_topk": (st, [cfgp, lsp, P, C.POINTER(U64), U32, U32, P, P, SZ, P, SZ, P]),
         "ds4c_sparse_swa_attn": (st, [cfgp, lsp, P, P, P, C.POINTER(U64), U32, U32, P, C.c_int, P, SZ, P]),
@@ -146,6 +147,12 @@ def ds4c_compress_prefill(cfg, attn_w, idx_w, state, hidden, n_tok, pos0, ws, ws
     return lib().ds4c_compress_prefill(C.byref(cfg), C.byref(attn_w) if attn_w is not None else None,
                                        C.byref(idx_w) if idx_w is not None else None, C.byref(state),
                                        hidden, n_tok, pos0, ws, ws_bytes, stream)
+
+
+def ds4c_compress_prefill_timed(cfg, attn_w, idx_w, state, hidden, n_tok, pos0, ws, ws_bytes, event, stream):
+    return lib().ds4c_compress_prefill_timed(C.byref(cfg), C.byref(attn_w) if attn_w is not None else None,
+                                             C.byref(idx_w) if idx_w is not None else None, C.byref(state),
+                                             hidden, n_tok, pos0, ws, ws_bytes, event, stream)
 
 
 def ds4c_compress_decode_step(cfg, attn_w, idx_w, state, hidden, pos_h, n_seq, ws, ws_bytes, stream):

@@ -138,7 +138,7 @@ ds4c_status check_lane_weights(const ds4c_lane_weights *w) {
 // workspace, then the fused compressor.
 ds4c_status run_compress(const ds4c_layer_cfg *cfg, const ds4c_lane_weights *aw, const ds4c_lane_weights *iw,
                          const ds4c_layer_state *st, const void *hidden, uint32_t rows, uint64_t pos0,
-                         const DecodePos *dp, void *ws, cudaStream_t stream) {
+                         const DecodePos *dp, void *ws, cudaStream_t stream, cudaEvent_t after_projection = nullptr) {
     const ds4c_layer_cfg &c = *cfg;
     const WsLayout L = (dp == nullptr) ? ws_prefill(c, rows) : ws_decode(c, rows);
     float *proj = reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + L.proj_off);
@@ -166,6 +166,7 @@ ds4c_status run_compress(const ds4c_layer_cfg *cfg, const ds4c_lane_weights *aw,
     if (c.dtype == DS4C_BF16) e = launch_gemm_tc(g, stream);
     if (e == cudaErrorNotSupported) e = launch_gemm_simt(g, stream);
     if (e != cudaSuccess) return cuda_status(e);
+    if (after_projection && (e = cudaEventRecord(after_projection, stream)) != cudaSuccess) return cuda_status(e);
 
     CompressArgs a{};
     a.n_lanes = (c.ratio == 4) ? 2 : 1;
@@ -276,10 +277,10 @@ ds4c_status ds4c_state_init(const ds4c_layer_cfg *cfg, const ds4c_layer_state *s
     return cuda_status(e);
 }
 
-ds4c_status ds4c_compress_prefill(const ds4c_layer_cfg *cfg, const ds4c_lane_weights *attn,
-                                  const ds4c_lane_weights *idx, const ds4c_layer_state *st,
-                                  const void *hidden, uint32_t n_tok, uint64_t pos0,
-                                  void *ws, size_t ws_bytes, cudaStream_t stream) {
+static ds4c_status compress_prefill_impl(const ds4c_layer_cfg *cfg, const ds4c_lane_weights *attn,
+                                         const ds4c_lane_weights *idx, const ds4c_layer_state *st,
+                                         const void *hidden, uint32_t n_tok, uint64_t pos0, void *ws,
+                                         size_t ws_bytes, cudaStream_t stream, cudaEvent_t after_projection) {
     ds4c_status s = check_cfg(cfg);
     if (s != DS4C_OK) return s;
     const ds4c_layer_cfg &c = *cfg;
@@ -300,7 +301,22 @@ ds4c_status ds4c_compress_prefill(const ds4c_layer_cfg *cfg, const ds4c_lane_wei
     if (tc_attention(c) && !st->attn.comp_split) return DS4C_ERR_NULL;
     if (!ws) return DS4C_ERR_WORKSPACE;
     if (ws_bytes < ws_prefill(c, n_tok).total) return DS4C_ERR_WORKSPACE;
-    return run_compress(cfg, attn, idx, st, hidden, n_tok, pos0, nullptr, ws, stream);
+    return run_compress(cfg, attn, idx, st, hidden, n_tok, pos0, nullptr, ws, stream, after_projection);
+}
+
+ds4c_status ds4c_compress_prefill(const ds4c_layer_cfg *cfg, const ds4c_lane_weights *attn,
+                                  const ds4c_lane_weights *idx, const ds4c_layer_state *st,
+                                  const void *hidden, uint32_t n_tok, uint64_t pos0,
+                                  void *ws, size_t ws_bytes, cudaStream_t stream) {
+    return compress_prefill_impl(cfg, attn, idx, st, hidden, n_tok, pos0, ws, ws_bytes, stream, nullptr);
+}
+
+ds4c_status ds4c_compress_prefill_timed(const ds4c_layer_cfg *cfg, const ds4c_lane_weights *attn,
+                                        const ds4c_lane_weights *idx, const ds4c_layer_state *st,
+                                        const void *hidden, uint32_t n_tok, uint64_t pos0, void *ws,
+                                        size_t ws_bytes, cudaEvent_t after_projection, cudaStream_t stream) {
+    if (!after_projection) return DS4C_ERR_NULL;
+    return compress_prefill_impl(cfg, attn, idx, st, hidden, n_tok, pos0, ws, ws_bytes, stream, after_projection);
 }
 
 ds4c_status ds4c_compress_decode_step(const ds4c_layer_cfg *cfg, const ds4c_lane_weights *attn,

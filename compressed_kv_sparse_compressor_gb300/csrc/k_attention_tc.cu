@@ -4,13 +4,16 @@
 // K = V = the stored row, all heads sharing it.
 //
 // Formulation (one query token at a time, all H heads together):
-//   S^T[r][h] = sum_d X[r][d] Q[h][d]        M = 128 rows, N = H, K = D
-//   O^T[d][h] += sum_r X[r][d] P[r][h]       M = 128 d (D/128 blocks), N = H, K = rows
-//   L[.][h]   += sum_r 1 * P[r][h]           (the softmax denominator, one MMA)
+//   S^T[r][h | H+h] = sum_d X[r][d] [Q_hi | Q_lo][h][d]   M = 128 rows, N = 2H, K = D
+//   O^T[d][h] += sum_r X[r][d] P[r][h]                   M = 128 d (D/128 blocks), N = H, K = rows
+//   L[h] += sum_r P[r][h]                                (the softmax denominator, on the CUDA cores)
 // Rows sit on TMEM lanes, heads on TMEM columns.  Accuracy: every operand is
-// split into bf16 hi + lo (x = hi + lo to 2^-17) and each product takes three
-// MMAs (hi*hi + hi*lo + lo*hi), fp32 accumulation in tensor memory; this keeps
-// the result within fp32-accumulation tolerance of the exact attention.
+// split into bf16 hi + lo (x = hi + lo to 2^-17) and each product takes the
+// three parts hi*hi + hi*lo + lo*hi, fp32 accumulation in tensor memory; this
+// keeps the result within fp32-accumulation tolerance of the exact attention.
+// The S product multiplies X by Q_hi and Q_lo in one N = 2H MMA (the two halves
+// land side by side in TMEM and the softmax adds them), so the X operand is
+// read from shared memory once for both.
 //
 // Data: row tiles arrive from bf16 hi/lo mirrors: raw rows by TMA from a
 // position-ordered mirror the call builds in the workspace (one 128-row box per
@@ -65,17 +68,15 @@ struct L {
     static constexpr int DC = D / 64;
     static constexpr int DB = D / 128;
     // Q: chunk c (64 d) at OFF_Q + c * QCH holds the fp32 box [H][64] as the
-    // TMA lands it, then in place its bf16 split: hi [H][64] at +0, lo at +QCH/2
+    // TMA lands it, then in place its bf16 split: hi [H][64] at +0, lo at +QCH/2,
+    // which together form one K-major [2H][64] operand (the S product's N = 2H)
     static constexpr int QCH = H * 64 * 4;
     static constexpr int PB = ROWS * H * 2;            // bytes of P hi (or lo)
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_X = OFF_Q + DC * QCH;
     static constexpr int OFF_PHI = OFF_X + RING * PAIR;
     static constexpr int OFF_PLO = OFF_PHI + PB;
-    // the all-ones A operand of the denominator MMA: one 8 x 8 bf16 core matrix
-    // that the descriptor repeats over every row group and k step (strides 0)
-    static constexpr int OFF_ONES = OFF_PLO + PB;
-    static constexpr int OFF_LIST = OFF_ONES + 128;
+    static constexpr int OFF_LIST = OFF_PLO + PB;
     // per head: the tile maximum as an order-preserving key, then (same word)
     // the rescale factor of the new reference
     static constexpr int OFF_TMAX = OFF_LIST + 4 * MAX_LIST;
@@ -87,13 +88,13 @@ struct L {
     // the 128-byte swizzle atoms of Q, the ring and P need
     static constexpr int SMEM = OFF_BAR + 8 * N_BAR + 16;
     // TMEM columns
-    static constexpr int T_S = 0;                      // two S^T buffers of H columns
-    static constexpr int T_O = 2 * H;                  // DB blocks of H columns
-    static constexpr int T_L = 2 * H + DB * H;         // H columns
+    static constexpr int T_S = 0;                      // two S^T buffers of 2H columns (Q_hi part | Q_lo part)
+    static constexpr int T_O = 4 * H;                  // DB blocks of H columns
     static constexpr int T_COLS = 512;
-    static_assert(T_L + H <= T_COLS, "tensor memory");
+    static_assert(T_O + DB * H <= T_COLS, "tensor memory");
     static_assert(SMEM <= 232448, "shared memory");
     static_assert(PB == 64 * H * 4, "an output staging box [H][64] fp32 fills P hi (or lo)");
+    static_assert(PB >= 4 * H * 4, "the four warps' denominator partials fit P hi");
 };
 
 // barrier indices
@@ -250,6 +251,54 @@ __device__ __forceinline__ void tmem_store(uint32_t taddr, const float (&v)[H]) 
 #pragma unroll
     for (int c = 0; c < H; c += 16) TMEM_ST16(taddr + c, r, c);
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// S of this thread's row: the Q_hi and the Q_lo halves of the N = 2H product
+// added, 16 columns at a time (keeps the register footprint at H + 32).
+template <int H>
+__device__ __forceinline__ void tmem_load_s(uint32_t taddr, float (&v)[H]) {
+#pragma unroll
+    for (int c = 0; c < H; c += 16) {
+        uint32_t a[16], b[16];
+        TMEM_LD16(taddr + c, a, 0);
+        TMEM_LD16(taddr + H + c, b, 0);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int j = 0; j < 16; j++) v[c + j] = __uint_as_float(a[j]) + __uint_as_float(b[j]);
+    }
+}
+
+// Warp reduction over the 32 rows of a warp of 64 per-head values, by a
+// transposing butterfly: at offset o each lane keeps the half of its heads
+// selected by lane bit o and takes the partner's values for it, so that after
+// the five steps lane l holds heads 2l (r0) and 2l + 1 (r1).  v is only read.
+template <bool MAX>
+__device__ __forceinline__ void warp_heads_reduce(const float (&v)[64], float &r0, float &r1) {
+    const int lane = threadIdx.x & 31;
+    float m[32];
+    {
+        const bool up = (lane & 16) != 0;
+#pragma unroll
+        for (int k = 0; k < 32; k++) {
+            const float send = up ? v[k] : v[k + 32];
+            const float keep = up ? v[k + 32] : v[k];
+            const float o = __shfl_xor_sync(0xffffffffu, send, 16);
+            m[k] = MAX ? fmaxf(keep, o) : keep + o;
+        }
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int k = 0; k < 2 * o; k++) {
+            const float send = up ? m[k] : m[k + 2 * o];
+            const float keep = up ? m[k + 2 * o] : m[k];
+            const float x = __shfl_xor_sync(0xffffffffu, send, o);
+            m[k] = MAX ? fmaxf(keep, x) : keep + x;
+        }
+    }
+    r0 = m[0];
+    r1 = m[1];
 }
 
 // order-preserving u32 image of a float (for atomicMax) and back
@@ -420,9 +469,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // the all-ones A operand of the denominator MMA (4 KB, layout-free)
-    for (int i = threadIdx.x; i < 128 / 4; i += THREADS)
-        reinterpret_cast<uint32_t *>(sm + Lay::OFF_ONES)[i] = 0x3F803F80u;
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(Lay::T_COLS)
@@ -455,6 +501,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                 if (i >= nc) return dummy;
                 return p.ratio == 4 ? list[i] : dummy + i;
             };
+            // this lane's eight tile rows 16 b + lane / 2 (b = 0 .. 7): every unit of a
+            // compressed tile copies from them, so their mirror addresses are formed once per tile
+            const uint16_t *rp[8];
+            int rp_tile = -1;
+            auto tile_rows = [&](int tile) {
+                if (tile == rp_tile) return;
+                rp_tile = tile;
+#pragma unroll
+                for (int b = 0; b < 8; b++) rp[b] = p.comp_split + (size_t)row_of(tile, 16 * b + (lane >> 1)) * 2 * D;
+            };
             // one 16 KB unit into the next ring pair; every lane takes part
             auto issue = [&](int tile, bool pv, int a, int hh, int lo) -> bool {
                 const int s_ = unit % RING;
@@ -481,30 +537,33 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                     }
                 } else {
                     // 1024 chunks of 16 bytes, 32 per lane, in the 128-byte swizzle layout
-                    const uint16_t *split = p.comp_split + lo * D;
+                    tile_rows(tile);
+                    const int sw = (lane >> 1) & 7;              // row & 7 of every row this lane copies
                     if (!pv) {
                         // lane pairs take the two halves of one 32-byte sector: an
                         // instruction covers 16 rows x 32 bytes
+                        const int off = lo * D + 64 * a;
 #pragma unroll
                         for (int b = 0; b < 8; b++) {
                             const int r = 16 * b + (lane >> 1);
-                            const uint16_t *src = split + (size_t)row_of(tile, r) * 2 * D + 64 * a;
+                            const uint16_t *src = rp[b] + off;
                             const uint32_t drow = dst + r * 128;
 #pragma unroll
                             for (int sct = 0; sct < 4; sct++) {
                                 const int u = 2 * sct + (lane & 1);
-                                cp_async16(drow + ((u ^ (r & 7)) << 4), src + 8 * u);
+                                cp_async16(drow + ((u ^ sw) << 4), src + 8 * u);
                             }
                         }
                     } else {
+                        const int off = lo * D + 128 * a;
 #pragma unroll
                         for (int b = 0; b < 4; b++) {
                             const int rr = 16 * b + (lane >> 1);
-                            const uint16_t *src0 = split + (size_t)row_of(tile, 64 * hh + rr) * 2 * D + 128 * a;
+                            const uint16_t *src0 = (hh ? rp[4 + b] : rp[b]) + off;
 #pragma unroll
                             for (int sct = 0; sct < 8; sct++) {
                                 const int half = sct >> 2, u = 2 * (sct & 3) + (lane & 1);
-                                cp_async16(dst + half * SLOT + rr * 128 + ((u ^ (rr & 7)) << 4), src0 + 64 * half + 8 * u);
+                                cp_async16(dst + half * SLOT + rr * 128 + ((u ^ sw) << 4), src0 + 64 * half + 8 * u);
                             }
                         }
                     }
@@ -537,11 +596,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         constexpr uint32_t ID_QK = idesc(128, H, 0, 0);
+        constexpr uint32_t ID_QK2 = idesc(128, 2 * H, 0, 0);
         constexpr uint32_t ID_PV = idesc(128, H, 1, 1);
-        constexpr uint32_t ID_L = idesc(128, H, 0, 1);
         const uint32_t qs = smem_u32(sm + Lay::OFF_Q);
         const uint32_t phi = smem_u32(sm + Lay::OFF_PHI), plo = smem_u32(sm + Lay::OFF_PLO);
-        const uint32_t ones = smem_u32(sm + Lay::OFF_ONES);
         // fp32 Q of query n into the Q chunks (lane 0; the Q buffer is free)
         auto issue_q = [&](int n) {
             mbar_expect_tx(bar(B_QLOAD), Lay::DC * Lay::QCH);
@@ -559,7 +617,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             const int sb = gt & 1;
             if (gt >= 2 && !mbar_wait(bar(B_SFREE0 + sb), ((gt >> 1) - 1) & 1, abort)) return false;
             fence_after();
-            const uint32_t d_t = tmem + Lay::T_S + sb * H;
+            const uint32_t d_t = tmem + Lay::T_S + sb * 2 * H;
             for (int c = 0; c < Lay::DC; c++) {
                 const bool has_lo = tile == 0 || c >= p.nope_chunks;
                 uint32_t xh, xl = 0;
@@ -569,11 +627,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                 fence_after();
                 for (int kk = 0; kk < 4; kk++) {
                     const uint64_t ah = make_desc(xh + kk * 32, 16, 1024, 2);
-                    const uint64_t bh = make_desc(qs + c * Lay::QCH + kk * 32, 16, 1024, 2);
-                    const uint64_t bl = make_desc(qs + c * Lay::QCH + Lay::QCH / 2 + kk * 32, 16, 1024, 2);
-                    mma(d_t, ah, bh, ID_QK, (c > 0 || kk > 0) ? 1u : 0u);
-                    mma(d_t, ah, bl, ID_QK, 1u);
-                    if (has_lo) mma(d_t, make_desc(xl + kk * 32, 16, 1024, 2), bh, ID_QK, 1u);
+                    // [Q_hi; Q_lo] rows 0 .. 2H-1: the lo half follows the hi half at the same pitch
+                    const uint64_t b2 = make_desc(qs + c * Lay::QCH + kk * 32, 16, 1024, 2);
+                    mma(d_t, ah, b2, ID_QK2, (c > 0 || kk > 0) ? 1u : 0u);
+                    if (has_lo) mma(d_t, make_desc(xl + kk * 32, 16, 1024, 2), b2, ID_QK, 1u);
                 }
                 free_unit(unit++);
                 if (has_lo) free_unit(unit++);
@@ -605,15 +662,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                     free_unit(unit++);
                     if (has_lo) free_unit(unit++);
                 }
-            }
-            // denominator: L += ones * P (hi and lo)
-            const uint32_t d_l = tmem + Lay::T_L;
-            for (int kk = 0; kk < ROWS / 16; kk++) {
-                const uint64_t a1 = make_desc(ones, 0, 0, 0);
-                const uint64_t bh = make_desc(phi + kk * 16 * 128, 8192, 1024, 2);
-                const uint64_t bl = make_desc(plo + kk * 16 * 128, 8192, 1024, 2);
-                mma(d_l, a1, bh, ID_L, (first && kk == 0) ? 0u : 1u);
-                mma(d_l, a1, bl, ID_L, 1u);
             }
             mma_commit(bar(B_PVDONE));
             return true;
@@ -718,13 +766,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                 continue;
             }
             if (tid < H) mref_s[tid] = -INFINITY;
+            // this lane's share of the softmax denominators (heads 2 lane, 2 lane + 1, the
+            // warp's rows), rescaled with O whenever the reference maximum moves
+            float lacc0 = 0.f, lacc1 = 0.f;
             if (!soft_bar()) { ok = false; break; }
             for (int i = itm.tb; i < itm.te; i++, g++) {
                 const int sb = g & 1;
                 if (!mbar_wait(bar(B_SFULL0 + sb), (g >> 1) & 1, abort)) { ok = false; break; }
                 fence_after();
                 float s[H];
-                tmem_load<H>(lane_base + Lay::T_S + sb * H, s);
+                tmem_load_s<H>(lane_base + Lay::T_S + sb * 2 * H, s);
                 fence_before();
                 mbar_arrive(bar(B_SFREE0 + sb));
                 const bool valid = (i == 0) ? (r >= k.raw_lo && r <= k.raw_hi) : ((i - 1) * ROWS + r < nc);
@@ -747,26 +798,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                     // half of its heads selected by lane bit o and takes the partner's maxima for
                     // it, so after the five steps lane l holds heads 2l and 2l + 1.
                     static_assert(H == 64, "the butterfly below assumes 64 heads");
-                    float m[H / 2];
-                    {
-                        const bool up = (lane & 16) != 0;
-#pragma unroll
-                        for (int k = 0; k < H / 2; k++) {
-                            const float send = up ? s[k] : s[k + H / 2];
-                            const float keep = up ? s[k + H / 2] : s[k];
-                            m[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-                        }
-                    }
-#pragma unroll
-                    for (int o = 8; o > 0; o >>= 1) {
-                        const bool up = (lane & o) != 0;
-#pragma unroll
-                        for (int k = 0; k < 2 * o; k++) {
-                            const float send = up ? m[k] : m[k + 2 * o];
-                            const float keep = up ? m[k + 2 * o] : m[k];
-                            m[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
-                        }
-                    }
+                    float m[2];
+                    warp_heads_reduce<true>(s, m[0], m[1]);
                     // the four warps' maxima meet in one key per head (the previous
                     // tile's factors have been read by now: the vote barrier came after)
                     if (tid < H) tmax[tid] = 0u;
@@ -782,6 +815,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                         mref_s[tid] = mn;
                     }
                     if (!soft_bar()) { ok = false; break; }
+                    lacc0 *= alpha_s[2 * lane];
+                    lacc1 *= alpha_s[2 * lane + 1];
                     if (i > itm.tb) {
                         if (!mbar_wait(bar(B_PVDONE), (g - 1) & 1, abort)) { ok = false; break; }
                         waited = true;
@@ -793,10 +828,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                             for (int h = 0; h < H; h++) v[h] *= alpha_s[h];
                             tmem_store<H>(lane_base + Lay::T_O + j * H, v);
                         }
-                        tmem_load<H>(lane_base + Lay::T_L, v);
-#pragma unroll
-                        for (int h = 0; h < H; h++) v[h] *= alpha_s[h];
-                        tmem_store<H>(lane_base + Lay::T_L, v);
                         fence_before();
                     }
                 }
@@ -805,13 +836,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                 }
                 // P^T row r (MN-major, 128-byte swizzle), hi and lo
 #pragma unroll
+                for (int h = 0; h < H; h++) s[h] = exp2f(s[h] - mref_s[h]);
+#pragma unroll
                 for (int u = 0; u < H / 8; u++) {
                     float hv[8], lv[8];
 #pragma unroll
-                    for (int e = 0; e < 8; e++) {
-                        const float pv = exp2f(s[u * 8 + e] - mref_s[u * 8 + e]);
-                        split_bf16(pv, hv[e], lv[e]);
-                    }
+                    for (int e = 0; e < 8; e++) split_bf16(s[u * 8 + e], hv[e], lv[e]);
                     const int off = r * (H * 2) + ((u ^ (r & 7)) * 16);
                     *reinterpret_cast<uint4 *>(phi_p + off) = make_uint4(pack_bf16x2(hv[0], hv[1]), pack_bf16x2(hv[2], hv[3]),
                                                                          pack_bf16x2(hv[4], hv[5]), pack_bf16x2(hv[6], hv[7]));
@@ -820,23 +850,35 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                 }
                 fence_proxy_async();
                 mbar_arrive(bar(B_PFULL));
+                {
+                    float l0, l1;
+                    warp_heads_reduce<false>(s, l0, l1);
+                    lacc0 += l0;
+                    lacc1 += l1;
+                }
                 if (i == itm.te - 1) {
                     // the last S of this item has been read: split the next item's Q
                     const int nx = next_item(p, it + gridDim.x, n_items);
                     if (nx < n_items && !split_q()) { ok = false; break; }
                     if (!mbar_wait(bar(B_PVDONE), g & 1, abort)) { ok = false; break; }
                     fence_after();
+                    // the denominators: the four warps' shares meet in P hi (free until the
+                    // output staging below), then L[h] goes to the alpha words
+                    float *lpart = reinterpret_cast<float *>(phi_p);
+                    lpart[q4 * H + 2 * lane] = lacc0;
+                    lpart[q4 * H + 2 * lane + 1] = lacc1;
+                    if (!soft_bar()) { ok = false; break; }
+                    if (tid < H) alpha_s[tid] = lpart[tid] + lpart[H + tid] + lpart[2 * H + tid] + lpart[3 * H + tid];
+                    if (!soft_bar()) { ok = false; break; }
                     float l[H], v[H];
-                    tmem_load<H>(lane_base + Lay::T_L, l);
+#pragma unroll
+                    for (int h = 0; h < H; h++) l[h] = alpha_s[h];
                     // whole query: out[n][h][d] = O / L; split rows: the unnormalised partial
                     // part_o[it][h][d] plus this part's reference maximum and denominator
                     const bool whole = p.parts == 1;
                     if (!whole && tid < H) {
-                        float lt = 0.f;
-#pragma unroll
-                        for (int h = 0; h < H; h++) lt = (h == tid) ? l[h] : lt;
                         p.part_ml[(size_t)it * 2 * H + tid] = mref_s[tid];
-                        p.part_ml[(size_t)it * 2 * H + H + tid] = lt;
+                        p.part_ml[(size_t)it * 2 * H + H + tid] = alpha_s[tid];
                     }
 #pragma unroll
                     for (int h = 0; h < H; h++) l[h] = whole ? 1.0f / l[h] : 1.0f;

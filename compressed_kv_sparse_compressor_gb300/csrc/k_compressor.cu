@@ -386,6 +386,35 @@ __global__ void __launch_bounds__(128) compress_decode_r4_kernel(CompressArgs a,
     for (int col = threadIdx.x * 4; col < W; col += 128 * 4) commit_col(a, lane_id, dp, 1, seq, col);
 }
 
+// Prefill chunk of a ratio-4 layer in one launch for both lanes (256-thread
+// blocks).  The frontier a chunk starts from is read only by the pools of the
+// chunk's first two windows (c0 = pos0 / 4 takes its previous window from it,
+// and both c0 and c0 + 1 take the tokens pos0 - pos0 % 4 .. pos0 - 1 from it),
+// and the frontier commit rewrites it.  So block 0 pools the attention lane's
+// windows c0 and c0 + 1 and then, after a block barrier, commits that lane's
+// frontier; block 1 does the same for the indexer lane (windows c0 .. c0 + 7,
+// eight per block); the other blocks pool the remaining windows, which read
+// only the projection output.  No block waits on another.
+template <int GA, int GI>
+__global__ void __launch_bounds__(256) compress_prefill_r4_kernel(CompressArgs a, int att_blocks, DecodePos dp) {
+    __shared__ float red[32];
+    pdl_wait();
+    pdl_launch_dependents();
+    constexpr int PA = 256 / GA, PI = 256 / GI;          // windows per block of each lane
+    const int b = blockIdx.x;
+    if (b == 0 || b == 1) {
+        const int lane_id = b;
+        if (lane_id == 0) pool_r4<GA>(a, 0, dp, 0, threadIdx.x / GA, red);
+        else pool_r4<GI>(a, 1, dp, 0, threadIdx.x / GI, red);
+        __syncthreads();                                  // the frontier has been read
+        const int W = 2 * a.lane[lane_id].Dl;
+        for (int col = threadIdx.x * 4; col < W; col += 256 * 4) commit_col(a, lane_id, dp, 0, 0, col);
+        return;
+    }
+    if (b < 2 + att_blocks) pool_r4<GA>(a, 0, dp, 0, PA + (b - 2) * PA + threadIdx.x / GA, red);
+    else pool_r4<GI>(a, 1, dp, 0, PI + (b - 2 - att_blocks) * PI + threadIdx.x / GI, red);
+}
+
 cudaError_t pool_lane(const CompressArgs &a, int lane, const DecodePos &dp, int decode, int n_tasks, cudaStream_t s) {
     const int Dl = a.lane[lane].Dl;
     if (n_tasks <= 0) return cudaSuccess;
@@ -420,6 +449,27 @@ cudaError_t commit_lane(const CompressArgs &a, int lane, const DecodePos &dp, in
 cudaError_t launch_compress_prefill(const CompressArgs &a, cudaStream_t s) {
     DecodePos dp{};
     const uint64_t n_win = (a.pos0 + a.T) / a.ratio - a.pos0 / a.ratio;
+    if (a.ratio == 4 && a.n_lanes == 2) {
+        const int ga = a.lane[0].Dl / 4, gi = a.lane[1].Dl / 4;
+        // windows past the special blocks' first PA (attention) / PI (indexer) ones
+        auto rest = [&](int per) { return n_win > (uint64_t)per ? (int)((n_win - per + per - 1) / per) : 0; };
+#define DS4C_CPRE(A, I)                                                                              \
+        if (ga == A && gi == I) {                                                                   \
+            const int ab = rest(256 / A), ib = rest(256 / I);                                       \
+            return launch_pdl(compress_prefill_r4_kernel<A, I>, dim3(2 + ab + ib), dim3(256), 0, s, a, ab, dp); \
+        }
+        DS4C_CPRE(128, 32)
+        DS4C_CPRE(128, 16)
+        DS4C_CPRE(64, 16)
+        DS4C_CPRE(32, 16)
+        DS4C_CPRE(128, 64)
+        DS4C_CPRE(64, 32)
+        DS4C_CPRE(128, 128)
+        DS4C_CPRE(64, 64)
+        DS4C_CPRE(32, 32)
+        DS4C_CPRE(16, 16)
+#undef DS4C_CPRE
+    }
     for (int l = 0; l < a.n_lanes; l++) {
         cudaError_t e = pool_lane(a, l, dp, 0, (int)n_win, s);
         if (e != cudaSuccess) return e;

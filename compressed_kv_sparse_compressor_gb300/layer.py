@@ -86,6 +86,15 @@ class DeviceLayer:
                                             hidden.shape[0], pos0, _ptr(self.ws), self.ws_bytes, _stream()),
                   "ds4c_compress_prefill")
 
+    def compress_prefill_timed(self, hidden: torch.Tensor, pos0: int, after_projection: torch.cuda.Event):
+        """ds4c_compress_prefill with `after_projection` recorded between the projection GEMM and the
+        fused compressor (a measurement hook)."""
+        after_projection.record()       # creates the event on this device; the library re-records it in the call
+        abi.check(abi.ds4c_compress_prefill_timed(self.cfg, self.attn_w, self.idx_w, self.state, _ptr(hidden),
+                                                  hidden.shape[0], pos0, _ptr(self.ws), self.ws_bytes,
+                                                  after_projection.cuda_event, _stream()),
+                  "ds4c_compress_prefill_timed")
+
     def compress_decode(self, hidden: torch.Tensor, positions):
         pos = abi.u64_array(positions)
         abi.check(abi.ds4c_compress_decode_step(self.cfg, self.attn_w, self.idx_w, self.state, _ptr(hidden), pos,

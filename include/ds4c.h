@@ -158,6 +158,16 @@ DS4C_API ds4c_status ds4c_compress_prefill(const ds4c_layer_cfg *cfg, const ds4c
                                   const void *hidden, uint32_t n_tok, uint64_t pos0,
                                   void *ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Measurement helper, not a step of the path: ds4c_compress_prefill with
+ * `after_projection` (a CUDA event, required) recorded on `stream` between the
+ * projection GEMM and the fused compressor kernel, so that a caller can time
+ * the two apart with events of its own before and after the call.  Same
+ * arguments, checks and results as ds4c_compress_prefill otherwise. */
+DS4C_API ds4c_status ds4c_compress_prefill_timed(const ds4c_layer_cfg *cfg, const ds4c_lane_weights *attn,
+                                                 const ds4c_lane_weights *idx, const ds4c_layer_state *state,
+                                                 const void *hidden, uint32_t n_tok, uint64_t pos0, void *ws,
+                                                 size_t ws_bytes, cudaEvent_t after_projection, cudaStream_t stream);
+
 /* Compressor for one token of each of n_seq independent sequences, sequence b
  * at position pos_h[b] (host array).  hidden: [n_seq][d_model].  n_seq <= 1024. */
 DS4C_API ds4c_status ds4c_compress_decode_step(const ds4c_layer_cfg *cfg, const ds4c_lane_weights *attn,
