@@ -39,7 +39,8 @@ class Cfg(C.Structure):
                 ("idx_head_dim", C.c_int32), ("n_heads", C.c_int32), ("ratio", C.c_int32),
                 ("swa", C.c_int32), ("top_k", C.c_int32), ("comp_cap", C.c_int32),
                 ("idx_cap", C.c_int32), ("bf16", C.c_int32), ("rms_eps", C.c_float),
-                ("attn_scale", C.c_float), ("rope_base", C.c_double)]
+                ("attn_scale", C.c_float), ("rope_base", C.c_double), ("idx_heads", C.c_int32),
+                ("idx_qat", C.c_int32)]
 
 
 class LaneW(C.Structure):
@@ -81,6 +82,13 @@ def lib():
             "orc_checkpoint_gather": (C.c_int64, [P, P, LaneS, LaneS, U64, P]),
             "orc_checkpoint_scatter": (C.c_int64, [P, P, LaneS, LaneS, U64, P]),
             "orc_payload_write": (C.c_int64, [P, I, P, P, P, P, P, P, P]),
+            "orc_hadamard": (None, [P, I]),
+            "orc_e2m1_rne": (F, [F]),
+            "orc_fp4_scale_exp": (I, [F]),
+            "orc_fp4_roundtrip": (None, [P, I]),
+            "orc_indexer_qat": (None, [P, I]),
+            "orc_index_score_heads": (F, [P, P, P, I, I]),
+            "orc_indexer_topk_heads": (None, [P, P, P, P, P, I, P, P, C.c_int64]),
             "orc_payload_read": (C.c_int64, [P, I, P, P, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -128,11 +136,13 @@ class Layer:
     rms_eps: float
     attn_scale: float
     rope_base: float
+    idx_heads: int = 0
+    idx_qat: int = 0
 
     def c(self) -> Cfg:
         return Cfg(self.d_model, self.head_dim, self.n_rot, self.idx_head_dim, self.n_heads,
                    self.ratio, self.swa, self.top_k, self.comp_cap, self.idx_cap, int(self.bf16),
-                   self.rms_eps, self.attn_scale, self.rope_base)
+                   self.rms_eps, self.attn_scale, self.rope_base, self.idx_heads, self.idx_qat)
 
     @property
     def coff(self):
@@ -393,3 +403,69 @@ def payload_read(buf, states, max_tokens: int, vocab: int):
     n = lib().orc_payload_read(_p(buf), len(states), cfgs, rings, attn, idx, _p(f), _p(tok), _p(lg))
     assert n >= 0, "payload magic or version mismatch"
     return f, tok[:f[5]], lg[:f[9]]
+
+
+# --------------------------------------------------------------------------
+# Full indexer: Hadamard + FP4 round trip, multi-head score
+# --------------------------------------------------------------------------
+
+def hadamard(x) -> np.ndarray:
+    x = _f32(x).copy()
+    flat = x.reshape(-1, x.shape[-1])
+    for i in range(flat.shape[0]):
+        r = np.ascontiguousarray(flat[i])
+        lib().orc_hadamard(_p(r), r.shape[0])
+        flat[i] = r
+    return flat.reshape(x.shape)
+
+
+def e2m1_rne(y) -> np.ndarray:
+    y = _f32(y)
+    f = lib().orc_e2m1_rne
+    return np.array([f(float(v)) for v in y.ravel()], dtype=np.float32).reshape(y.shape)
+
+
+def fp4_scale_exp(amax: float) -> int:
+    return lib().orc_fp4_scale_exp(float(amax))
+
+
+def fp4_roundtrip(x) -> np.ndarray:
+    x = _f32(x).copy()
+    flat = x.reshape(-1, x.shape[-1])
+    for i in range(flat.shape[0]):
+        r = np.ascontiguousarray(flat[i])
+        lib().orc_fp4_roundtrip(_p(r), r.shape[0])
+        flat[i] = r
+    return flat.reshape(x.shape)
+
+
+def indexer_qat(x) -> np.ndarray:
+    x = _f32(x).copy()
+    flat = x.reshape(-1, x.shape[-1])
+    for i in range(flat.shape[0]):
+        r = np.ascontiguousarray(flat[i])
+        lib().orc_indexer_qat(_p(r), r.shape[0])
+        flat[i] = r
+    return flat.reshape(x.shape)
+
+
+def index_score_heads(q, w, row) -> float:
+    """q [heads][d] (after the round trip), w [heads], row [d]."""
+    q, w, row = _f32(q), _f32(w), _f32(row)
+    return lib().orc_index_score_heads(_p(q), _p(w), _p(row), q.shape[1], q.shape[0])
+
+
+def indexer_topk_heads(st: State, q_raw, w, positions, want_scores: bool = False):
+    """Multi-head top-k lists [n, k] (and scores) for queries q_raw [n, heads, d], weights w [n, heads]."""
+    L = st.L
+    cfg = L.c()
+    q_raw, w = _f32(q_raw), _f32(w)
+    assert q_raw.shape[1] == L.idx_heads and w.shape == q_raw.shape[:2]
+    pos = np.ascontiguousarray(positions, dtype=np.uint64)
+    n = pos.shape[0]
+    out = np.zeros((n, L.top_k), dtype=np.int32)
+    vmax = int((pos.max() + 1) // 4) if n else 0
+    scores = np.full((n, max(vmax, 1)), np.nan, dtype=np.float32) if want_scores else None
+    lib().orc_indexer_topk_heads(C.byref(cfg), _p(st.idx.comp), _p(q_raw), _p(w), _p(pos), n, _p(out), _p(scores),
+                                 max(vmax, 1))
+    return (out, scores) if want_scores else out

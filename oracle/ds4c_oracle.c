@@ -35,6 +35,8 @@ typedef struct {
     float rms_eps;
     float attn_scale;
     double rope_base;
+    int32_t idx_heads;     /* indexer query heads of the multi-head score (0 or 1: one query vector) */
+    int32_t idx_qat;       /* 1: the indexer rows and queries take the Hadamard + FP4 round trip */
 } orc_cfg;
 
 typedef struct {
@@ -184,6 +186,94 @@ void orc_fp8_roundtrip(float *row, int n_nope) {
 }
 
 /* ---------------------------------------------------------------------------
+ * Indexer QAT round trip.  "Metal グラフと圧縮 KV の実装を読む" §9: the indexer row
+ * (and, the page says, the indexer query) goes through a Hadamard transform of
+ * order 128 and an FP4 activation-quantisation round trip instead of the FP8
+ * one, so that the top-k selection follows the model's graph.
+ * READING R-16: the orthonormal Sylvester Hadamard transform y = H x / sqrt(n),
+ * H[i][j] = (-1)^popcount(i & j), evaluated as the fast Walsh-Hadamard
+ * transform in binary32 (stages h = 1, 2, 4, ..., n/2; stage h replaces each
+ * pair (x[j], x[j + h]) with j & h == 0 by (x[j] + x[j + h], x[j] - x[j + h]))
+ * followed by one binary32 multiply by binary32(1 / sqrt(n)).  The evaluation
+ * order is part of the reading because the FP4 rounding that follows decides
+ * codes from these binary32 values.
+ * READING R-17: OCP E2M1 (values 0, 0.5, 1, 1.5, 2, 3, 4, 6), round to nearest
+ * with ties to the even code, saturating at +-6; one power-of-two scale per
+ * block of 32 consecutive values, the smallest 2^e with amax <= 6 * 2^e (e = 0
+ * for an all-zero block); value = e2m1(x / 2^e) * 2^e.
+ * ------------------------------------------------------------------------- */
+void orc_hadamard(float *x, int n) {
+    for (int h = 1; h < n; h <<= 1) {
+        for (int j = 0; j < n; j++) {
+            if (j & h) continue;
+            float a = x[j], b = x[j + h];
+            x[j] = a + b;
+            x[j + h] = a - b;
+        }
+    }
+    const float c = (float)(1.0 / sqrt((double)n));
+    for (int j = 0; j < n; j++) x[j] = x[j] * c;
+}
+
+/* Value of the non-negative E2M1 code c (0..7): exponent bits c >> 1 (bias 1),
+ * mantissa bit c & 1; code 1 is the subnormal 0.5. */
+static double e2m1_value(int c) {
+    int E = c >> 1, m = c & 1;
+    if (E == 0) return 0.5 * (double)m;
+    return ldexp(1.0 + 0.5 * (double)m, E - 1);
+}
+
+/* Nearest E2M1 value to y, ties to the even code, saturating to +-6. */
+float orc_e2m1_rne(float y) {
+    double a = fabs((double)y);
+    double r;
+    if (a >= 6.0) {
+        r = 6.0;
+    } else {
+        int lo = 0;                                     /* largest code with value <= a */
+        for (int c = 0; c <= 7; c++)
+            if (e2m1_value(c) <= a) lo = c;
+        double vlo = e2m1_value(lo), vhi = e2m1_value(lo + 1);
+        double dlo = a - vlo, dhi = vhi - a;
+        if (dlo < dhi) r = vlo;
+        else if (dhi < dlo) r = vhi;
+        else r = ((lo & 1) == 0) ? vlo : vhi;
+    }
+    return (float)(signbit(y) ? -r : r);
+}
+
+/* Smallest integer e with amax <= 6 * 2^e; 0 when amax == 0. */
+int orc_fp4_scale_exp(float amax) {
+    if (!(amax > 0.0f)) return 0;
+    int e = 0;
+    while ((double)amax > ldexp(6.0, e)) e++;
+    while ((double)amax <= ldexp(6.0, e - 1)) e--;
+    return e;
+}
+
+void orc_fp4_roundtrip(float *x, int n) {
+    for (int b0 = 0; b0 < n; b0 += 32) {
+        int b1 = b0 + 32 < n ? b0 + 32 : n;
+        float amax = 0.0f;
+        for (int j = b0; j < b1; j++) {
+            float a = fabsf(x[j]);
+            if (a > amax) amax = a;
+        }
+        int e = orc_fp4_scale_exp(amax);
+        for (int j = b0; j < b1; j++) {
+            double y = ldexp((double)x[j], -e);         /* exact */
+            x[j] = (float)ldexp((double)orc_e2m1_rne((float)y), e);
+        }
+    }
+}
+
+/* The round trip of one indexer row or query head: Hadamard, then FP4. */
+void orc_indexer_qat(float *x, int n) {
+    orc_hadamard(x, n);
+    orc_fp4_roundtrip(x, n);
+}
+
+/* ---------------------------------------------------------------------------
  * A6. Tail RoPE.  [P2] §8, rope_tail_ext_inplace: only the last n_rot dims of
  * a head rotate (n_nope = head_dim - n_rot untouched).
  * READING (C-5): pairs (2i, 2i+1) of the tail; angle = float(p * inv_freq[i])
@@ -266,6 +356,7 @@ void orc_compress_token(const orc_cfg *cfg, int lane_is_attn, const float *ape, 
     for (int j = 0; j < Dl; j++) out[j] = (float)x[j];
     if (st.prequant) memcpy(st.prequant + (size_t)c * Dl, out, sizeof(float) * (size_t)Dl);
     if (lane_is_attn) orc_fp8_roundtrip(out, Dl - cfg->n_rot);
+    else if (cfg->idx_qat) orc_indexer_qat(out, Dl);
     free(x);
 
     /* ratio-4 shift (kernel_dsv4_ratio4_shift_f32): rows 4..7 -> rows 0..3 */
@@ -373,6 +464,48 @@ void orc_indexer_topk(const orc_cfg *cfg, const float *idx_comp, const float *q_
         if (scores_out)
             for (int c = 0; c < visible; c++) scores_out[(size_t)j * score_stride + c] = s[c];
         free(s);
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Multi-head indexer score ("Metal グラフと圧縮 KV の実装を読む" §6: 64 indexer heads
+ * of width 128 score each compressed row, four heads at a time).
+ * READING R-15: the heads' dot products with the row, each the in-order binary32
+ * fmaf chain of R-8, are clamped at zero (ReLU) and summed with per-query head
+ * weights w as one more in-order fmaf chain over the heads:
+ *   s = 0; for j = 0 .. heads-1: s = fmaf(w[j], max(dot_j, 0), s).
+ * q holds the heads' query vectors after the round trip, [heads][d].
+ * ------------------------------------------------------------------------- */
+float orc_index_score_heads(const float *q, const float *w, const float *row, int d, int heads) {
+    float s = 0.0f;
+    for (int j = 0; j < heads; j++) {
+        float dj = orc_index_score(q + (size_t)j * d, row, d);
+        s = fmaf(w[j], dj > 0.0f ? dj : 0.0f, s);
+    }
+    return s;
+}
+
+/* n queries of one sequence at positions pos[j]: q_raw [n][heads][d] (before the
+ * round trip; it is applied here when cfg->idx_qat), w [n][heads]; rows = that
+ * sequence's index_comp_kv; top-k as orc_indexer_topk. */
+void orc_indexer_topk_heads(const orc_cfg *cfg, const float *idx_comp, const float *q_raw, const float *w,
+                            const uint64_t *pos, int n, int32_t *topk, float *scores_out, int64_t score_stride) {
+    const int d = cfg->idx_head_dim, k = cfg->top_k, H = cfg->idx_heads;
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int j = 0; j < n; j++) {
+        float *q = (float *)malloc(sizeof(float) * (size_t)H * d);
+        memcpy(q, q_raw + (size_t)j * H * d, sizeof(float) * (size_t)H * d);
+        if (cfg->idx_qat)
+            for (int h = 0; h < H; h++) orc_indexer_qat(q + (size_t)h * d, d);
+        int visible = (int)((pos[j] + 1) / 4);
+        float *s = (float *)malloc(sizeof(float) * (size_t)(visible > 0 ? visible : 1));
+        for (int c = 0; c < visible; c++)
+            s[c] = orc_index_score_heads(q, w + (size_t)j * H, idx_comp + (size_t)c * d, d, H);
+        orc_topk(s, visible, k, topk + (size_t)j * k);
+        if (scores_out)
+            for (int c = 0; c < visible; c++) scores_out[(size_t)j * score_stride + c] = s[c];
+        free(s);
+        free(q);
     }
 }
 

@@ -636,3 +636,187 @@ def test_payload_round_trip_restores_every_layer(orc):
     bad[0] ^= 1
     with pytest.raises(AssertionError):
         orc.payload_read(bad, [orc.State(s.L) for s in states], pos, 5)
+
+
+# --------------------------------------------------------------------------
+# Full indexer: Hadamard + FP4 round trip, multi-head score
+# ("Metal グラフと圧縮 KV の実装を読む" §6 and §9)
+# --------------------------------------------------------------------------
+
+def _sylvester(n):
+    return np.array([[(-1) ** bin(i & j).count("1") for j in range(n)] for i in range(n)], dtype=np.float64)
+
+
+def test_hadamard_sylvester_and_evaluation(orc):
+    g = _golden("hadamard_sylvester.json")
+    for name, n in (("H2", 2), ("H4", 4), ("H8", 8)):
+        np.testing.assert_array_equal(_sylvester(n), np.array(g[name], dtype=np.float64))
+    for n in (2, 8, 64, 128):
+        Hm = _sylvester(n)
+        np.testing.assert_array_equal(Hm @ Hm.T, n * np.eye(n))
+        c = np.float32(1.0 / math.sqrt(n))
+        # unit vectors: every butterfly step is exact, so column k comes out as H[:, k] * fp32(1/sqrt(n))
+        for k in sorted({0, 1, min(n // 2 + 1, n - 1), n - 1}):
+            e = np.zeros(n, np.float32)
+            e[k] = 1.0
+            np.testing.assert_array_equal(orc.hadamard(e), (Hm[:, k] * np.float64(c)).astype(np.float32))
+        rng = np.random.default_rng(n)
+        for _ in range(20):
+            x = rng.standard_normal(n).astype(np.float32)
+            y = orc.hadamard(x)
+            exact = Hm @ x.astype(np.float64) / math.sqrt(n)
+            # log2(n) rounded add/sub stages and one rounded multiply
+            bound = (math.log2(n) + 2) * 2.0 ** -24 * np.abs(x).astype(np.float64).sum() / math.sqrt(n) * 2
+            assert np.max(np.abs(y - exact)) <= bound
+            np.testing.assert_allclose(np.linalg.norm(y), np.linalg.norm(x), rtol=1e-5)
+            np.testing.assert_allclose(orc.hadamard(y), x, rtol=1e-5, atol=1e-5)     # orthonormal and symmetric
+
+
+def test_hadamard_evaluation_order_is_the_butterfly(orc):
+    """The binary32 values are those of the stage-by-stage butterfly (written out here
+    independently), not of a row-by-row matrix product: the FP4 codes depend on them."""
+    rng = np.random.default_rng(21)
+    n = 128
+    Hm = _sylvester(n)
+    differs = 0
+    for _ in range(50):
+        x = (rng.standard_normal(n) * 10.0 ** rng.uniform(-3, 3, n)).astype(np.float32)
+        y = x.copy()
+        h = 1
+        while h < n:
+            for j in range(n):
+                if j & h == 0:
+                    a, b = y[j], y[j + h]
+                    y[j], y[j + h] = np.float32(a + b), np.float32(a - b)
+            h *= 2
+        y = (y * np.float32(1.0 / math.sqrt(n))).astype(np.float32)
+        np.testing.assert_array_equal(orc.hadamard(x), y)
+        rowwise = np.array([np.float32(np.sum((Hm[i] * x).astype(np.float32), dtype=np.float32)) for i in range(n)],
+                           np.float32) * np.float32(1.0 / math.sqrt(n))
+        differs += int(np.any(rowwise != y))
+    assert differs > 0
+
+
+def test_e2m1_format_golden(orc):
+    g = _golden("e2m1_format.json")
+    for v in g["values"]:
+        assert orc.e2m1_rne(np.float32(v)) == v and orc.e2m1_rne(np.float32(-v)) == -v
+    for y, want in g["round_cases"]:
+        assert orc.e2m1_rne(np.float32(y)) == np.float32(want), y
+    # brute force over a fine grid: nearest grid value, ties to the even code
+    grid = np.array(g["values"])
+    for y in np.linspace(0, 7, 2801):
+        a = min(abs(y), 6.0)
+        d = np.abs(grid - a)
+        best = np.flatnonzero(d == d.min())
+        code = best[0] if len(best) == 1 else [c for c in best if c % 2 == 0][0]
+        assert orc.e2m1_rne(np.float32(y)) == np.float32(grid[code])
+
+
+def test_fp4_roundtrip_properties(orc):
+    rng = np.random.default_rng(23)
+    g = np.array(_golden("e2m1_format.json")["values"])
+    for a in np.concatenate([10.0 ** rng.uniform(-6, 6, 300), [6.0, 3.0, 12.0, 6.0000005]]):
+        a = np.float32(a)
+        e = orc.fp4_scale_exp(a)
+        assert a <= 6.0 * 2.0 ** e and a > 6.0 * 2.0 ** (e - 1)
+    assert orc.fp4_scale_exp(0.0) == 0
+    x = (rng.standard_normal((5, 128)) * rng.uniform(0.01, 100, (5, 1))).astype(np.float32)
+    x[2, 32:64] = 0.0
+    y = orc.fp4_roundtrip(x)
+    np.testing.assert_array_equal(y[2, 32:64], 0.0)
+    for i in range(5):
+        for b in range(4):
+            blk, src = y[i, 32 * b:32 * b + 32], x[i, 32 * b:32 * b + 32]
+            e = orc.fp4_scale_exp(np.max(np.abs(src)))
+            mags = np.abs(blk.astype(np.float64)) * 2.0 ** -e
+            assert np.all(np.isin(mags, g))                                      # on the grid
+            # half a grid step: at most 0.25 * 2^e below magnitude 2^e, at most a quarter of |x| above it
+            assert np.all(np.abs(blk - src) <= np.maximum(0.25 * 2.0 ** e, 0.25 * np.abs(src)))
+            # each block depends on its own 32 values only
+            z = x[i].copy()
+            z[(32 * b + 32) % 128:(32 * b + 32) % 128 + 32] *= 3.0
+            np.testing.assert_array_equal(orc.fp4_roundtrip(z)[32 * b:32 * b + 32], blk)
+    np.testing.assert_array_equal(orc.fp4_roundtrip(y), y)                       # fixed points
+    np.testing.assert_array_equal(orc.indexer_qat(x), orc.fp4_roundtrip(orc.hadamard(x)))
+
+
+def test_index_score_heads_is_the_in_order_chain(orc):
+    """Per-head fmaf chains, ReLU, and the weighted head sum as one more in-order fmaf
+    chain, computed here in exact rational arithmetic."""
+    from fractions import Fraction
+
+    from fp_exact import fma_chain, round_f32
+    rng = np.random.default_rng(29)
+    separated = 0
+    for trial in range(60):
+        H, d = int(rng.integers(1, 7)), int(rng.integers(2, 9))
+        q = rng.uniform(-2, 2, (H, d)).astype(np.float32)
+        w = rng.uniform(-1.5, 2, H).astype(np.float32)
+        row = rng.uniform(-2, 2, d).astype(np.float32)
+        dots = [fma_chain(q[j], row) for j in range(H)]
+        s = np.float32(0.0)
+        for j in range(H):
+            r = dots[j] if dots[j] > 0 else np.float32(0.0)
+            s = round_f32(Fraction(float(w[j])) * Fraction(float(r)) + Fraction(float(s)))
+        assert np.float32(orc.index_score_heads(q, w, row)) == s, trial
+        # an unfused head sum, or no ReLU, would give another value on some of these
+        u = np.float32(0.0)
+        for j in range(H):
+            r = dots[j] if dots[j] > 0 else np.float32(0.0)
+            u = np.float32(u + np.float32(w[j] * r))
+        nr = np.float32(0.0)
+        for j in range(H):
+            nr = round_f32(Fraction(float(w[j])) * Fraction(float(dots[j])) + Fraction(float(nr)))
+        separated += int(u != s) + int(nr != s)
+    assert separated > 10
+
+
+def test_indexer_topk_heads_brute_force(orc):
+    from compressed_kv_sparse_compressor_gb300 import configs as cf
+    for qat in (0, 1):
+        shape = cf.LayerShape(d_model=64, head_dim=128, n_rot=32, idx_head_dim=64, n_heads=8, ratio=4, top_k=5,
+                              dtype="f32")
+        L = orc_layer(shape, comp_cap=40, idx_cap=40)
+        L.idx_heads, L.idx_qat = 4, qat
+        st = orc.State(L)
+        rng = np.random.default_rng(31 + qat)
+        st.idx.comp[:] = rng.standard_normal(st.idx.comp.shape).astype(np.float32)
+        pos = np.array([0, 3, 7, 19, 25, 101, 159])
+        q = rng.standard_normal((len(pos), 4, 64)).astype(np.float32)
+        w = rng.uniform(0.1, 1, (len(pos), 4)).astype(np.float32)
+        tk, sc = orc.indexer_topk_heads(st, q, w, pos, want_scores=True)
+        for j, t in enumerate(pos):
+            V = (t + 1) // 4
+            qj = orc.indexer_qat(q[j]) if qat else q[j]
+            s = [orc.index_score_heads(qj, w[j], st.idx.comp[c]) for c in range(V)]
+            want = sorted(sorted(range(V), key=lambda c: (-s[c], c))[:5])
+            assert tk[j].tolist() == want + [-1] * (5 - len(want))
+            np.testing.assert_array_equal(sc[j, :V], np.array(s, np.float32))
+            # the score is a ReLU-weighted sum: with one head and w = 1 it is max(dot, 0)
+            d0 = orc.index_score(qj[0], st.idx.comp[0]) if V else 0.0
+            if V:
+                np.testing.assert_equal(np.float32(orc.index_score_heads(qj[:1], np.ones(1, np.float32),
+                                                                         st.idx.comp[0])), np.float32(max(d0, 0.0)))
+
+
+def test_compressor_indexer_lane_qat(orc):
+    """With the round trip on, every indexer row is the QAT image of the row the
+    same compressor makes without it (after RMSNorm and RoPE); the attention lane
+    is unchanged."""
+    shape = _small_shape(4, D=128, d=64, R=32)
+    wa = configs.lane_weights(shape, 3, 0, "attn")
+    wi = configs.lane_weights(shape, 3, 0, "idx")
+    h = configs.hidden(shape, 3, 37)
+    outs = []
+    for qat in (0, 1):
+        L = orc_layer(shape, comp_cap=16, idx_cap=16)
+        L.idx_qat = qat
+        st = orc.State(L)
+        orc.state_init(st)
+        orc.compress(st, lane_np(wa), lane_np(wi), np_in(h), 0)
+        outs.append(st)
+    n = 37 // 4
+    np.testing.assert_array_equal(outs[1].attn.comp[:n], outs[0].attn.comp[:n])
+    np.testing.assert_array_equal(outs[1].idx.comp[:n], orc.indexer_qat(outs[0].idx.comp[:n]))
+    np.testing.assert_array_equal(outs[1].idx.state_kv, outs[0].idx.state_kv)
