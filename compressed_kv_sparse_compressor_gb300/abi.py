@@ -28,6 +28,7 @@ EXPORTS = (
     "ds4c_sync_status", "ds4c_status_string", "ds4c_last_cuda_error", "ds4c_attn_uses_tensor_cores",
     "ds4c_indexer_topk_noalloc", "ds4c_checkpoint_scatter", "ds4c_payload_header", "ds4c_fma_probe",
     "ds4c_payload_bytes", "ds4c_payload_write", "ds4c_payload_read", "ds4c_compress_prefill_timed",
+    "ds4c_indexer_topk_heads",
 )
 PAYLOAD_U32_FIELDS = 13
 NOALLOC_SCORE_FLOATS = 2 * 1024 * 1024
@@ -47,7 +48,8 @@ class LayerCfg(C.Structure):
                 ("idx_head_dim", C.c_uint32), ("n_heads", C.c_uint32), ("ratio", C.c_uint32),
                 ("swa", C.c_uint32), ("top_k", C.c_uint32), ("comp_cap", C.c_uint32),
                 ("idx_cap", C.c_uint32), ("dtype", C.c_uint32), ("rms_eps", C.c_float),
-                ("attn_scale", C.c_float), ("rope_base", C.c_float)]
+                ("attn_scale", C.c_float), ("rope_base", C.c_float), ("idx_heads", C.c_uint32),
+                ("idx_qat", C.c_uint32)]
 
 
 class LaneWeights(C.Structure):
@@ -91,6 +93,7 @@ def lib() -> C.CDLL:
         "ds4c_compress_prefill_timed": (st, [cfgp, lwp, lwp, lsp, P, U32, U64, P, SZ, P, P]),
         "ds4c_compress_decode_step": (st, [cfgp, lwp, lwp, lsp, P, C.POINTER(U64), U32, P, SZ, P]),
         "ds4c_indexer_topk": (st, [cfgp, lsp, P, C.POINTER(U64), U32, U32, P, P, SZ, P, SZ, P]),
+        "ds4c_indexer_topk_heads": (st, [cfgp, lsp, P, P, C.POINTER(U64), U32, U32, P, P, SZ, P, SZ, P]),
         "ds4c_sparse_swa_attn": (st, [cfgp, lsp, P, P, P, C.POINTER(U64), U32, U32, P, C.c_int, P, SZ, P]),
         "ds4c_indexer_topk_noalloc": (st, [cfgp, lsp, P, C.POINTER(U64), U32, U32, P, P]),
         "ds4c_checkpoint_floats": (SZ, [cfgp, U64]),
@@ -164,6 +167,12 @@ def ds4c_compress_decode_step(cfg, attn_w, idx_w, state, hidden, pos_h, n_seq, w
 def ds4c_indexer_topk(cfg, state, q_idx, pos_h, n_seq, n_tok, topk, scores, score_stride, ws, ws_bytes, stream):
     return lib().ds4c_indexer_topk(C.byref(cfg), C.byref(state), q_idx, pos_h, n_seq, n_tok, topk, scores,
                                    score_stride, ws, ws_bytes, stream)
+
+
+def ds4c_indexer_topk_heads(cfg, state, q_idx, w_idx, pos_h, n_seq, n_tok, topk, scores, score_stride, ws, ws_bytes,
+                            stream):
+    return lib().ds4c_indexer_topk_heads(C.byref(cfg), C.byref(state), q_idx, w_idx, pos_h, n_seq, n_tok, topk,
+                                         scores, score_stride, ws, ws_bytes, stream)
 
 
 def ds4c_indexer_topk_noalloc(cfg, state, q_idx, pos_h, n_seq, n_tok, topk, stream):

@@ -30,6 +30,8 @@ class LayerShape:
     ape_std: float = 0.1
     rope_base: float = 10000.0
     rms_eps: float = 1e-6
+    idx_heads: int = 0     # indexer query heads of the multi-head score (0: one query vector)
+    idx_qat: int = 0       # 1: the indexer rows and queries take the Hadamard + FP4 round trip
 
     @property
     def coff(self) -> int:

@@ -35,6 +35,8 @@ ds4c_status check_cfg(const ds4c_layer_cfg *c) {
         if (!pow2_width(c->idx_head_dim) || c->n_rot > c->idx_head_dim) return DS4C_ERR_SHAPE;
         if (c->top_k == 0 || c->top_k > 2048) return DS4C_ERR_SHAPE;
         if (c->idx_cap == 0 || c->idx_cap > kMaxIdxCap) return DS4C_ERR_SHAPE;
+        if (c->idx_heads > 64 || c->idx_qat > 1) return DS4C_ERR_SHAPE;
+        if (c->idx_qat && c->idx_head_dim != 64 && c->idx_head_dim != 128) return DS4C_ERR_SHAPE;
     }
     return DS4C_OK;
 }
@@ -65,6 +67,8 @@ int proj_width(const ds4c_layer_cfg &c, bool attn) { return coff_of(c) * lane_wi
 //           over `parts` work items: [n_seq*parts][H][D] + [n_seq*parts][2][H] float
 //   gemm:   decode steps of bf16 layers with at most 128 sequences: split-K
 //           partials of the projections, [kSplitK][rows][P] float
+//   qheads: ratio-4 layers with indexer heads and the round trip: the heads'
+//           query vectors after it, [rows][idx_heads][idx_head_dim] float
 constexpr int kSplitK = 16;
 struct WsLayout {
     size_t proj_off, proj_ld;
@@ -72,6 +76,7 @@ struct WsLayout {
     size_t mirror_off;
     size_t part_o_off, part_ml_off;
     size_t gemm_part_off;            // 0: no split-K region
+    size_t qheads_off;               // 0: no region
     int parts;
     size_t total;
 };
@@ -106,6 +111,10 @@ WsLayout ws_layout(const ds4c_layer_cfg &c, uint32_t rows, uint64_t mirror_rows,
     if (decode && c.dtype == DS4C_BF16 && P > 0 && rows <= 128) {
         L.gemm_part_off = o;
         o += align_up(sizeof(float) * (size_t)kSplitK * rows * P, 256);
+    }
+    if (c.ratio == 4 && c.idx_heads > 0 && c.idx_qat) {
+        L.qheads_off = o;
+        o += align_up(sizeof(float) * (size_t)rows * c.idx_heads * c.idx_head_dim, 256);
     }
     L.total = o < 256 ? 256 : o;
     return L;
@@ -195,6 +204,8 @@ ds4c_status run_compress(const ds4c_layer_cfg *cfg, const ds4c_lane_weights *aw,
         la.Dl = lane_width(c, attn);
         la.cap = (int)(attn ? c.comp_cap : c.idx_cap);
         la.is_attn = attn ? 1 : 0;
+        la.qat = (!attn && c.idx_qat) ? 1 : 0;
+        la.qat_c = (float)(1.0 / sqrt((double)la.Dl));
     }
     if (dp == nullptr) {
         a.n_seg = 1;
@@ -402,6 +413,66 @@ ds4c_status ds4c_indexer_topk(const ds4c_layer_cfg *cfg, const ds4c_layer_state 
     a.pos0 = pos_h[0];
     cudaError_t e = (n_seq == 1) ? launch_indexer_prefill(a, stream) : launch_indexer_decode(a, dp, stream);
     return cuda_status(e);
+}
+
+ds4c_status ds4c_indexer_topk_heads(const ds4c_layer_cfg *cfg, const ds4c_layer_state *st, const float *q_idx,
+                                    const float *w_idx, const uint64_t *pos_h, uint32_t n_seq, uint32_t n_tok,
+                                    int32_t *topk, float *scores, size_t score_stride, void *ws, size_t ws_bytes,
+                                    cudaStream_t stream) {
+    ds4c_status s = check_cfg(cfg);
+    if (s != DS4C_OK) return s;
+    const ds4c_layer_cfg &c = *cfg;
+    if (c.ratio != 4 || c.idx_heads == 0) return DS4C_ERR_SHAPE;
+    if (c.idx_head_dim != 64 && c.idx_head_dim != 128) return DS4C_ERR_SHAPE;
+    if (n_seq == 0 || n_tok == 0) return DS4C_ERR_SHAPE;
+    if (n_seq > 1 && n_tok > 1) return DS4C_ERR_UNSUPPORTED;
+    if (n_seq > (uint32_t)kMaxDecodeSeq) return DS4C_ERR_UNSUPPORTED;
+    if (!st || !q_idx || !w_idx || !pos_h || !topk || !st->idx.comp) return DS4C_ERR_NULL;
+    if (!aligned16(q_idx) || !aligned16(w_idx) || !aligned16(st->idx.comp) || !aligned16(topk) || !aligned16(scores))
+        return DS4C_ERR_SHAPE;
+    const uint32_t rows = n_seq * n_tok;
+    uint64_t vis_max = 0;
+    DecodePos dp;
+    if (n_seq == 1) {
+        vis_max = (pos_h[0] + n_tok) / 4;
+    } else {
+        for (uint32_t b = 0; b < n_seq; b++) {
+            dp.pos[b] = pos_h[b];
+            const uint64_t v = (pos_h[b] + 1) / 4;
+            vis_max = v > vis_max ? v : vis_max;
+        }
+    }
+    if (vis_max > c.idx_cap) return DS4C_ERR_CAPACITY;
+    if (scores && score_stride < vis_max) return DS4C_ERR_CAPACITY;
+    if (!ws) return DS4C_ERR_WORKSPACE;
+    const WsLayout L = (n_seq == 1) ? ws_prefill(c, rows) : ws_decode(c, rows);
+    if (ws_bytes < L.total) return DS4C_ERR_WORKSPACE;
+    IndexerArgs a{};
+    a.q = q_idx;
+    if (c.idx_qat) {
+        // the heads' query vectors take the same round trip as the rows
+        float *qh = reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + L.qheads_off);
+        cudaError_t e = launch_qat_vectors(q_idx, qh, (int64_t)rows * c.idx_heads, (int)c.idx_head_dim,
+                                           (float)(1.0 / sqrt((double)c.idx_head_dim)), stream);
+        if (e != cudaSuccess) return cuda_status(e);
+        a.q = qh;
+    }
+    a.rows = st->idx.comp;
+    a.seq_stride = (int64_t)c.idx_cap * c.idx_head_dim;
+    if (scores) {
+        a.scores = scores;
+        a.lds = (int64_t)score_stride;
+    } else {
+        a.scores = reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + L.scores_off);
+        a.lds = (int64_t)L.scores_ld;
+    }
+    a.topk = topk;
+    a.d = (int)c.idx_head_dim;
+    a.k = (int)c.top_k;
+    a.n_seq = (int)n_seq;
+    a.n_tok = (int)n_tok;
+    a.pos0 = pos_h[0];
+    return cuda_status(launch_indexer_heads(a, w_idx, (int)c.idx_heads, n_seq > 1 ? &dp : nullptr, stream));
 }
 
 ds4c_status ds4c_sparse_swa_attn(const ds4c_layer_cfg *cfg, const ds4c_layer_state *st, const float *q,

@@ -51,6 +51,70 @@ cudaError_t launch_fma_probe(uint32_t blocks, uint32_t iters, float *out, cudaSt
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// ----------------------------------------------------------------------------
+// Indexer QAT round trip of one row held by G consecutive threads, four values
+// each (element 4t + e in thread t of the group, e = x, y, z, w): the
+// orthonormal Sylvester Hadamard transform evaluated as the binary32 fast
+// Walsh-Hadamard butterfly (stage h combines x[j], x[j + h] with j & h == 0
+// into x[j] + x[j + h], x[j] - x[j + h]) and one multiply by c = binary32(1 /
+// sqrt(4G)), then an FP4 E2M1 round trip with one power-of-two scale per block
+// of 32 values ("Metal グラフと圧縮 KV の実装を読む" §9: Hadamard 128 and FP4 on the
+// indexer row and queries; the evaluation order, block and scale rule are this
+// library's reading).  G <= 32, the group aligned inside its warp; every lane
+// of the warp calls this.
+// ----------------------------------------------------------------------------
+// Nearest E2M1 value (0, 0.5, 1, 1.5, 2, 3, 4, 6) to y, ties to the even code,
+// saturating at +-6; the sign of y is kept.
+__device__ __forceinline__ float e2m1_rne(float y) {
+    const float a = fabsf(y);
+    float r;
+    if (a <= 0.25f) r = 0.0f;          // 0.25: tie between codes 0 and 1 -> 0
+    else if (a < 0.75f) r = 0.5f;      // 0.75: tie -> 1.0 (code 2)
+    else if (a <= 1.25f) r = 1.0f;     // 1.25: tie -> 1.0 (code 2)
+    else if (a < 1.75f) r = 1.5f;      // 1.75: tie -> 2.0 (code 4)
+    else if (a <= 2.5f) r = 2.0f;      // 2.5: tie -> 2.0 (code 4)
+    else if (a < 3.5f) r = 3.0f;       // 3.5: tie -> 4.0 (code 6)
+    else if (a <= 5.0f) r = 4.0f;      // 5.0: tie -> 4.0 (code 6)
+    else r = 6.0f;
+    return copysignf(r, y);
+}
+
+// Smallest e with amax <= 6 * 2^e (0 for amax == 0).  With amax = m * 2^E,
+// m in [0.5, 1): 6 * 2^(E-3) = 0.75 * 2^E, so e = E - 3 when m <= 0.75, else E - 2.
+__device__ __forceinline__ int fp4_scale_exp(float amax) {
+    if (!(amax > 0.f)) return 0;
+    int E;
+    const float m = frexpf(amax, &E);                     // exact
+    return (m <= 0.75f) ? E - 3 : E - 2;
+}
+
+template <int G>
+__device__ __forceinline__ void indexer_qat_group(float4 &v, float c) {
+    static_assert(G >= 8 && G <= 32 && (G & (G - 1)) == 0, "QAT groups of 8 .. 32 threads");
+    const int t = threadIdx.x % G;
+    // stages h = 1 and 2 inside the thread
+    float a0 = v.x + v.y, a1 = v.x - v.y, a2 = v.z + v.w, a3 = v.z - v.w;
+    v = make_float4(a0 + a2, a1 + a3, a0 - a2, a1 - a3);
+    // stages h = 4 .. 2G across threads: partner t ^ (h / 4)
+#pragma unroll
+    for (int o = 1; o < G; o <<= 1) {
+        const float4 p = make_float4(__shfl_xor_sync(0xffffffffu, v.x, o), __shfl_xor_sync(0xffffffffu, v.y, o),
+                                     __shfl_xor_sync(0xffffffffu, v.z, o), __shfl_xor_sync(0xffffffffu, v.w, o));
+        if ((t & o) == 0) v = make_float4(v.x + p.x, v.y + p.y, v.z + p.z, v.w + p.w);
+        else v = make_float4(p.x - v.x, p.y - v.y, p.z - v.z, p.w - v.w);
+    }
+    v = make_float4(v.x * c, v.y * c, v.z * c, v.w * c);
+    // FP4: a block of 32 values is 8 consecutive threads
+    float am = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    const int e = fp4_scale_exp(am);
+    v.x = ldexpf(e2m1_rne(ldexpf(v.x, -e)), e);
+    v.y = ldexpf(e2m1_rne(ldexpf(v.y, -e)), e);
+    v.z = ldexpf(e2m1_rne(ldexpf(v.z, -e)), e);
+    v.w = ldexpf(e2m1_rne(ldexpf(v.w, -e)), e);
+}
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                               Args &&...args) {
@@ -110,6 +174,8 @@ struct LaneArgs {
     float *skv, *ssc;                  // [n_seq][coff*ratio][W]
     uint16_t *split;                   // attention lane: [n_seq][cap][2][Dl] bf16 hi, lo (or null)
     int Dl, cap, is_attn;
+    int qat;                           // indexer lane: Hadamard + FP4 round trip of each appended row
+    float qat_c;                       // binary32(1 / sqrt(Dl)) of that round trip
 };
 struct CompressArgs {
     LaneArgs lane[2];
@@ -143,6 +209,12 @@ struct IndexerArgs {
     uint64_t pos0;           // prefill
 };
 cudaError_t launch_indexer_prefill(const IndexerArgs &a, cudaStream_t s);
+// Multi-head score (heads > 1, or one head with the ReLU-weighted form): q holds
+// the heads' query vectors [n][heads][d] (after the round trip), w [n][heads];
+// then the same top-k.  dp == nullptr for a prefill chunk of one sequence.
+cudaError_t launch_indexer_heads(const IndexerArgs &a, const float *w, int heads, const DecodePos *dp, cudaStream_t s);
+// Hadamard + FP4 round trip of n_vec vectors of d floats (d = 64 or 128), in -> out.
+cudaError_t launch_qat_vectors(const float *in, float *out, int64_t n_vec, int d, float c, cudaStream_t s);
 cudaError_t launch_indexer_decode(const IndexerArgs &a, const DecodePos &p, cudaStream_t s);
 // device error word of the indexer kernels (a bounded wait gave up); read and cleared
 unsigned int idx_read_clear_error();

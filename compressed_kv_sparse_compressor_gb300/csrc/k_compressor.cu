@@ -109,6 +109,10 @@ __device__ __forceinline__ void finish_row(const CompressArgs &a, const LaneArgs
     }
     const size_t off = ((size_t)seq * L.cap + (size_t)c) * Dl + j;
     if (active && L.prequant) st4(L.prequant + off, y);
+    if constexpr (G >= 8 && G <= 32) {
+        // indexer lane: Hadamard + FP4 round trip of the whole row ("Metal グラフと圧縮 KV の実装を読む" §9)
+        if (!L.is_attn && L.qat) indexer_qat_group<G>(y, L.qat_c);
+    }
     if (L.is_attn) {
         float am = (j < nope) ? fmaxf(fmaxf(fabsf(y.x), fabsf(y.y)), fmaxf(fabsf(y.z), fabsf(y.w))) : 0.f;
 #pragma unroll

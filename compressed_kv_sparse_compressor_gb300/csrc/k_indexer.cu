@@ -694,6 +694,95 @@ cudaError_t launch_topk(const IndexerArgs &a, const DecodePos &dp, int n_q, uint
     return cudaErrorNotSupported;
 }
 
+
+// ---------------------------------------------------------------------------
+// Multi-head indexer score ("Metal グラフと圧縮 KV の実装を読む" §6: 64 indexer heads
+// score each compressed row).  Per query and row: for each head j the in-order
+// fp32 fma chain of its query vector with the row, clamped at zero, then the
+// weighted head sum as one more in-order fma chain, s = fma(w[j], relu(dot_j), s)
+// (this library's reading of the head combine).  A 128-thread block scores 128
+// rows (one per thread, the row held in registers) for QB queries whose head
+// vectors and weights sit in shared memory (read as broadcasts).  Prefill: QB
+// consecutive queries of one sequence; decode: one query (its sequence) per block.
+// ---------------------------------------------------------------------------
+template <int DD, int QB>
+__global__ void __launch_bounds__(128) score_heads_kernel(IndexerArgs a, const float *__restrict__ w, int heads,
+                                                          DecodePos dp, int decode) {
+    extern __shared__ __align__(16) float hsm[];
+    float *qs = hsm;                                   // [QB][heads][DD]
+    float *ws = hsm + (size_t)QB * heads * DD;         // [QB][heads]
+    pdl_wait();
+    pdl_launch_dependents();
+    const int n_q = decode ? a.n_seq : a.n_tok;
+    const int qb0 = blockIdx.y * QB;
+    const int seq = decode ? qb0 : 0;
+    uint64_t vis[QB];
+    uint64_t vmax = 0;
+#pragma unroll
+    for (int k = 0; k < QB; k++) {
+        const int n = qb0 + k;
+        vis[k] = 0;
+        if (n < n_q) vis[k] = decode ? (dp.pos[n] + 1) / 4 : (a.pos0 + (uint64_t)n + 1) / 4;
+        vmax = vis[k] > vmax ? vis[k] : vmax;
+    }
+    const uint64_t c0 = (uint64_t)blockIdx.x * 128;
+    if (c0 >= vmax) return;                            // block-uniform, before any barrier
+    const int hd = heads * DD;
+    for (int i = threadIdx.x; i < QB * hd; i += 128) {
+        const int k = i / hd;
+        qs[i] = (qb0 + k < n_q) ? a.q[(size_t)(qb0 + k) * hd + (i - k * hd)] : 0.f;
+    }
+    for (int i = threadIdx.x; i < QB * heads; i += 128) {
+        const int k = i / heads;
+        ws[i] = (qb0 + k < n_q) ? w[(size_t)(qb0 + k) * heads + (i - k * heads)] : 0.f;
+    }
+    __syncthreads();
+    const uint64_t c = c0 + threadIdx.x;
+    if (c >= vmax) return;
+    const float4 *row = reinterpret_cast<const float4 *>(a.rows + (size_t)seq * a.seq_stride + (size_t)c * DD);
+    float4 v[DD / 4];
+#pragma unroll
+    for (int i = 0; i < DD / 4; i++) v[i] = __ldg(row + i);
+    float s[QB];
+#pragma unroll
+    for (int k = 0; k < QB; k++) s[k] = 0.f;
+    for (int j = 0; j < heads; j++) {
+        float acc[QB];
+#pragma unroll
+        for (int k = 0; k < QB; k++) acc[k] = 0.f;
+#pragma unroll
+        for (int i = 0; i < DD / 4; i++) {
+#pragma unroll
+            for (int k = 0; k < QB; k++) {
+                const float4 q4 = *reinterpret_cast<const float4 *>(qs + ((size_t)k * heads + j) * DD + 4 * i);
+                acc[k] = __fmaf_rn(q4.x, v[i].x, acc[k]);
+                acc[k] = __fmaf_rn(q4.y, v[i].y, acc[k]);
+                acc[k] = __fmaf_rn(q4.z, v[i].z, acc[k]);
+                acc[k] = __fmaf_rn(q4.w, v[i].w, acc[k]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < QB; k++) s[k] = __fmaf_rn(ws[k * heads + j], acc[k] > 0.f ? acc[k] : 0.f, s[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < QB; k++)
+        if (qb0 + k < n_q && c < vis[k]) a.scores[(size_t)(qb0 + k) * a.lds + c] = s[k];
+}
+
+// Hadamard + FP4 round trip of n_vec vectors of 4G floats: G threads per vector.
+template <int G>
+__global__ void __launch_bounds__(128) qat_vectors_kernel(const float *__restrict__ in, float *__restrict__ out,
+                                                          int64_t n_vec, float c) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t vec = (int64_t)blockIdx.x * (128 / G) + threadIdx.x / G;
+    const int t = threadIdx.x % G;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (vec < n_vec) v = *reinterpret_cast<const float4 *>(in + vec * 4 * G + 4 * t);
+    indexer_qat_group<G>(v, c);                        // every lane takes part in the shuffles
+    if (vec < n_vec) *reinterpret_cast<float4 *>(out + vec * 4 * G + 4 * t) = v;
+}
+
 }  // namespace
 
 cudaError_t launch_indexer_prefill(const IndexerArgs &a, cudaStream_t s) {
@@ -760,6 +849,49 @@ cudaError_t launch_indexer_decode(const IndexerArgs &a, const DecodePos &p, cuda
         if (e != cudaSuccess) return e;
     }
     return launch_topk<TK_DECODE>(a, p, a.n_seq, vis_max, true, s);
+}
+
+cudaError_t launch_indexer_heads(const IndexerArgs &a, const float *w, int heads, const DecodePos *dp, cudaStream_t s) {
+    const bool decode = dp != nullptr;
+    const int n_q = decode ? a.n_seq : a.n_tok;
+    if (n_q <= 0) return cudaSuccess;
+    uint64_t vis_max = 0;
+    if (decode) {
+        for (int b = 0; b < a.n_seq; b++) vis_max = ((dp->pos[b] + 1) / 4 > vis_max) ? (dp->pos[b] + 1) / 4 : vis_max;
+    } else {
+        vis_max = (a.pos0 + (uint64_t)a.n_tok) / 4;
+    }
+    DecodePos none{};
+    const DecodePos &p = decode ? *dp : none;
+    if (vis_max > 0) {
+        const int QB = decode ? 1 : 4;
+        const dim3 grid((unsigned)((vis_max + 127) / 128), (unsigned)((n_q + QB - 1) / QB));
+        const size_t smem = (size_t)QB * heads * a.d * 4 + (size_t)QB * heads * 4;
+        cudaError_t e = cudaErrorInvalidValue;
+#define DS4C_HEADS(dd, qb)                                                                              \
+        if (a.d == dd && QB == qb) {                                                                   \
+            e = ensure_dyn_smem(score_heads_kernel<dd, qb>, smem);                                     \
+            if (e == cudaSuccess)                                                                      \
+                e = launch_pdl(score_heads_kernel<dd, qb>, grid, dim3(128), smem, s, a, w, heads, p, decode ? 1 : 0); \
+        }
+        DS4C_HEADS(64, 1)
+        DS4C_HEADS(64, 4)
+        DS4C_HEADS(128, 1)
+        DS4C_HEADS(128, 4)
+#undef DS4C_HEADS
+        if (e != cudaSuccess) return e;
+    }
+    return decode ? launch_topk<TK_DECODE>(a, p, n_q, vis_max, true, s)
+                  : launch_topk<TK_PREFILL>(a, p, n_q, vis_max, false, s);
+}
+
+cudaError_t launch_qat_vectors(const float *in, float *out, int64_t n_vec, int d, float c, cudaStream_t s) {
+    if (n_vec <= 0) return cudaSuccess;
+    const int G = d / 4;
+    const int64_t blocks = (n_vec * G + 127) / 128;
+    if (G == 16) return launch_pdl(qat_vectors_kernel<16>, dim3((unsigned)blocks), dim3(128), 0, s, in, out, n_vec, c);
+    if (G == 32) return launch_pdl(qat_vectors_kernel<32>, dim3((unsigned)blocks), dim3(128), 0, s, in, out, n_vec, c);
+    return cudaErrorInvalidValue;
 }
 
 unsigned int idx_read_clear_error() {

@@ -35,7 +35,8 @@ class DeviceLayer:
             d_model=shape.d_model, head_dim=D, n_rot=shape.n_rot, idx_head_dim=d, n_heads=shape.n_heads,
             ratio=r, swa=shape.swa, top_k=shape.top_k, comp_cap=self.comp_cap, idx_cap=self.idx_cap,
             dtype=abi.DS4C_F32 if shape.dtype == "f32" else abi.DS4C_BF16, rms_eps=shape.rms_eps,
-            attn_scale=shape.attn_scale, rope_base=shape.rope_base)
+            attn_scale=shape.attn_scale, rope_base=shape.rope_base, idx_heads=shape.idx_heads,
+            idx_qat=shape.idx_qat)
         f32 = dict(dtype=torch.float32, device=device)
         self.raw = torch.zeros(n_seq, shape.swa, D, **f32)
         self.attn_comp = self.attn_kv = self.attn_score = self.attn_pre = self.attn_split = None
@@ -49,15 +50,18 @@ class DeviceLayer:
             if abi.ds4c_attn_uses_tensor_cores(self.cfg):
                 # bf16 hi / lo mirror of the compressed rows, read by the tensor-core attention
                 self.attn_split = torch.zeros(n_seq, self.comp_cap, 2, D, dtype=torch.int16, device=device)
+        self.idx_pre = None
         if r == 4:
             self.idx_comp = torch.zeros(n_seq, self.idx_cap, d, **f32)
+            if with_prequant:
+                self.idx_pre = torch.zeros(n_seq, self.idx_cap, d, **f32)
             self.idx_kv = torch.zeros(n_seq, 8, 2 * d, **f32)
             self.idx_score = torch.zeros(n_seq, 8, 2 * d, **f32)
         self.state = abi.LayerState(
             raw=_ptr(self.raw),
             attn=abi.LaneState(_ptr(self.attn_comp), _ptr(self.attn_kv), _ptr(self.attn_score), _ptr(self.attn_pre),
                                _ptr(self.attn_split)),
-            idx=abi.LaneState(_ptr(self.idx_comp), _ptr(self.idx_kv), _ptr(self.idx_score), None, None))
+            idx=abi.LaneState(_ptr(self.idx_comp), _ptr(self.idx_kv), _ptr(self.idx_score), _ptr(self.idx_pre), None))
         self.ws_bytes = abi.ds4c_workspace_bytes(self.cfg, max_rows, n_seq if n_seq > 1 else 0)
         if self.ws_bytes == 0:
             raise abi.Ds4cError(abi.DS4C_ERR_SHAPE, "ds4c_workspace_bytes")
@@ -107,6 +111,12 @@ class DeviceLayer:
                                         _ptr(scores), score_stride, _ptr(self.ws), self.ws_bytes, _stream()),
                   "ds4c_indexer_topk")
 
+    def indexer_topk_heads(self, q_idx, w_idx, positions, n_seq, n_tok, topk, scores=None, score_stride=0):
+        pos = abi.u64_array(positions)
+        abi.check(abi.ds4c_indexer_topk_heads(self.cfg, self.state, _ptr(q_idx), _ptr(w_idx), pos, n_seq, n_tok,
+                                              _ptr(topk), _ptr(scores), score_stride, _ptr(self.ws), self.ws_bytes,
+                                              _stream()), "ds4c_indexer_topk_heads")
+
     def attention(self, q, raw_new, topk, positions, n_seq, n_tok, out, commit_ring=True):
         pos = abi.u64_array(positions)
         abi.check(abi.ds4c_sparse_swa_attn(self.cfg, self.state, _ptr(q), _ptr(raw_new), _ptr(topk), pos, n_seq,
@@ -138,4 +148,4 @@ class DeviceLayer:
             raw=off(self.raw),
             attn=abi.LaneState(off(self.attn_comp), off(self.attn_kv), off(self.attn_score), off(self.attn_pre),
                                off(self.attn_split)),
-            idx=abi.LaneState(off(self.idx_comp), off(self.idx_kv), off(self.idx_score), None, None))
+            idx=abi.LaneState(off(self.idx_comp), off(self.idx_kv), off(self.idx_score), off(self.idx_pre), None))

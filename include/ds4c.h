@@ -80,6 +80,9 @@ typedef struct {
     float rms_eps;          /* RMSNorm epsilon */
     float attn_scale;       /* logit scale, 1/sqrt(head_dim) in the shipped configs */
     float rope_base;        /* compressed-layer RoPE base; theta_i = base^(-2i/n_rot) */
+    uint32_t idx_heads;     /* ratio 4: indexer query heads of ds4c_indexer_topk_heads ([P2] §6: 64), 0 if unused */
+    uint32_t idx_qat;       /* ratio 4: 1 = the indexer rows (and the heads' queries) take the Hadamard + FP4
+                               round trip of [P2] §9; requires idx_head_dim 64 or 128.  0 = identity */
 } ds4c_layer_cfg;
 
 /* One compressor lane's weights ([P2] §4, §6: the attention lane and, on
@@ -188,6 +191,22 @@ DS4C_API ds4c_status ds4c_indexer_topk(const ds4c_layer_cfg *cfg, const ds4c_lay
                               const float *q_idx, const uint64_t *pos_h, uint32_t n_seq,
                               uint32_t n_tok, int32_t *topk, float *scores, size_t score_stride,
                               void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Multi-head indexer top-k of a ratio-4 layer with cfg->idx_heads = H_i >= 1
+ * heads ([P2] §6: 64 indexer heads of width 128 score the compressed rows; §9:
+ * the indexer queries take the same Hadamard + FP4 round trip as the rows when
+ * cfg->idx_qat is 1).  Query layout as ds4c_indexer_topk; q_idx: [n][H_i]
+ * [idx_head_dim] float, the heads' query vectors before the round trip; w_idx:
+ * [n][H_i] float, per-query head weights.  The score of row c for a query is
+ * s = 0; for j = 0 .. H_i-1: s = fmaf(w[j], max(dot_j, 0), s), dot_j the in-order
+ * fmaf chain of head j's (round-tripped) vector with the row (the pages give no
+ * combine; this is the library's reading), then the top_k largest as
+ * ds4c_indexer_topk.  Requires idx_head_dim 64 or 128.  Workspace as
+ * ds4c_workspace_bytes (it includes the round-tripped query vectors). */
+DS4C_API ds4c_status ds4c_indexer_topk_heads(const ds4c_layer_cfg *cfg, const ds4c_layer_state *state,
+                                             const float *q_idx, const float *w_idx, const uint64_t *pos_h,
+                                             uint32_t n_seq, uint32_t n_tok, int32_t *topk, float *scores,
+                                             size_t score_stride, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Sparse sliding-window attention ([P2] §7 indexed mixed attention): for each
  * query at position t and head h, one softmax over the raw rows of positions

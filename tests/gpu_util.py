@@ -51,7 +51,7 @@ def download(dl: DeviceLayer, b: int = 0) -> orc.State:
         st.idx.comp[:] = dl.idx_comp[b].cpu().numpy()
         st.idx.state_kv[:] = dl.idx_kv[b].cpu().numpy()
         st.idx.state_score[:] = dl.idx_score[b].cpu().numpy()
-        st.idx.prequant[:] = st.idx.comp
+        st.idx.prequant[:] = dl.idx_pre[b].cpu().numpy() if getattr(dl, "idx_pre", None) is not None else st.idx.comp
     return st
 
 
@@ -93,7 +93,22 @@ def check_compress(before: orc.State, after_gpu: orc.State, wa, wi, hidden: torc
     np.testing.assert_allclose(after_gpu.attn.state_kv, ref.attn.state_kv, rtol=RTOL, atol=ATOL, err_msg="attn state_kv")
     np.testing.assert_allclose(after_gpu.attn.state_score, ref.attn.state_score, rtol=RTOL, atol=ATOL,
                                err_msg="attn state_score")
-    if r == 4:
+    if r == 4 and L.idx_qat:
+        # indexer rows with the Hadamard + FP4 round trip: the GPU's own pre-round-trip row,
+        # re-quantised by the oracle, equals the GPU row bit for bit; the pre-round-trip rows
+        # agree within tolerance, so an end-to-end code flip can only be a rounding straddle
+        irows = slice(pos0 // 4, (pos0 + T) // 4)
+        gpi = after_gpu.idx.prequant[irows]
+        np.testing.assert_allclose(gpi, ref.idx.prequant[irows], rtol=RTOL, atol=ATOL, err_msg="idx pre-QAT rows")
+        np.testing.assert_array_equal(orc.indexer_qat(gpi), after_gpu.idx.comp[irows], err_msg="idx QAT arithmetic")
+        gi, oi = after_gpu.idx.comp[irows], ref.idx.comp[irows]
+        iflips = int(np.sum(gi != oi))
+        assert iflips <= max(2, gi.size // 200), f"FP4 flips {iflips}/{gi.size}"
+        if report is not None:
+            report["fp4_flips"] = report.get("fp4_flips", 0) + iflips
+        np.testing.assert_allclose(after_gpu.idx.state_kv, ref.idx.state_kv, rtol=RTOL, atol=ATOL)
+        np.testing.assert_allclose(after_gpu.idx.state_score, ref.idx.state_score, rtol=RTOL, atol=ATOL)
+    elif r == 4:
         irows = slice(pos0 // 4, (pos0 + T) // 4)
         np.testing.assert_allclose(after_gpu.idx.comp[irows], ref.idx.comp[irows], rtol=RTOL, atol=ATOL,
                                    err_msg="idx rows")

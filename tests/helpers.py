@@ -29,7 +29,8 @@ def orc_layer(shape: configs.LayerShape, comp_cap: int, idx_cap: int = 0) -> ora
                         idx_head_dim=shape.idx_head_dim, n_heads=shape.n_heads, ratio=shape.ratio,
                         swa=shape.swa, top_k=shape.top_k, comp_cap=comp_cap, idx_cap=idx_cap,
                         bf16=(shape.dtype == "bf16"), rms_eps=shape.rms_eps,
-                        attn_scale=shape.attn_scale, rope_base=shape.rope_base)
+                        attn_scale=shape.attn_scale, rope_base=shape.rope_base, idx_heads=shape.idx_heads,
+                        idx_qat=shape.idx_qat)
 
 
 def lane_np(w):
