@@ -28,7 +28,7 @@ EXPORTS = (
     "ds4c_sync_status", "ds4c_status_string", "ds4c_last_cuda_error", "ds4c_attn_uses_tensor_cores",
     "ds4c_indexer_topk_noalloc", "ds4c_checkpoint_scatter", "ds4c_payload_header", "ds4c_fma_probe",
     "ds4c_payload_bytes", "ds4c_payload_write", "ds4c_payload_read", "ds4c_compress_prefill_timed",
-    "ds4c_indexer_topk_heads",
+    "ds4c_indexer_topk_heads", "ds4c_test_set_wait_limit", "ds4c_test_wait_timeout",
 )
 PAYLOAD_U32_FIELDS = 13
 NOALLOC_SCORE_FLOATS = 2 * 1024 * 1024
@@ -105,6 +105,8 @@ def lib() -> C.CDLL:
         "ds4c_payload_read": (st, [C.POINTER(PayloadInfo), cfgp, lsp, U32, U32, P, SZ, P, SZ, P,
                                    C.POINTER(U32), P]),
         "ds4c_fma_probe": (st, [U32, U32, P, C.POINTER(C.c_double), P]),
+        "ds4c_test_set_wait_limit": (st, [U64]),
+        "ds4c_test_wait_timeout": (st, [U64, P]),
         "ds4c_sync_status": (st, [P]),
         "ds4c_status_string": (C.c_char_p, [C.c_int]),
         "ds4c_last_cuda_error": (C.c_char_p, []),
@@ -241,6 +243,14 @@ def ds4c_fma_probe(blocks, iters, out_ptr, stream):
     fl = C.c_double(0.0)
     s = lib().ds4c_fma_probe(blocks, iters, out_ptr, C.byref(fl), stream)
     return s, fl.value
+
+
+def ds4c_test_set_wait_limit(limit_ns):
+    return lib().ds4c_test_set_wait_limit(limit_ns)
+
+
+def ds4c_test_wait_timeout(limit_ns, stream):
+    return lib().ds4c_test_wait_timeout(limit_ns, stream)
 
 
 def ds4c_sync_status(stream):

@@ -682,6 +682,18 @@ ds4c_status ds4c_payload_header(const ds4c_payload_info *info, uint32_t out[DS4C
 
 const char *ds4c_last_cuda_error(void) { return cudaGetErrorName(t_last_cuda_error); }
 
+ds4c_status ds4c_test_set_wait_limit(uint64_t limit_ns) {
+    const unsigned long long ns = limit_ns ? limit_ns : kWaitNsDefault;
+    cudaError_t e = gemm_tc_set_wait_ns(ns);
+    if (e == cudaSuccess) e = attn_tc_set_wait_ns(ns);
+    if (e == cudaSuccess) e = idx_set_wait_ns(ns);
+    return cuda_status(e);
+}
+
+ds4c_status ds4c_test_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {
+    return cuda_status(launch_wait_selftest(limit_ns, stream));
+}
+
 ds4c_status ds4c_sync_status(cudaStream_t stream) {
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_status(e);

@@ -36,6 +36,21 @@ inline cudaError_t ensure_dyn_smem(F *func, size_t bytes) {
     return e;
 }
 
+// Bounded waits.  Every spin of the kernels gives up after a limit (4 s), raises
+// its translation unit's device error word and winds the CTA down; the limit
+// sits in a device variable of each unit, changed only by the test hook
+// ds4c_test_set_wait_limit.  Waits that drain copies or MMAs still in flight
+// after a give-up use kDrainNs whatever that limit is.
+constexpr unsigned long long kWaitNsDefault = 4000000000ull;
+constexpr unsigned long long kDrainNs = 4000000000ull;
+cudaError_t gemm_tc_set_wait_ns(unsigned long long ns);
+cudaError_t attn_tc_set_wait_ns(unsigned long long ns);
+cudaError_t idx_set_wait_ns(unsigned long long ns);
+// One CTA waits on an mbarrier that nothing arrives on, bounded by limit_ns, with
+// the indexer kernels' wait routine: it gives up, raises the indexer's error word
+// and returns (the self-test of the error path; no fault, no hang).
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t s);
+
 // FP32 FMA-rate probe (the ALU roofline's denominator): flops of one launch
 // of `blocks` 256-thread CTAs running `iters` rounds, and the launch itself.
 double fma_probe_flops(uint32_t blocks, uint32_t iters);

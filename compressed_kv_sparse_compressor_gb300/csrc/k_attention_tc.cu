@@ -51,6 +51,7 @@
 namespace ds4c {
 
 __device__ unsigned int g_attn_tc_err;
+__device__ unsigned long long g_attn_wait_ns = kWaitNsDefault;
 
 namespace {
 
@@ -61,7 +62,6 @@ constexpr int RING = 4;
 constexpr int THREADS = 192;
 constexpr int MAX_LIST = 512;
 constexpr float TAU = 8.0f;           // log2 units
-constexpr unsigned long long WAIT_NS = 4000000000ull;
 
 template <int H, int D>
 struct L {
@@ -83,7 +83,7 @@ struct L {
     static constexpr int OFF_MREF = OFF_TMAX + 4 * H;
     static constexpr int OFF_FLAG = OFF_MREF + 4 * H;
     static constexpr int OFF_BAR = OFF_FLAG + 64;
-    static constexpr int N_BAR = 2 * RING + 10;
+    static constexpr int N_BAR = 2 * RING + 11;
     // the dynamic shared memory starts 1024-byte aligned (checked at entry), as
     // the 128-byte swizzle atoms of Q, the ring and P need
     static constexpr int SMEM = OFF_BAR + 8 * N_BAR + 16;
@@ -99,7 +99,7 @@ struct L {
 
 // barrier indices
 enum { B_FULL = 0, B_EMPTY = RING, B_QREADY = 2 * RING, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1, B_PFULL, B_PVDONE,
-       B_OFREE, B_SOFT, B_QLOAD };
+       B_OFREE, B_SOFT, B_QLOAD, B_DRAIN };
 
 struct TcAttnParams {
     float *out;
@@ -150,11 +150,33 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
             if (*abort) return false;
             const uint64_t now = globaltimer();
             if (t0 == 0) t0 = now;
-            else if (now - t0 > WAIT_NS) {
+            else if (now - t0 > g_attn_wait_ns) {
                 *abort = 1;
                 atomicOr(&g_attn_tc_err, 1u);
                 return false;
             }
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag: drains copies or MMAs still in
+// flight after a give-up, before the CTA frees its TMEM and exits.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return;
+        if ((i & 255u) == 255u) {
+            const uint64_t now = globaltimer();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > kDrainNs) return;
         }
     }
 }
@@ -466,6 +488,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         mbar_init(bar(B_OFREE), 128);
         mbar_init(bar(B_SOFT), 128);
         mbar_init(bar(B_QLOAD), 1);
+        mbar_init(bar(B_DRAIN), 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -518,7 +541,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                 unit++;
                 int okw = 1;
                 if (lane == 0) okw = mbar_wait(bar(B_EMPTY + s_), ph ^ 1, abort) ? 1 : 0;
-                if (__shfl_sync(0xffffffffu, okw, 0) == 0) return false;
+                if (__shfl_sync(0xffffffffu, okw, 0) == 0) {
+                    unit--;                                  // nothing was issued for this unit
+                    return false;
+                }
                 const uint32_t dst = smem_u32(sm + Lay::OFF_X + s_ * PAIR);
                 const uint32_t fb = bar(B_FULL + s_);
                 if (tile == 0) {
@@ -593,6 +619,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             }
             ok = good;
         }
+        if (!ok) {
+            // after a give-up: this lane's row copies complete, and every unit issued to the ring
+            // (the last RING at most are still open) has landed before the CTA exits
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            __syncwarp();
+            if (lane == 0)
+                for (uint32_t u = unit > (uint32_t)RING ? unit - RING : 0; u < unit; u++)
+                    mbar_drain(bar(B_FULL + u % RING), (u / RING) & 1);
+        }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         constexpr uint32_t ID_QK = idesc(128, H, 0, 0);
@@ -601,7 +636,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         const uint32_t qs = smem_u32(sm + Lay::OFF_Q);
         const uint32_t phi = smem_u32(sm + Lay::OFF_PHI), plo = smem_u32(sm + Lay::OFF_PLO);
         // fp32 Q of query n into the Q chunks (lane 0; the Q buffer is free)
+        uint32_t nq = 0;                                  // Q loads issued
         auto issue_q = [&](int n) {
+            nq++;
             mbar_expect_tx(bar(B_QLOAD), Lay::DC * Lay::QCH);
             for (int c = 0; c < Lay::DC; c++) tma_box(qs + c * Lay::QCH, &qMap, 64 * c, n * H, bar(B_QLOAD));
         };
@@ -699,8 +736,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             g += itm.te - itm.tb;
             tok++;
         }
-        // drain: every MMA issued so far has completed before the TMEM is freed
-        if (lane == 0 && g > 0) mbar_wait(bar(B_PVDONE), (g - 1) & 1, abort);
+        // drain: every MMA issued so far completes before the TMEM is freed (one more commit
+        // tracks all of them; bounded, given up or not)
+        if (lane == 0) {
+            mma_commit(bar(B_DRAIN));
+            mbar_drain(bar(B_DRAIN), 0);
+            if (nq > 0) mbar_drain(bar(B_QLOAD), (nq - 1) & 1);   // the last Q load has landed
+        }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax / epilogue
@@ -1134,6 +1176,8 @@ cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *dp, cudaSt
 #undef DS4C_HD
     return cudaErrorNotSupported;
 }
+
+cudaError_t attn_tc_set_wait_ns(unsigned long long ns) { return cudaMemcpyToSymbol(g_attn_wait_ns, &ns, sizeof ns); }
 
 unsigned int attn_tc_read_clear_error() {
     unsigned int v = 0, z = 0;

@@ -25,12 +25,12 @@
 namespace ds4c {
 
 __device__ unsigned int g_gemm_tc_err;
+__device__ unsigned long long g_gemm_wait_ns = kWaitNsDefault;
 
 namespace {
 
 constexpr int BM = 128, BK = 64;
 constexpr int THREADS = 192;
-constexpr unsigned long long WAIT_NS = 4000000000ull;
 
 // Tile width BN: 256 for prefill chunks; 32 for decode-sized M, where the
 // weights are the traffic and more, narrower tiles spread them over the SMs.
@@ -47,7 +47,9 @@ struct GT {
     static constexpr int STAGES = AR < BM ? (BN >= 128 ? 8 : 20) : (BN >= 128 ? 4 : 8);
     static constexpr int PAD = (BM - AR) * BK * 2;
     static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + PAD + 1024 + 256;
+    // barriers (2 * STAGES + 5) and the TMEM slot / abort flag after the stages, plus the
+    // realignment of the base to 1024 bytes
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + PAD + 1024 + 8 * (2 * STAGES + 5) + 16;
     // instruction descriptor: kind::f16, A = B = bf16, D = f32, both K-major, M = 128, N = BN
     static constexpr uint32_t IDESC =
         (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
@@ -106,11 +108,33 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
             if (*abort) return false;
             const uint64_t now = globaltimer();
             if (t0 == 0) t0 = now;
-            else if (now - t0 > WAIT_NS) {
+            else if (now - t0 > g_gemm_wait_ns) {
                 *abort = 1;
                 atomicOr(&g_gemm_tc_err, 1u);
                 return false;
             }
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag: drains copies or MMAs still in
+// flight after a give-up, before the CTA frees its TMEM and exits.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return;
+        if ((i & 255u) == 255u) {
+            const uint64_t now = globaltimer();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > kDrainNs) return;
         }
     }
 }
@@ -184,7 +208,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES + G::PAD);
     uint64_t *full = bars, *empty = bars + STAGES, *acc_full = bars + 2 * STAGES, *acc_empty = bars + 2 * STAGES + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 4);
+    uint64_t *drain = bars + 2 * STAGES + 4;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -201,6 +226,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
             mbar_init(smem_u32(&acc_full[a]), 1);
             mbar_init(smem_u32(&acc_empty[a]), 128);
         }
+        mbar_init(smem_u32(drain), 1);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapA)) : "memory");
@@ -240,6 +266,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
                     tma_load_2d(smem_u32(sb), mb, kb * BK, nt * BN, bar);
                 }
             }
+            // after a give-up: the loads still in flight (the last STAGES issued) land before the CTA exits
+            if (!ok)
+                for (uint32_t u = it > (uint32_t)STAGES ? it - STAGES : 0; u < it; u++)
+                    mbar_drain(smem_u32(&full[u % STAGES]), (u / STAGES) & 1);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -270,11 +300,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
                 }
                 if (ok) mma_commit(smem_u32(&acc_full[acc]));
             }
-            // drain: wait (bounded) for every issued MMA before the TMEM is freed
-            if (it > 0) {
-                const uint32_t last = it - 1;
-                mbar_wait(smem_u32(&empty[last % STAGES]), (last / STAGES) & 1, abort);
-            }
+            // drain: every MMA issued so far completes (bounded wait, given up or not) before the
+            // TMEM is freed: one more commit tracks all of them
+            mma_commit(smem_u32(drain));
+            mbar_drain(smem_u32(drain), 0);
         }
     } else {
         // epilogue: warps 2..5 -> TMEM lane quarter (warp % 4)
@@ -450,6 +479,8 @@ cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
     if (a.M <= 32) return launch_bn<128, 32>(a, s);
     return a.M <= 256 ? launch_bn<32, BM>(a, s) : launch_bn<256, BM>(a, s);
 }
+
+cudaError_t gemm_tc_set_wait_ns(unsigned long long ns) { return cudaMemcpyToSymbol(g_gemm_wait_ns, &ns, sizeof ns); }
 
 unsigned int gemm_tc_read_clear_error() {
     unsigned int v = 0, z = 0;

@@ -20,6 +20,7 @@
 namespace ds4c {
 
 __device__ unsigned int g_idx_err;
+__device__ unsigned long long g_idx_wait_ns = kWaitNsDefault;
 
 namespace {
 
@@ -191,9 +192,40 @@ __global__ void __launch_bounds__(128) score_decode_kernel(IndexerArgs a, Decode
 // then the same in-order fma chain.  Several blocks share an SM, so the HBM
 // stream has many boxes in flight.
 // ---------------------------------------------------------------------------
-constexpr unsigned long long IDX_WAIT_NS = 4000000000ull;
-
 __device__ __forceinline__ uint32_t idx_smem_u32(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+// Bounded wait for the completion of phase `parity` of an mbarrier (the time is
+// checked every 256 polls); false when limit_ns ran out first.
+__device__ __forceinline__ bool idx_bounded_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((it & 255u) == 255u) {
+            uint64_t now;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > limit_ns) return false;
+        }
+    }
+}
+
+// Self-test of the error path: one thread waits on a barrier that nothing
+// arrives on (bounded), raises the error word when the limit runs out.
+__global__ void wait_selftest_kernel(unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    const uint32_t b = idx_smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (!idx_bounded_wait(b, 0, limit_ns)) atomicOr(&g_idx_err, 2u);
+    }
+}
 
 template <int DD>
 __global__ void __launch_bounds__(128) score_decode_tma_kernel(const __grid_constant__ CUtensorMap rowsMap, IndexerArgs a,
@@ -229,25 +261,12 @@ __global__ void __launch_bounds__(128) score_decode_tma_kernel(const __grid_cons
     }
     for (int i = threadIdx.x; i < DD; i += 128) qs[i] = a.q[(size_t)b * DD + i];
     __syncthreads();
-    // bounded wait for the boxes; a wait that gives up raises the error word
-    uint64_t t0 = 0;
-    for (uint32_t it = 0;; ++it) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done)
-            : "r"(bar_a)
-            : "memory");
-        if (done) break;
-        if ((it & 255u) == 255u) {
-            uint64_t now;
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
-            if (t0 == 0) t0 = now;
-            else if (now - t0 > IDX_WAIT_NS) {
-                atomicOr(&g_idx_err, 1u);
-                return;
-            }
-        }
+    // bounded wait for the boxes; a wait that gives up raises the error word and, before
+    // the CTA returns, waits (bounded again) for the boxes still landing in its shared memory
+    if (!idx_bounded_wait(bar_a, 0, g_idx_wait_ns)) {
+        atomicOr(&g_idx_err, 1u);                       // every thread that gave up: its score is missing
+        idx_bounded_wait(bar_a, 0, kDrainNs);
+        return;
     }
     const int t = threadIdx.x;
     const int c = c0 + t;
@@ -892,6 +911,13 @@ cudaError_t launch_qat_vectors(const float *in, float *out, int64_t n_vec, int d
     if (G == 16) return launch_pdl(qat_vectors_kernel<16>, dim3((unsigned)blocks), dim3(128), 0, s, in, out, n_vec, c);
     if (G == 32) return launch_pdl(qat_vectors_kernel<32>, dim3((unsigned)blocks), dim3(128), 0, s, in, out, n_vec, c);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t idx_set_wait_ns(unsigned long long ns) { return cudaMemcpyToSymbol(g_idx_wait_ns, &ns, sizeof ns); }
+
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t s) {
+    wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns);
+    return cudaGetLastError();
 }
 
 unsigned int idx_read_clear_error() {

@@ -355,6 +355,19 @@ DS4C_API ds4c_status ds4c_payload_read(const ds4c_payload_info *expect, const ds
 DS4C_API ds4c_status ds4c_fma_probe(uint32_t blocks, uint32_t iters, float *out, double *flops_h,
                                     cudaStream_t stream);
 
+/* Test hooks of the failure path (not steps of the method).  Every spin-wait in
+ * the kernels (an mbarrier wait for copies or MMAs) is bounded: when its limit
+ * runs out the kernel raises a sticky device error word, waits (bounded again)
+ * for what it still has in flight, frees its tensor memory and returns, so the
+ * context stays usable and ds4c_sync_status reports DS4C_ERR_DEVICE.
+ * ds4c_test_set_wait_limit sets that limit on the current device (0 = the
+ * default of 4 s); ds4c_test_wait_timeout launches one CTA that waits, bounded
+ * by limit_ns, on an mbarrier nothing arrives on, through the same wait routine
+ * as the indexer kernels, so its limit runs out and it raises the indexer's
+ * error word (no fault, no hang). */
+DS4C_API ds4c_status ds4c_test_set_wait_limit(uint64_t limit_ns);
+DS4C_API ds4c_status ds4c_test_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
+
 /* Synchronises `stream`, then reports (and clears) the device error word:
  * DS4C_ERR_DEVICE if a kernel raised it, DS4C_ERR_CUDA if the stream failed. */
 DS4C_API ds4c_status ds4c_sync_status(cudaStream_t stream);
