@@ -12,8 +12,9 @@ import torch
 
 import oracle as orc
 from compressed_kv_sparse_compressor_gb300 import configs
-from gpu_util import (check_attention_sampled, check_compress, check_indexer_sampled, check_split_mirror,
-                      device_layer, download, require_gpu)
+from gpu_util import (ATOL, RTOL, check_attention_sampled, check_compress, check_indexer_sampled, check_split_mirror,
+                      device_layer, download, require_gpu, unexplained_fp8_flips)
+from helpers import lane_np, np_in, orc_layer
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -73,6 +74,31 @@ def _gather_check(dl, pos):
     np.testing.assert_array_equal(dst.cpu().numpy(), orc.checkpoint_gather(download(dl), pos))
 
 
+def _check_windows_across_the_run(dl, wa, wi, shape, seed, windows):
+    """Compressed rows of windows sampled over the whole prefill, both lanes, against the
+    oracle: row c of a ratio-4 lane depends only on tokens 4(c-1) .. 4c+3, so the oracle
+    compresses those eight tokens from a fresh state and takes its window c."""
+    st = download(dl)
+    n_nope = shape.head_dim - shape.n_rot
+    attn_w, idx_w = lane_np(wa), lane_np(wi)
+    gp, gc, op, oc = [], [], [], []
+    for c in windows:
+        p0 = max(0, 4 * (c - 1))
+        h = configs.hidden(shape, seed, 4 * c + 4 - p0, offset_tok=p0)
+        ref = orc.State(orc_layer(shape, c + 1, c + 1))
+        orc.state_init(ref)
+        orc.compress(ref, attn_w, idx_w, np_in(h), p0)
+        np.testing.assert_allclose(st.attn.prequant[c], ref.attn.prequant[c], rtol=RTOL, atol=ATOL,
+                                   err_msg=f"attn pre-FP8 row {c}")
+        np.testing.assert_array_equal(orc.fp8_roundtrip(st.attn.prequant[c:c + 1], n_nope)[0], st.attn.comp[c],
+                                      err_msg=f"attn FP8 arithmetic row {c}")
+        np.testing.assert_allclose(st.attn.comp[c, n_nope:], ref.attn.comp[c, n_nope:], rtol=RTOL, atol=ATOL)
+        np.testing.assert_allclose(st.idx.comp[c], ref.idx.comp[c], rtol=RTOL, atol=ATOL, err_msg=f"idx row {c}")
+        gp.append(st.attn.prequant[c]); gc.append(st.attn.comp[c]); op.append(ref.attn.prequant[c])
+        oc.append(ref.attn.comp[c])
+    assert unexplained_fp8_flips(np.array(gp), np.array(gc), np.array(op), np.array(oc), n_nope) == 0
+
+
 def test_c5_full():
     """Long-context ratio-4 layer: 131072 tokens in 32 chunks, then the gather."""
     w = configs.C5
@@ -88,6 +114,15 @@ def test_c5_full():
     sample = sorted(set([0, 1, 2, 3, C - 1] + rng.integers(0, C, 11).tolist()))
     _checked_chunk(dl, wa, wi, shape, w.seed, T - C, C, sample)
     _gather_check(dl, T)
+    # 64 windows over all 32 chunks: the first, chunk edges (the last window of a chunk and the
+    # first of the next), the last, and random ones
+    n_win = T // 4
+    edges = [c for k in (1, 7, 15, 16, 31) for c in (k * (C // 4) - 1, k * (C // 4))]
+    windows = set([0, 1, n_win - 1] + edges)
+    while len(windows) < 64:
+        windows.add(int(rng.integers(0, n_win)))
+    windows = sorted(windows)
+    _check_windows_across_the_run(dl, wa, wi, shape, w.seed, windows)
 
 
 def test_c4_decode_full():
