@@ -30,9 +30,9 @@ import torch  # noqa: E402
 from compressed_kv_sparse_compressor_gb300 import configs  # noqa: E402
 
 METRIC = "prefill tokens/s per layer"
-# dram__bytes_read.sum + dram__bytes_write.sum of one attention launch (4096 queries), from the ncu capture
-# in profiles/kernels_prefill_8192tok_chunk2_full.md; set to None when the kernel changes until re-captured
-ATTN_TRAFFIC = 556861952 + 482737664   # dram__bytes_read.sum + dram__bytes_write.sum, one launch
+# dram__bytes_read.sum + dram__bytes_write.sum of one attention launch (4096 queries), from an ncu capture
+# under profiles/; None when the kernel has changed since the counters were taken
+ATTN_TRAFFIC = 557535744 + 482841344   # profiles/attn_tc_kernel_prefill_8192tok_chunk2.md
 ATTN_TRAFFIC_SRC = "ncu, one 4096-query launch of the 8192-token case (same units per launch as C5)"
 UNIT = "tokens/s"
 
@@ -415,7 +415,7 @@ def run_e2e(pf, args, device):
     dev_in, dev_out = pf.inputs(), pf.outputs()
     s_up, s_comp, s_down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     dl = pf.dl
-    steps = max(1, min(args.steps, 3))
+    steps = max(3, min(args.steps, 6))
 
     def one_step():
         with torch.cuda.stream(s_comp):
@@ -461,9 +461,24 @@ def run_e2e(pf, args, device):
     dl.sync()
     bi = sum(t.numel() * t.element_size() for t in host_in)
     bo = sum(t.numel() * t.element_size() for t in host_out)
+    # the host link alone: the same bytes copied one way at a time, pinned host memory, one stream
+    link = {}
+    for name, pairs in (("h2d", list(zip(dev_in, host_in))), ("d2h", list(zip(host_out, dev_out)))):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for dst, src in pairs:
+            dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        link[name + "_gbs"] = round((bi if name == "h2d" else bo) / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
     return {"value": round(pf.T / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "ms_per_step": round(ms, 3), "ms_each_step": [round(x, 1) for x in each], "steps": steps,
-            "pipeline": "per chunk: upload, compute and download on three streams"}
+            "median_step_ms": round(statistics.median(each), 3),
+            "host_link": link,
+            "host_link_ms": {"h2d": round(bi / (link["h2d_gbs"] * 1e9) * 1e3, 1),
+                             "d2h": round(bo / (link["d2h_gbs"] * 1e9) * 1e3, 1)},
+            "pipeline": "per chunk: upload, compute and download on three streams; host_link: the step's bytes "
+                        "copied one direction at a time on one stream, measured after the timed steps"}
 
 
 def run_decode(device, P, profile=False):
