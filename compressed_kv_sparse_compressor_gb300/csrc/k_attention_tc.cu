@@ -134,19 +134,21 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Each poll may suspend the thread for up to 1 us (woken when the phase completes), so a waiting
+// warp does not keep issuing beside the MMA warp; the time is checked every 16 polls.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
     uint64_t t0 = 0;
     for (uint32_t i = 0;; ++i) {
         uint32_t ok;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}"
             : "=r"(ok)
-            : "r"(bar), "r"(parity)
+            : "r"(bar), "r"(parity), "r"(1000u)
             : "memory");
         if (ok) return true;
-        if ((i & 255u) == 255u) {
+        if ((i & 15u) == 15u) {
             if (*abort) return false;
             const uint64_t now = globaltimer();
             if (t0 == 0) t0 = now;
