@@ -37,9 +37,16 @@
 // reference (and rescales O and L in tensor memory) when a logit exceeds it by
 // more than 2^8, so p <= 256 and the final O/L is exact for any reference.
 //
-// Warp roles (192 threads, persistent over query tokens):
-//   warp 0  row lists and TMA producer      warp 1  MMA issuer, TMEM owner
-//   warps 2-5  Q split, softmax, P, epilogue (thread = TMEM lane)
+// Warp roles (384 threads in three warpgroups, persistent over query tokens):
+//   warp 0  row lists and producer         warp 1  MMA issuer, TMEM owner   (warps 2-3 idle)
+//   warps 4-7   softmax and P (thread = TMEM lane = tile row)
+//   warps 8-11  Q loader and epilogue (thread = TMEM lane = d within a block): the next
+//               query's Q is loaded and split as soon as the current query's last S has
+//               been computed, and the output is read out of tensor memory and stored
+//               while the softmax and the MMAs carry on with the next query; only the
+//               first O product of the next query waits, block by block, for the read.
+// The warpgroups resize their register files at entry (setmaxnreg) so that the softmax
+// holds its 64 logits and a block of O without spilling.
 // Every mbarrier wait is bounded; a wait that gives up raises the device error
 // word and the CTA winds down.
 #include <cuda.h>
@@ -59,7 +66,14 @@ constexpr int ROWS = 128;
 constexpr int SLOT = 8192;            // [64 rows][64 d] bf16
 constexpr int PAIR = 2 * SLOT;
 constexpr int RING = 4;
-constexpr int THREADS = 192;
+// three warpgroups: {producer, MMA, two idle warps}, the softmax, the Q loader / epilogue
+constexpr int THREADS = 384;
+// registers per thread after the reallocation at entry (setmaxnreg): the first warpgroup gives
+// up registers, the softmax warpgroup takes them, the third keeps its launch allocation.  The
+// launch allocation must be at least (REG_LOW + REG_SOFT) / 2 for the two to fit (host-checked).
+constexpr int REG_LOW = 128;
+constexpr int REG_SOFT = 240;
+constexpr int REG_AUX = 136;
 constexpr int MAX_LIST = 512;
 constexpr float TAU = 8.0f;           // log2 units
 
@@ -82,8 +96,10 @@ struct L {
     static constexpr int OFF_TMAX = OFF_LIST + 4 * MAX_LIST;
     static constexpr int OFF_MREF = OFF_TMAX + 4 * H;
     static constexpr int OFF_FLAG = OFF_MREF + 4 * H;
-    static constexpr int OFF_BAR = OFF_FLAG + 64;
-    static constexpr int N_BAR = 2 * RING + 11;
+    // per head: the softmax denominator of the item the epilogue writes
+    static constexpr int OFF_LFIN = OFF_FLAG + 32;
+    static constexpr int OFF_BAR = OFF_LFIN + 4 * H;
+    static constexpr int N_BAR = 2 * RING + 17;
     // the dynamic shared memory starts 1024-byte aligned (checked at entry), as
     // the 128-byte swizzle atoms of Q, the ring and P need
     static constexpr int SMEM = OFF_BAR + 8 * N_BAR + 16;
@@ -93,13 +109,12 @@ struct L {
     static constexpr int T_COLS = 512;
     static_assert(T_O + DB * H <= T_COLS, "tensor memory");
     static_assert(SMEM <= 232448, "shared memory");
-    static_assert(PB == 64 * H * 4, "an output staging box [H][64] fp32 fills P hi (or lo)");
-    static_assert(PB >= 4 * H * 4, "the four warps' denominator partials fit P hi");
+    static_assert(DB <= 4, "one output-free barrier per d-block");
 };
 
 // barrier indices
 enum { B_FULL = 0, B_EMPTY = RING, B_QREADY = 2 * RING, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1, B_PFULL, B_PVDONE,
-       B_OFREE, B_SOFT, B_QLOAD, B_DRAIN };
+       B_OFREE0, B_OFREE1, B_OFREE2, B_OFREE3, B_SOFT, B_QLOAD, B_DRAIN, B_QFREE, B_ABAR, B_LREADY };
 
 struct TcAttnParams {
     float *out;
@@ -190,17 +205,6 @@ __device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap *map, in
         : "memory");
 }
 
-// shared -> global tensor store of one box, tracked by the issuing thread's bulk groups
-__device__ __forceinline__ void tma_store_box(const CUtensorMap *map, int x, int y, uint32_t src) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y), "r"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// the shared-memory sources of this thread's committed stores have been read
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Shared-memory matrix descriptor (tcgen05): start, leading / stride byte
 // offsets, version 1, layout (0 = no swizzle, 2 = 128-byte swizzle).
@@ -454,8 +458,7 @@ __device__ __forceinline__ int next_item(const TcAttnParams &p, int it, int n_it
 template <int H, int D>
 __global__ void __launch_bounds__(THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant__ CUtensorMap rawLo,
-               const __grid_constant__ CUtensorMap qMap, const __grid_constant__ CUtensorMap oMap,
-               const TcAttnParams p) {
+               const __grid_constant__ CUtensorMap qMap, const TcAttnParams p) {
     using Lay = L<H, D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if ((smem_u32(smem_raw) & 1023u) != 0) {            // the layout has no room to realign
@@ -472,6 +475,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
     float *alpha_s = reinterpret_cast<float *>(sm + Lay::OFF_TMAX);
     float *mref_s = reinterpret_cast<float *>(sm + Lay::OFF_MREF);
     volatile int *flags = reinterpret_cast<volatile int *>(sm + Lay::OFF_FLAG);
+    float *lfin = reinterpret_cast<float *>(sm + Lay::OFF_LFIN);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -487,10 +491,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         mbar_init(bar(B_SFREE1), 128);
         mbar_init(bar(B_PFULL), 128);
         mbar_init(bar(B_PVDONE), 1);
-        mbar_init(bar(B_OFREE), 128);
+        for (int j = 0; j < 4; j++) mbar_init(bar(B_OFREE0 + j), 128);
         mbar_init(bar(B_SOFT), 128);
         mbar_init(bar(B_QLOAD), 1);
         mbar_init(bar(B_DRAIN), 1);
+        mbar_init(bar(B_QFREE), 1);
+        mbar_init(bar(B_ABAR), 128);
+        mbar_init(bar(B_LREADY), 128);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -508,6 +515,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
     pdl_wait();
     pdl_launch_dependents();
 
+    // Each warpgroup first resizes its register allocation (setmaxnreg, one instruction for its
+    // four warps, which the code of the role then follows); the host checked that the three
+    // shares fit the launch allocation.
+    if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REG_LOW));
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         uint32_t unit = 0;
@@ -637,13 +649,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         constexpr uint32_t ID_PV = idesc(128, H, 1, 1);
         const uint32_t qs = smem_u32(sm + Lay::OFF_Q);
         const uint32_t phi = smem_u32(sm + Lay::OFF_PHI), plo = smem_u32(sm + Lay::OFF_PLO);
-        // fp32 Q of query n into the Q chunks (lane 0; the Q buffer is free)
-        uint32_t nq = 0;                                  // Q loads issued
-        auto issue_q = [&](int n) {
-            nq++;
-            mbar_expect_tx(bar(B_QLOAD), Lay::DC * Lay::QCH);
-            for (int c = 0; c < Lay::DC; c++) tma_box(qs + c * Lay::QCH, &qMap, 64 * c, n * H, bar(B_QLOAD));
-        };
         uint32_t unit = 0, g = 0, tok = 0;
         bool ok = true;
         // unit u of the ring: wait until loaded / hand back once its MMAs finish
@@ -652,7 +657,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             return mbar_wait(bar(B_FULL + u % RING), (u / RING) & 1, abort);
         };
         auto free_unit = [&](uint32_t u) { mma_commit(bar(B_EMPTY + u % RING)); };
-        auto do_qk = [&](uint32_t gt, int tile) -> bool {
+        // S of global tile gt; `last`: the item's last tile, after which Q is no longer read
+        auto do_qk = [&](uint32_t gt, int tile, bool last) -> bool {
             const int sb = gt & 1;
             if (gt >= 2 && !mbar_wait(bar(B_SFREE0 + sb), ((gt >> 1) - 1) & 1, abort)) return false;
             fence_after();
@@ -675,10 +681,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                 if (has_lo) free_unit(unit++);
             }
             mma_commit(bar(B_SFULL0 + sb));
+            if (last) mma_commit(bar(B_QFREE));        // the Q buffer may take the next query
             return true;
         };
+        // O of tile i; `first`: the item's first tile (overwrites the accumulator), which
+        // waits per d-block until the epilogue has read the previous item's block
         auto do_pv = [&](int i, bool first) -> bool {
             for (int j = 0; j < Lay::DB; j++) {
+                if (first && tok > 0) {
+                    if (!mbar_wait(bar(B_OFREE0 + j), (tok - 1) & 1, abort)) return false;
+                    fence_after();
+                }
                 const uint32_t d_o = tmem + Lay::T_O + j * H;
                 const bool has_lo = i == 0 || j >= p.nope_blocks;
                 for (int hh = 0; hh < 2; hh++) {
@@ -706,30 +719,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             return true;
         };
         const int n_items = p.n_q * p.parts;
-        {
-            const int first = next_item(p, blockIdx.x, n_items);
-            if (lane == 0 && first < n_items) issue_q(first / p.parts);
-        }
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const Tok k = token_geom(p, it / p.parts);
             const int nc = comp_rows(p, k, nullptr);          // whole warp
             const Item itm = item_tiles(p, it, 1 + (nc + ROWS - 1) / ROWS);
             if (itm.tb >= itm.te) continue;
-            const int nx = next_item(p, it + gridDim.x, n_items);
             int good = 1;
             if (lane == 0) {
                 good = mbar_wait(bar(B_QREADY), tok & 1, abort) ? 1 : 0;
                 if (good) {
                     fence_after();
-                    good = do_qk(g, itm.tb) ? 1 : 0;
+                    good = do_qk(g, itm.tb, itm.tb == itm.te - 1) ? 1 : 0;
                 }
                 for (int i = itm.tb; i < itm.te && good; i++) {
                     const uint32_t gi = g + (i - itm.tb);
-                    if (i + 1 < itm.te && !do_qk(gi + 1, i + 1)) { good = 0; break; }
+                    if (i + 1 < itm.te && !do_qk(gi + 1, i + 1, i + 1 == itm.te - 1)) { good = 0; break; }
                     if (!mbar_wait(bar(B_PFULL), gi & 1, abort)) { good = 0; break; }
-                    // every S of this item has been read, so its Q MMAs are complete: load the next Q
-                    if (i == itm.te - 1 && nx < n_items) issue_q(nx / p.parts);
-                    if (i == itm.tb && tok > 0 && !mbar_wait(bar(B_OFREE), (tok - 1) & 1, abort)) { good = 0; break; }
                     fence_after();
                     if (!do_pv(i, i == itm.tb)) { good = 0; break; }
                 }
@@ -743,18 +748,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         if (lane == 0) {
             mma_commit(bar(B_DRAIN));
             mbar_drain(bar(B_DRAIN), 0);
-            if (nq > 0) mbar_drain(bar(B_QLOAD), (nq - 1) & 1);   // the last Q load has landed
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------------------ softmax / epilogue
+    }
+    } else if (warp < 8) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REG_SOFT));
+        // ------------------------------------------------------------ softmax
         const int q4 = warp & 3;                 // TMEM lane quarter
-        const int r = q4 * 32 + lane;            // tile row / d within a block
+        const int r = q4 * 32 + lane;            // tile row
         const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
         uint8_t *phi_p = sm + Lay::OFF_PHI;
         uint8_t *plo_p = sm + Lay::OFF_PLO;
-        const int tid = threadIdx.x - 64;        // 0..127
-        uint32_t g = 0, sphase = 0, qph = 0;
+        const int tid = threadIdx.x - 128;       // 0..127
+        uint32_t g = 0, sphase = 0, tok = 0;
         bool ok = true;
         // barrier of the 128 softmax threads on an mbarrier, so that its wait is bounded
         auto soft_bar = [&]() -> bool {
@@ -763,39 +769,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             sphase ^= 1;
             return r_;
         };
-        // Q split: once the fp32 boxes have landed, each 64-d chunk [H][64] fp32
-        // is rewritten in place as its bf16 hi (K-major, 128-byte swizzle) and lo
-        // halves, one chunk per round (all reads of a round before its writes).
-        auto split_q = [&]() -> bool {
-            if (!mbar_wait(bar(B_QLOAD), qph, abort)) return false;
-            qph ^= 1;
-            constexpr int PER = H * 64 / 4 / 128;          // float4 per thread per chunk
-            for (int c = 0; c < Lay::DC; c++) {
-                uint8_t *qc = sm + Lay::OFF_Q + c * Lay::QCH;
-                float4 v[PER];
-#pragma unroll
-                for (int j = 0; j < PER; j++) v[j] = *reinterpret_cast<const float4 *>(qc + (j * 128 + tid) * 16);
-                if (!soft_bar()) return false;
-#pragma unroll
-                for (int j = 0; j < PER; j++) {
-                    const int f = j * 128 + tid;
-                    const int h = f / 16, d = (f % 16) * 4;
-                    const int off = h * 128 + (((d / 8) ^ (h & 7)) * 16) + (d % 8) * 2;
-                    float h0, l0, h1, l1, h2, l2, h3, l3;
-                    split_bf16(v[j].x, h0, l0);
-                    split_bf16(v[j].y, h1, l1);
-                    split_bf16(v[j].z, h2, l2);
-                    split_bf16(v[j].w, h3, l3);
-                    *reinterpret_cast<uint2 *>(qc + off) = make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3));
-                    *reinterpret_cast<uint2 *>(qc + off + Lay::QCH / 2) = make_uint2(pack_bf16x2(l0, l1), pack_bf16x2(l2, l3));
-                }
-            }
-            fence_proxy_async();
-            mbar_arrive(bar(B_QREADY));
-            return true;
-        };
         const int n_items = p.n_q * p.parts;
-        if (next_item(p, blockIdx.x, n_items) < n_items && !split_q()) ok = false;
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const int n = it / p.parts;
             const Tok k = token_geom(p, n);
@@ -875,7 +849,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                         fence_before();
                     }
                 }
-                if (i > itm.tb && !waited) {
+                // the P buffers are free once the previous tile's O (of this item or the
+                // previous one) has been computed
+                if (g > 0 && !waited) {
                     if (!mbar_wait(bar(B_PVDONE), (g - 1) & 1, abort)) { ok = false; break; }
                 }
                 // P^T row r (MN-major, 128-byte swizzle), hi and lo
@@ -901,64 +877,124 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                     lacc1 += l1;
                 }
                 if (i == itm.te - 1) {
-                    // the last S of this item has been read: split the next item's Q
-                    const int nx = next_item(p, it + gridDim.x, n_items);
-                    if (nx < n_items && !split_q()) { ok = false; break; }
-                    if (!mbar_wait(bar(B_PVDONE), g & 1, abort)) { ok = false; break; }
-                    fence_after();
-                    // the denominators: the four warps' shares meet in P hi (free until the
-                    // output staging below), then L[h] goes to the alpha words
-                    float *lpart = reinterpret_cast<float *>(phi_p);
-                    lpart[q4 * H + 2 * lane] = lacc0;
-                    lpart[q4 * H + 2 * lane + 1] = lacc1;
+                    // L[h] = (warp 0 + warp 1) + (warp 2 + warp 3) into the denominator words,
+                    // warps 2 and 3 meeting in the tile-maximum words (once every warp is done
+                    // with this tile's rescale factors there).  The denominator words still hold
+                    // the previous item's L until its epilogue has read them (which precedes its
+                    // first output-free arrival).
+                    if (tok > 0 && !mbar_wait(bar(B_OFREE0), (tok - 1) & 1, abort)) { ok = false; break; }
                     if (!soft_bar()) { ok = false; break; }
-                    if (tid < H) alpha_s[tid] = lpart[tid] + lpart[H + tid] + lpart[2 * H + tid] + lpart[3 * H + tid];
+                    float *lb = reinterpret_cast<float *>(tmax);
+                    if (q4 == 0) { lfin[2 * lane] = lacc0; lfin[2 * lane + 1] = lacc1; }
+                    if (q4 == 2) { lb[2 * lane] = lacc0; lb[2 * lane + 1] = lacc1; }
                     if (!soft_bar()) { ok = false; break; }
-                    float l[H], v[H];
-#pragma unroll
-                    for (int h = 0; h < H; h++) l[h] = alpha_s[h];
-                    // whole query: out[n][h][d] = O / L; split rows: the unnormalised partial
-                    // part_o[it][h][d] plus this part's reference maximum and denominator
-                    const bool whole = p.parts == 1;
-                    if (!whole && tid < H) {
-                        p.part_ml[(size_t)it * 2 * H + tid] = mref_s[tid];
-                        p.part_ml[(size_t)it * 2 * H + H + tid] = alpha_s[tid];
-                    }
-#pragma unroll
-                    for (int h = 0; h < H; h++) l[h] = whole ? 1.0f / l[h] : 1.0f;
-                    const int orow = (whole ? n : it) * H;
-                    // through two staging boxes [H][64] fp32 in the P buffers (rows r < 64 at
-                    // P hi, r >= 64 at P lo), stored by TMA
-                    float *stg = reinterpret_cast<float *>(phi_p + (r >> 6) * Lay::PB);
-                    const int rr = r & 63;
-                    for (int j = 0; j < Lay::DB; j++) {
-                        tmem_load<H>(lane_base + Lay::T_O + j * H, v);
-                        if (j == Lay::DB - 1) {
-                            fence_before();
-                            mbar_arrive(bar(B_OFREE));
-                        }
-                        if (j > 0) {
-                            if (tid == 0) bulk_wait_read();
-                            if (!soft_bar()) { ok = false; break; }
-                        }
-#pragma unroll
-                        for (int h = 0; h < H; h++) stg[h * 64 + rr] = v[h] * l[h];
-                        fence_proxy_async();
-                        if (!soft_bar()) { ok = false; break; }
-                        if (tid == 0) {
-                            tma_store_box(&oMap, 128 * j, orow, smem_u32(phi_p));
-                            tma_store_box(&oMap, 128 * j + 64, orow, smem_u32(plo_p));
-                            bulk_commit();
+                    if (q4 == 1) { lfin[2 * lane] += lacc0; lfin[2 * lane + 1] += lacc1; }
+                    if (q4 == 3) { lb[2 * lane] += lacc0; lb[2 * lane + 1] += lacc1; }
+                    if (!soft_bar()) { ok = false; break; }
+                    if (tid < H) {
+                        const float l = lfin[tid] + lb[tid];
+                        lfin[tid] = l;
+                        // split rows: this part's reference maximum and denominator
+                        if (p.parts > 1) {
+                            p.part_ml[(size_t)it * 2 * H + tid] = mref_s[tid];
+                            p.part_ml[(size_t)it * 2 * H + H + tid] = l;
                         }
                     }
-                    if (!ok) break;
-                    // the next P writes reuse the staging boxes
-                    if (tid == 0) bulk_wait_read();
+                    mbar_arrive(bar(B_LREADY));
                 }
             }
+            tok++;
         }
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REG_AUX));
+        // ------------------------------------------------------------ Q loader / epilogue
+        const int q4 = warp & 3;                 // TMEM lane quarter
+        const int r = q4 * 32 + lane;            // d within a 128-wide block
+        const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+        const int tid = threadIdx.x - 256;       // 0..127
+        uint32_t aphase = 0, qph = 0, nq = 0, tok = 0, g = 0;
+        bool ok = true;
+        auto aux_bar = [&]() -> bool {
+            mbar_arrive(bar(B_ABAR));
+            const bool r_ = mbar_wait(bar(B_ABAR), aphase, abort);
+            aphase ^= 1;
+            return r_;
+        };
+        // fp32 Q of the item's query by TMA into the Q chunks, then each 64-d chunk [H][64]
+        // rewritten in place as its bf16 hi (K-major, 128-byte swizzle) and lo halves, one
+        // chunk per round (all reads of a round before its writes)
+        auto load_split = [&](int item) -> bool {
+            nq++;
+            if (tid == 0) {
+                mbar_expect_tx(bar(B_QLOAD), Lay::DC * Lay::QCH);
+                for (int c = 0; c < Lay::DC; c++)
+                    tma_box(smem_u32(sm + Lay::OFF_Q + c * Lay::QCH), &qMap, 64 * c, (item / p.parts) * H, bar(B_QLOAD));
+            }
+            if (!mbar_wait(bar(B_QLOAD), qph, abort)) return false;
+            qph ^= 1;
+            constexpr int PER = H * 64 / 4 / 128;          // float4 per thread per chunk
+            for (int c = 0; c < Lay::DC; c++) {
+                uint8_t *qc = sm + Lay::OFF_Q + c * Lay::QCH;
+                float4 v[PER];
+#pragma unroll
+                for (int j = 0; j < PER; j++) v[j] = *reinterpret_cast<const float4 *>(qc + (j * 128 + tid) * 16);
+                if (!aux_bar()) return false;
+#pragma unroll
+                for (int j = 0; j < PER; j++) {
+                    const int f = j * 128 + tid;
+                    const int h = f / 16, d = (f % 16) * 4;
+                    const int off = h * 128 + (((d / 8) ^ (h & 7)) * 16) + (d % 8) * 2;
+                    float h0, l0, h1, l1, h2, l2, h3, l3;
+                    split_bf16(v[j].x, h0, l0);
+                    split_bf16(v[j].y, h1, l1);
+                    split_bf16(v[j].z, h2, l2);
+                    split_bf16(v[j].w, h3, l3);
+                    *reinterpret_cast<uint2 *>(qc + off) = make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3));
+                    *reinterpret_cast<uint2 *>(qc + off + Lay::QCH / 2) = make_uint2(pack_bf16x2(l0, l1), pack_bf16x2(l2, l3));
+                }
+            }
+            fence_proxy_async();
+            mbar_arrive(bar(B_QREADY));
+            return true;
+        };
+        const int n_items = p.n_q * p.parts;
+        int it = next_item(p, blockIdx.x, n_items);
+        if (it < n_items && !load_split(it)) ok = false;
+        while (ok && it < n_items) {
+            const int nx = next_item(p, it + gridDim.x, n_items);
+            const Tok k = token_geom(p, it / p.parts);
+            const int nc = comp_rows(p, k, nullptr);
+            const Item itm = item_tiles(p, it, 1 + (nc + ROWS - 1) / ROWS);
+            const uint32_t nt = (uint32_t)(itm.te - itm.tb);
+            // the next query's Q as soon as this item's last S has been computed
+            if (nx < n_items) {
+                if (!mbar_wait(bar(B_QFREE), tok & 1, abort) || !load_split(nx)) { ok = false; break; }
+            }
+            // this item's output once its last O and its denominators are complete
+            if (!mbar_wait(bar(B_LREADY), tok & 1, abort)) { ok = false; break; }
+            if (!mbar_wait(bar(B_PVDONE), (g + nt - 1) & 1, abort)) { ok = false; break; }
+            fence_after();
+            // whole query: out[n][h][d] = O / L; split rows: the unnormalised partial part_o[it][h][d]
+            const bool whole = p.parts == 1;
+            float inv[H];
+#pragma unroll
+            for (int h = 0; h < H; h++) inv[h] = whole ? 1.0f / lfin[h] : 1.0f;
+            float *dst = (whole ? p.out : p.part_o) + (size_t)it * H * D + r;
+            for (int j = 0; j < Lay::DB; j++) {
+                float v[H];
+                tmem_load<H>(lane_base + Lay::T_O + j * H, v);
+                fence_before();
+                mbar_arrive(bar(B_OFREE0 + j));
+#pragma unroll
+                for (int h = 0; h < H; h++) __stcs(dst + (size_t)h * D + 128 * j, v[h] * inv[h]);
+            }
+            g += nt;
+            tok++;
+            it = nx;
+        }
+        // the last Q load has landed before the CTA exits (bounded, given up or not)
+        if (nq > 0) mbar_drain(bar(B_QLOAD), (nq - 1) & 1);
     }
-    if (threadIdx.x == 64) bulk_wait_all();
     __syncthreads();
     if (warp == 1) {
         fence_after();
@@ -1099,25 +1135,29 @@ template <int H, int D>
 cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, cudaStream_t s) {
     using Lay = L<H, D>;
     const uint64_t raw_rows = (a.n_seq == 1) ? (uint64_t)(ROWS + a.n_tok) : (uint64_t)a.n_seq * ROWS;
-    const uint64_t comp_rows_total = (uint64_t)a.n_seq_state * a.comp_cap;
     CUtensorMap rh, rl;
     const uint64_t pitch = (uint64_t)2 * D * 2;
     if (!make_map(&rh, a.raw_mirror, raw_rows, D, pitch, 64) || !make_map(&rl, a.raw_mirror + D, raw_rows, D, pitch, 64))
         return cudaErrorNotSupported;
-    // Q in and out, both [n_q * H][D] fp32, one 64 x H box per 64-d chunk
+    // Q [n_q * H][D] fp32, one 64 x H box per 64-d chunk
     const uint64_t qrows = (uint64_t)a.n_seq * a.n_tok * H;
-    // the output map covers out, or the partial outputs [n_q * parts][H][D] when rows are split
-    CUtensorMap qm, om;
-    const bool whole = p.parts == 1;
-    if (!make_map_f32(&qm, a.q, qrows, D, H) ||
-        !make_map_f32(&om, whole ? a.out : a.part_o, whole ? qrows : qrows * (uint64_t)p.parts, D, H))
-        return cudaErrorNotSupported;
-    (void)comp_rows_total;
+    CUtensorMap qm;
+    if (!make_map_f32(&qm, a.q, qrows, D, H)) return cudaErrorNotSupported;
     cudaError_t e = ensure_dyn_smem(attn_tc_kernel<H, D>, Lay::SMEM);
     if (e != cudaSuccess) return e;
+    // the register reallocation at entry needs the launch allocation to cover both shares
+    // (a shortfall would leave the softmax warpgroup waiting for registers): refuse otherwise
+    static int regs = -1;
+    if (regs < 0) {
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, attn_tc_kernel<H, D>);
+        if (e != cudaSuccess) return e;
+        regs = fa.numRegs;
+    }
+    if (4 * 32 * (REG_LOW + REG_SOFT + REG_AUX) > THREADS * regs) return cudaErrorNotSupported;
     const int items = a.n_seq * a.n_tok * p.parts;
     const int grid = items < sm_count() ? items : sm_count();
-    e = launch_pdl(attn_tc_kernel<H, D>, dim3(grid), dim3(THREADS), Lay::SMEM, s, rh, rl, qm, om, p);
+    e = launch_pdl(attn_tc_kernel<H, D>, dim3(grid), dim3(THREADS), Lay::SMEM, s, rh, rl, qm, p);
     if (e != cudaSuccess || p.parts == 1) return e;
     return launch_pdl(attn_combine_kernel, dim3(a.n_seq * a.n_tok * H), dim3(128), 0, s, a.out,
                       (const float *)p.part_o, (const float *)p.part_ml, H, D, p.parts,
