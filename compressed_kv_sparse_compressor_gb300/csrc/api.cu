@@ -63,6 +63,8 @@ int proj_width(const ds4c_layer_cfg &c, bool attn) { return coff_of(c) * lane_wi
 //   mirror: [mirror_rows][2][head_dim] bf16 raw rows for the tensor-core
 //           attention (128 + n_tok rows for a prefill chunk, 128 per sequence
 //           for a decode step)
+//   qsplit: the tensor-core attention's split queries, two buffers of [H][D]
+//           bf16 hi + lo per CTA (one CTA per SM)
 //   parts:  decode steps on the tensor-core attention split each query's rows
 //           over `parts` work items: [n_seq*parts][H][D] + [n_seq*parts][2][H] float
 //   gemm:   decode steps of bf16 layers with at most 128 sequences: split-K
@@ -74,6 +76,7 @@ struct WsLayout {
     size_t proj_off, proj_ld;
     size_t scores_off, scores_ld;
     size_t mirror_off;
+    size_t qsplit_off;
     size_t part_o_off, part_ml_off;
     size_t gemm_part_off;            // 0: no split-K region
     size_t qheads_off;               // 0: no region
@@ -99,6 +102,8 @@ WsLayout ws_layout(const ds4c_layer_cfg &c, uint32_t rows, uint64_t mirror_rows,
     L.parts = 1;
     if (tc_attention(c)) {
         o += align_up((size_t)mirror_rows * 2 * c.head_dim * sizeof(uint16_t), 256);
+        L.qsplit_off = o;
+        o += align_up(attn_tc_qsplit_bytes((int)c.n_heads, (int)c.head_dim), 256);
         if (decode) {
             L.parts = attn_tc_decode_parts((int)c.ratio, (int)c.top_k, (int)c.comp_cap);
             const size_t items = (size_t)rows * L.parts;
@@ -514,6 +519,7 @@ ds4c_status ds4c_sparse_swa_attn(const ds4c_layer_cfg *cfg, const ds4c_layer_sta
         a.ring = st->raw;
         a.comp_split = st->attn.comp_split;
         a.raw_mirror = reinterpret_cast<uint16_t *>(reinterpret_cast<char *>(ws) + L.mirror_off);
+        a.qsplit = reinterpret_cast<uint16_t *>(reinterpret_cast<char *>(ws) + L.qsplit_off);
         a.topk = topk;
         a.out = out;
         a.D = (int)c.head_dim;

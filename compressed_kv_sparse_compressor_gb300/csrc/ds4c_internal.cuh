@@ -258,6 +258,7 @@ struct AttnTcArgs {
     const float *ring;
     const uint16_t *comp_split;   // [n_seq_state][comp_cap][2][D]
     uint16_t *raw_mirror;         // workspace: [rows][2][D]
+    uint16_t *qsplit;             // workspace: attn_tc_qsplit_bytes
     const int32_t *topk;
     float *out;
     int D, H, ratio, k, comp_cap, n_rot;
@@ -271,6 +272,8 @@ struct AttnTcArgs {
 // Work items per decode query: one per two 128-row tiles (the raw window plus
 // the compressed rows a query can see), at most 8.
 int attn_tc_decode_parts(int ratio, int k, int comp_cap);
+// Workspace bytes of the split queries (two buffers per CTA, one CTA per SM).
+size_t attn_tc_qsplit_bytes(int H, int D);
 bool attn_tc_supported(int H, int D, int S, int ratio, int k);
 cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *p, cudaStream_t s);
 unsigned int attn_tc_read_clear_error();

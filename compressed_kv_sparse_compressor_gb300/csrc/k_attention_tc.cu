@@ -38,7 +38,7 @@
 // more than 2^8, so p <= 256 and the final O/L is exact for any reference.
 //
 // Warp roles (384 threads in three warpgroups, persistent over query tokens):
-//   warp 0  row lists and producer         warp 1  MMA issuer, TMEM owner   (warps 2-3 idle)
+//   warps 0, 2  row lists and producers    warp 1  MMA issuer, TMEM owner   (warp 3 idle)
 //   warps 4-7   softmax and P (thread = TMEM lane = tile row)
 //   warps 8-11  Q loader and epilogue (thread = TMEM lane = d within a block): the next
 //               query's Q is loaded and split as soon as the current query's last S has
@@ -65,7 +65,8 @@ namespace {
 constexpr int ROWS = 128;
 constexpr int SLOT = 8192;            // [64 rows][64 d] bf16
 constexpr int PAIR = 2 * SLOT;
-constexpr int RING = 4;
+constexpr int USLOT = 2 * PAIR;      // one ring slot
+constexpr int RING = 5;
 // three warpgroups: {producer, MMA, two idle warps}, the softmax, the Q loader / epilogue
 constexpr int THREADS = 384;
 // registers per thread after the reallocation at entry (setmaxnreg): the first warpgroup gives
@@ -81,14 +82,11 @@ template <int H, int D>
 struct L {
     static constexpr int DC = D / 64;
     static constexpr int DB = D / 128;
-    // Q: chunk c (64 d) at OFF_Q + c * QCH holds the fp32 box [H][64] as the
-    // TMA lands it, then in place its bf16 split: hi [H][64] at +0, lo at +QCH/2,
-    // which together form one K-major [2H][64] operand (the S product's N = 2H)
-    static constexpr int QCH = H * 64 * 4;
     static constexpr int PB = ROWS * H * 2;            // bytes of P hi (or lo)
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_X = OFF_Q + DC * QCH;
-    static constexpr int OFF_PHI = OFF_X + RING * PAIR;
+    // the ring: 16 KB units of gathered rows, raw-row boxes and query chunks (a query
+    // chunk [2H][64] bf16 holds Q_hi of 64 d in rows 0 .. H-1 and Q_lo in rows H .. 2H-1)
+    static constexpr int OFF_X = 0;
+    static constexpr int OFF_PHI = OFF_X + RING * USLOT;
     static constexpr int OFF_PLO = OFF_PHI + PB;
     static constexpr int OFF_LIST = OFF_PLO + PB;
     // per head: the tile maximum as an order-preserving key, then (same word)
@@ -99,7 +97,8 @@ struct L {
     // per head: the softmax denominator of the item the epilogue writes
     static constexpr int OFF_LFIN = OFF_FLAG + 32;
     static constexpr int OFF_BAR = OFF_LFIN + 4 * H;
-    static constexpr int N_BAR = 2 * RING + 17;
+    static constexpr int N_BAR = 2 * RING + 18;
+    static_assert(2 * H * 64 * 2 == PAIR, "a query chunk fills half a ring slot");
     // the dynamic shared memory starts 1024-byte aligned (checked at entry), as
     // the 128-byte swizzle atoms of Q, the ring and P need
     static constexpr int SMEM = OFF_BAR + 8 * N_BAR + 16;
@@ -113,12 +112,13 @@ struct L {
 };
 
 // barrier indices
-enum { B_FULL = 0, B_EMPTY = RING, B_QREADY = 2 * RING, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1, B_PFULL, B_PVDONE,
-       B_OFREE0, B_OFREE1, B_OFREE2, B_OFREE3, B_SOFT, B_QLOAD, B_DRAIN, B_QFREE, B_ABAR, B_LREADY };
+enum { B_FULL = 0, B_EMPTY = RING, B_QREADY0 = 2 * RING, B_QREADY1, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1, B_PFULL,
+       B_PVDONE, B_OFREE0, B_OFREE1, B_OFREE2, B_OFREE3, B_SOFT, B_DRAIN, B_QFREE0, B_QFREE1, B_LREADY, B_PBAR };
 
 struct TcAttnParams {
     float *out;
     const float *q;
+    uint16_t *qsplit;                // per CTA two buffers [D/64][2H][64] bf16 of split queries
     const int32_t *topk;
     const uint16_t *comp_split;      // [rows][2][D]
     int n_q, n_seq, n_tok, k, ratio, comp_cap;
@@ -142,8 +142,9 @@ __device__ __forceinline__ uint64_t globaltimer() {
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+// the bytes a phase still waits for, without an arrival
+__device__ __forceinline__ void mbar_expect_tx_only(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -205,17 +206,13 @@ __device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap *map, in
         : "memory");
 }
 
-
-// Shared-memory matrix descriptor (tcgen05): start, leading / stride byte
-// offsets, version 1, layout (0 = no swizzle, 2 = 128-byte swizzle).
-__device__ __forceinline__ uint64_t make_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
-    uint64_t d = 0;
-    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)layout << 61;
-    return d;
+// Shared-memory matrix descriptor (tcgen05) with the start address left zero: leading /
+// stride byte offsets, version 1, layout (2 = 128-byte swizzle).  Adding (address >> 4)
+// fills in the start (shared-memory addresses are below 256 KB, so the sum stays inside
+// the 14-bit field).
+__host__ __device__ constexpr uint64_t desc_template(uint32_t lbo, uint32_t sbo, uint32_t layout) {
+    return ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) |
+           ((uint64_t)layout << 61);
 }
 
 // Instruction descriptor, kind::f16 with bf16 operands and f32 accumulation.
@@ -458,7 +455,7 @@ __device__ __forceinline__ int next_item(const TcAttnParams &p, int it, int n_it
 template <int H, int D>
 __global__ void __launch_bounds__(THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant__ CUtensorMap rawLo,
-               const __grid_constant__ CUtensorMap qMap, const TcAttnParams p) {
+               const __grid_constant__ CUtensorMap qsMap, const TcAttnParams p) {
     using Lay = L<H, D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if ((smem_u32(smem_raw) & 1023u) != 0) {            // the layout has no room to realign
@@ -481,10 +478,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
         for (int i = 0; i < RING; i++) {
-            mbar_init(bar(B_FULL + i), 32);        // one arrival per producer lane
+            mbar_init(bar(B_FULL + i), 64);        // one arrival per lane of the two producer warps
             mbar_init(bar(B_EMPTY + i), 1);
         }
-        mbar_init(bar(B_QREADY), 128);
+        mbar_init(bar(B_QREADY0), 128);
+        mbar_init(bar(B_QREADY1), 128);
         mbar_init(bar(B_SFULL0), 1);
         mbar_init(bar(B_SFULL1), 1);
         mbar_init(bar(B_SFREE0), 128);
@@ -493,11 +491,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         mbar_init(bar(B_PVDONE), 1);
         for (int j = 0; j < 4; j++) mbar_init(bar(B_OFREE0 + j), 128);
         mbar_init(bar(B_SOFT), 128);
-        mbar_init(bar(B_QLOAD), 1);
         mbar_init(bar(B_DRAIN), 1);
-        mbar_init(bar(B_QFREE), 1);
-        mbar_init(bar(B_ABAR), 128);
+        mbar_init(bar(B_QFREE0), 1);
+        mbar_init(bar(B_QFREE1), 1);
         mbar_init(bar(B_LREADY), 128);
+        mbar_init(bar(B_PBAR), 64);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -520,110 +518,194 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
     // shares fit the launch allocation.
     if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REG_LOW));
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        uint32_t unit = 0;
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------------------------------ producer pair
+        // warps 0 and 2 share every unit: each copies the 16-row blocks of its parity, and
+        // both count on the unit's barrier; the row list is written by warp 0 between two
+        // barriers of the pair (the previous list read by both, the new one complete)
+        const int pw = warp >> 1;
+        uint32_t unit = 0, pphase = 0, tok = 0;
         bool ok = true;
+        auto pair_bar = [&]() -> bool {
+            mbar_arrive(bar(B_PBAR));
+            const bool r_ = mbar_wait(bar(B_PBAR), pphase, abort);
+            pphase ^= 1;
+            return r_;
+        };
         const int n_items = p.n_q * p.parts;
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const Tok k = token_geom(p, it / p.parts);
+            if (!pair_bar()) { ok = false; break; }
+            const int nc = comp_rows(p, k, (p.ratio == 4 && pw == 0) ? list : nullptr);
             __syncwarp();
-            const int nc = comp_rows(p, k, p.ratio == 4 ? list : nullptr);
-            __syncwarp();
+            if (!pair_bar()) { ok = false; break; }
             const Item itm = item_tiles(p, it, 1 + (nc + ROWS - 1) / ROWS);
             if (itm.tb >= itm.te) continue;
+            // this item's split query (buffer tok & 1 of this CTA) has been written
+            const int qbuf = tok & 1;
+            if (pw == 0) {
+                int okq = 1;
+                if (lane == 0) okq = mbar_wait(bar(B_QREADY0 + qbuf), (tok >> 1) & 1, abort) ? 1 : 0;
+                if (__shfl_sync(0xffffffffu, okq, 0) == 0) { ok = false; break; }
+            }
+            tok++;
+            const int qrow0 = (blockIdx.x * 2 + qbuf) * Lay::DC * 2 * H;
             const int dummy = k.seq * p.comp_cap;
             auto row_of = [&](int tile, int r) -> int {   // comp mirror row of tile >= 1, row r
                 const int i = (tile - 1) * ROWS + r;
                 if (i >= nc) return dummy;
                 return p.ratio == 4 ? list[i] : dummy + i;
             };
-            // this lane's eight tile rows 16 b + lane / 2 (b = 0 .. 7): every unit of a
-            // compressed tile copies from them, so their mirror addresses are formed once per tile
-            const uint16_t *rp[8];
+            // this lane's rows 16 b + lane / 2 for the four row blocks b = 2 bb + pw of this
+            // warp: every slot of a compressed tile copies from them, so their mirror
+            // addresses are formed once per tile
+            const uint16_t *rp[4];
             int rp_tile = -1;
             auto tile_rows = [&](int tile) {
                 if (tile == rp_tile) return;
                 rp_tile = tile;
 #pragma unroll
-                for (int b = 0; b < 8; b++) rp[b] = p.comp_split + (size_t)row_of(tile, 16 * b + (lane >> 1)) * 2 * D;
+                for (int bb = 0; bb < 4; bb++)
+                    rp[bb] = p.comp_split + (size_t)row_of(tile, 16 * (2 * bb + pw) + (lane >> 1)) * 2 * D;
             };
-            // one 16 KB unit into the next ring pair; every lane takes part
-            auto issue = [&](int tile, bool pv, int a, int hh, int lo) -> bool {
+            // this warp's half of 16 KB of gathered compressed rows at dst, in the 128-byte swizzle
+            // layout: (pv = false) rows 0 .. 127 of the 64-d chunk at element offset off; (pv =
+            // true) rows 64 hh .. 64 hh + 63 of the 128-d block at off, as two [64][64] halves
+            // SLOT apart.  Lane pairs take the two halves of one 32-byte sector, so an
+            // instruction covers 16 rows x 32 bytes.
+            auto gather16 = [&](uint32_t dst, int tile, bool pv, int off, int hh) {
+                tile_rows(tile);
+                const int sw = (lane >> 1) & 7;              // row & 7 of every row this lane copies
+                if (!pv) {
+#pragma unroll
+                    for (int bb = 0; bb < 4; bb++) {
+                        const int r = 16 * (2 * bb + pw) + (lane >> 1);
+                        const uint16_t *src = rp[bb] + off;
+                        const uint32_t drow = dst + r * 128;
+#pragma unroll
+                        for (int sct = 0; sct < 4; sct++) {
+                            const int u = 2 * sct + (lane & 1);
+                            cp_async16(drow + ((u ^ sw) << 4), src + 8 * u);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int bb = 0; bb < 2; bb++) {
+                        const int rr = 16 * (2 * bb + pw) + (lane >> 1);
+                        const uint16_t *src0 = rp[2 * hh + bb] + off;
+#pragma unroll
+                        for (int sct = 0; sct < 8; sct++) {
+                            const int half = sct >> 2, u = 2 * (sct & 3) + (lane & 1);
+                            cp_async16(dst + half * SLOT + rr * 128 + ((u ^ sw) << 4), src0 + 64 * half + 8 * u);
+                        }
+                    }
+                }
+            };
+            // the next 32 KB slot of the ring, once the MMAs of its previous contents are done
+            auto open_slot = [&](uint32_t &dst, uint32_t &fb) -> bool {
                 const int s_ = unit % RING;
                 const uint32_t ph = (unit / RING) & 1;
                 unit++;
                 int okw = 1;
                 if (lane == 0) okw = mbar_wait(bar(B_EMPTY + s_), ph ^ 1, abort) ? 1 : 0;
                 if (__shfl_sync(0xffffffffu, okw, 0) == 0) {
-                    unit--;                                  // nothing was issued for this unit
+                    unit--;                                  // nothing was issued for this slot
                     return false;
                 }
-                const uint32_t dst = smem_u32(sm + Lay::OFF_X + s_ * PAIR);
-                const uint32_t fb = bar(B_FULL + s_);
+                dst = smem_u32(sm + Lay::OFF_X + s_ * USLOT);
+                fb = bar(B_FULL + s_);
+                return true;
+            };
+            // A slot's barrier takes one arrival per lane of the pair (a lane that gathered arrives
+            // when its copies land) plus the bytes of the slot's TMA boxes, which lane 0 of warp 0
+            // announces before issuing them.
+            const bool lead = pw == 0 && lane == 0;
+            // S operands of chunk c: [query chunk c | hi of the rows' chunk c]
+            auto slot_qk = [&](int tile, int c) -> bool {
+                uint32_t dst, fb;
+                if (!open_slot(dst, fb)) return false;
                 if (tile == 0) {
-                    if (lane == 0) {
-                        const CUtensorMap *m = lo ? &rawLo : &rawHi;
-                        mbar_expect_tx(fb, PAIR);
-                        if (!pv) {      // d-chunk a, rows 0..127
-                            tma_box(dst, m, 64 * a, k.raw_row0, fb);
-                            tma_box(dst + SLOT, m, 64 * a, k.raw_row0 + 64, fb);
-                        } else {        // d-block a, rows 64*hh .. 64*hh+63
-                            tma_box(dst, m, 128 * a, k.raw_row0 + 64 * hh, fb);
-                            tma_box(dst + SLOT, m, 128 * a + 64, k.raw_row0 + 64 * hh, fb);
-                        }
-                    } else {
-                        mbar_arrive(fb);
+                    if (lead) {
+                        mbar_expect_tx_only(fb, USLOT);
+                        tma_box(dst, &qsMap, 0, qrow0 + c * 2 * H, fb);
+                        tma_box(dst + PAIR, &rawHi, 64 * c, k.raw_row0, fb);
+                        tma_box(dst + PAIR + SLOT, &rawHi, 64 * c, k.raw_row0 + 64, fb);
                     }
+                    mbar_arrive(fb);
                 } else {
-                    // 1024 chunks of 16 bytes, 32 per lane, in the 128-byte swizzle layout
-                    tile_rows(tile);
-                    const int sw = (lane >> 1) & 7;              // row & 7 of every row this lane copies
-                    if (!pv) {
-                        // lane pairs take the two halves of one 32-byte sector: an
-                        // instruction covers 16 rows x 32 bytes
-                        const int off = lo * D + 64 * a;
-#pragma unroll
-                        for (int b = 0; b < 8; b++) {
-                            const int r = 16 * b + (lane >> 1);
-                            const uint16_t *src = rp[b] + off;
-                            const uint32_t drow = dst + r * 128;
-#pragma unroll
-                            for (int sct = 0; sct < 4; sct++) {
-                                const int u = 2 * sct + (lane & 1);
-                                cp_async16(drow + ((u ^ sw) << 4), src + 8 * u);
-                            }
-                        }
-                    } else {
-                        const int off = lo * D + 128 * a;
-#pragma unroll
-                        for (int b = 0; b < 4; b++) {
-                            const int rr = 16 * b + (lane >> 1);
-                            const uint16_t *src0 = (hh ? rp[4 + b] : rp[b]) + off;
-#pragma unroll
-                            for (int sct = 0; sct < 8; sct++) {
-                                const int half = sct >> 2, u = 2 * (sct & 3) + (lane & 1);
-                                cp_async16(dst + half * SLOT + rr * 128 + ((u ^ sw) << 4), src0 + 64 * half + 8 * u);
-                            }
-                        }
+                    if (lead) {
+                        mbar_expect_tx_only(fb, PAIR);
+                        tma_box(dst, &qsMap, 0, qrow0 + c * 2 * H, fb);
                     }
+                    gather16(dst + PAIR, tile, false, 64 * c, 0);
                     cp_async_arrive(fb);
                 }
                 return true;
             };
+            // lo of the rows' chunks c0 and c1 (c1 < 0: none): [lo c0 | lo c1]
+            auto slot_qk_lo = [&](int tile, int c0, int c1) -> bool {
+                uint32_t dst, fb;
+                if (!open_slot(dst, fb)) return false;
+                if (tile == 0) {
+                    if (lead) {
+                        mbar_expect_tx_only(fb, c1 >= 0 ? USLOT : PAIR);
+                        tma_box(dst, &rawLo, 64 * c0, k.raw_row0, fb);
+                        tma_box(dst + SLOT, &rawLo, 64 * c0, k.raw_row0 + 64, fb);
+                        if (c1 >= 0) {
+                            tma_box(dst + PAIR, &rawLo, 64 * c1, k.raw_row0, fb);
+                            tma_box(dst + PAIR + SLOT, &rawLo, 64 * c1, k.raw_row0 + 64, fb);
+                        }
+                    }
+                    mbar_arrive(fb);
+                } else {
+                    gather16(dst, tile, false, D + 64 * c0, 0);
+                    if (c1 >= 0) gather16(dst + PAIR, tile, false, D + 64 * c1, 0);
+                    cp_async_arrive(fb);
+                }
+                return true;
+            };
+            // O operands of d-block j, hi (lo = 0) or lo (lo = 1): [rows 0 .. 63 | rows 64 .. 127]
+            auto slot_pv = [&](int tile, int j, int lo) -> bool {
+                uint32_t dst, fb;
+                if (!open_slot(dst, fb)) return false;
+                if (tile == 0) {
+                    if (lead) {
+                        const CUtensorMap *m = lo ? &rawLo : &rawHi;
+                        mbar_expect_tx_only(fb, USLOT);
+                        for (int hh = 0; hh < 2; hh++) {
+                            tma_box(dst + hh * PAIR, m, 128 * j, k.raw_row0 + 64 * hh, fb);
+                            tma_box(dst + hh * PAIR + SLOT, m, 128 * j + 64, k.raw_row0 + 64 * hh, fb);
+                        }
+                    }
+                    mbar_arrive(fb);
+                } else {
+                    gather16(dst, tile, true, lo * D + 128 * j, 0);
+                    gather16(dst + PAIR, tile, true, lo * D + 128 * j, 1);
+                    cp_async_arrive(fb);
+                }
+                return true;
+            };
+            // the S slots of a tile: every chunk's, each lo chunk pair's (or a last single one's)
+            // right after the pair's second chunk
             auto issue_qk = [&](int tile) -> bool {
+                const int c0 = tile == 0 ? 0 : p.nope_chunks;     // the first chunk with a lo half
                 for (int c = 0; c < Lay::DC; c++) {
-                    if (!issue(tile, false, c, 0, 0)) return false;
-                    if ((tile == 0 || c >= p.nope_chunks) && !issue(tile, false, c, 0, 1)) return false;
+                    if (!slot_qk(tile, c)) return false;
+                    if (c >= c0) {
+                        if ((c - c0) & 1) {
+                            if (!slot_qk_lo(tile, c - 1, c)) return false;
+                        } else if (c == Lay::DC - 1) {
+                            if (!slot_qk_lo(tile, c, -1)) return false;
+                        }
+                    }
                 }
                 return true;
             };
             auto issue_pv = [&](int tile) -> bool {
-                for (int j = 0; j < Lay::DB; j++)
-                    for (int hh = 0; hh < 2; hh++) {
-                        if (!issue(tile, true, j, hh, 0)) return false;
-                        if ((tile == 0 || j >= p.nope_blocks) && !issue(tile, true, j, hh, 1)) return false;
-                    }
+                for (int j = 0; j < Lay::DB; j++) {
+                    if (!slot_pv(tile, j, 0)) return false;
+                    if ((tile == 0 || j >= p.nope_blocks) && !slot_pv(tile, j, 1)) return false;
+                }
                 return true;
             };
             bool good = issue_qk(itm.tb);
@@ -647,41 +729,71 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         constexpr uint32_t ID_QK = idesc(128, H, 0, 0);
         constexpr uint32_t ID_QK2 = idesc(128, 2 * H, 0, 0);
         constexpr uint32_t ID_PV = idesc(128, H, 1, 1);
-        const uint32_t qs = smem_u32(sm + Lay::OFF_Q);
+        constexpr uint64_t DK = desc_template(16, 1024, 2);      // S operands
+        constexpr uint64_t DA = desc_template(SLOT, 1024, 2);    // X^T of the O product
+        constexpr uint64_t DP = desc_template(8192, 1024, 2);    // P^T
         const uint32_t phi = smem_u32(sm + Lay::OFF_PHI), plo = smem_u32(sm + Lay::OFF_PLO);
         uint32_t unit = 0, g = 0, tok = 0;
         bool ok = true;
-        // unit u of the ring: wait until loaded / hand back once its MMAs finish
-        auto wait_unit = [&](uint32_t u, uint32_t &base) -> bool {
-            base = smem_u32(sm + Lay::OFF_X + (u % RING) * PAIR);
+        // slot u of the ring: wait until loaded / hand back once its MMAs finish
+        auto wait_slot = [&](uint32_t u, uint32_t &base) -> bool {
+            base = smem_u32(sm + Lay::OFF_X + (u % RING) * USLOT);
             return mbar_wait(bar(B_FULL + u % RING), (u / RING) & 1, abort);
         };
-        auto free_unit = [&](uint32_t u) { mma_commit(bar(B_EMPTY + u % RING)); };
-        // S of global tile gt; `last`: the item's last tile, after which Q is no longer read
+        auto free_slot = [&](uint32_t u) { mma_commit(bar(B_EMPTY + u % RING)); };
+        // S of global tile gt; `last`: the item's last tile, after which its query chunks are
+        // no longer read.  The slots of a lo chunk pair's query chunks stay held until the
+        // pair's lo product has been issued.
         auto do_qk = [&](uint32_t gt, int tile, bool last) -> bool {
             const int sb = gt & 1;
             if (gt >= 2 && !mbar_wait(bar(B_SFREE0 + sb), ((gt >> 1) - 1) & 1, abort)) return false;
             fence_after();
             const uint32_t d_t = tmem + Lay::T_S + sb * 2 * H;
+            const int c0 = tile == 0 ? 0 : p.nope_chunks;
+            uint32_t hu0 = 0, hb0 = 0, hu1 = 0, hb1 = 0;   // held slots (index, address)
+            int nheld = 0;
             for (int c = 0; c < Lay::DC; c++) {
-                const bool has_lo = tile == 0 || c >= p.nope_chunks;
-                uint32_t xh, xl = 0;
-                if (!wait_unit(unit, xh)) return false;
-                if (has_lo && !wait_unit(unit + 1, xl)) return false;
+                uint32_t b;
+                if (!wait_slot(unit, b)) return false;
                 fence_proxy_async();
                 fence_after();
-                for (int kk = 0; kk < 4; kk++) {
-                    const uint64_t ah = make_desc(xh + kk * 32, 16, 1024, 2);
-                    // [Q_hi; Q_lo] rows 0 .. 2H-1: the lo half follows the hi half at the same pitch
-                    const uint64_t b2 = make_desc(qs + c * Lay::QCH + kk * 32, 16, 1024, 2);
-                    mma(d_t, ah, b2, ID_QK2, (c > 0 || kk > 0) ? 1u : 0u);
-                    if (has_lo) mma(d_t, make_desc(xl + kk * 32, 16, 1024, 2), b2, ID_QK, 1u);
+                // K-major operands, 32 bytes (2 descriptor units) per K step of 16: the rows' hi
+                // against [Q_hi; Q_lo] (rows 0 .. 2H-1 of the query chunk)
+                const uint64_t q0 = DK + (b >> 4), x0 = DK + ((b + PAIR) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < 4; kk++) mma(d_t, x0 + 2 * kk, q0 + 2 * kk, ID_QK2, (c > 0 || kk > 0) ? 1u : 0u);
+                const uint32_t mu = unit++;
+                if (c < c0) {
+                    free_slot(mu);
+                    continue;
                 }
-                free_unit(unit++);
-                if (has_lo) free_unit(unit++);
+                if (nheld == 0) { hu0 = mu; hb0 = b; } else { hu1 = mu; hb1 = b; }
+                nheld++;
+                if (((c - c0) & 1) || c == Lay::DC - 1) {
+                    // the rows' lo of the held chunks against Q_hi
+                    uint32_t lb;
+                    if (!wait_slot(unit, lb)) return false;
+                    fence_proxy_async();
+                    fence_after();
+                    {
+                        const uint64_t ql = DK + (hb0 >> 4), xl = DK + (lb >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < 4; kk++) mma(d_t, xl + 2 * kk, ql + 2 * kk, ID_QK, 1u);
+                    }
+                    if (nheld == 2) {
+                        const uint64_t ql = DK + (hb1 >> 4), xl = DK + ((lb + PAIR) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < 4; kk++) mma(d_t, xl + 2 * kk, ql + 2 * kk, ID_QK, 1u);
+                    }
+                    free_slot(hu0);
+                    if (nheld == 2) free_slot(hu1);
+                    free_slot(unit++);
+                    nheld = 0;
+                }
             }
             mma_commit(bar(B_SFULL0 + sb));
-            if (last) mma_commit(bar(B_QFREE));        // the Q buffer may take the next query
+            // every query chunk of this item has been read: its split buffer may be refilled
+            if (last) mma_commit(bar(B_QFREE0 + (tok & 1)));
             return true;
         };
         // O of tile i; `first`: the item's first tile (overwrites the accumulator), which
@@ -694,25 +806,32 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                 }
                 const uint32_t d_o = tmem + Lay::T_O + j * H;
                 const bool has_lo = i == 0 || j >= p.nope_blocks;
-                for (int hh = 0; hh < 2; hh++) {
-                    uint32_t xh, xl = 0;
-                    if (!wait_unit(unit, xh)) return false;
-                    if (has_lo && !wait_unit(unit + 1, xl)) return false;
+                uint32_t xb;
+                if (!wait_slot(unit, xb)) return false;
+                fence_proxy_async();
+                fence_after();
+                // MN-major operands, 16 rows (128 descriptor units) per K step; rows 0 .. 63 in the
+                // slot's first half, 64 .. 127 in its second
+#pragma unroll
+                for (int kk = 0; kk < 8; kk++) {
+                    const uint32_t aoff = (uint32_t)((kk >> 2) * PAIR + (kk & 3) * 2048);
+                    const uint64_t ah = DA + ((xb + aoff) >> 4);
+                    const uint64_t bh = DP + ((phi + kk * 2048) >> 4), bl = DP + ((plo + kk * 2048) >> 4);
+                    mma(d_o, ah, bh, ID_PV, (first && kk == 0) ? 0u : 1u);
+                    mma(d_o, ah, bl, ID_PV, 1u);
+                }
+                free_slot(unit++);
+                if (has_lo) {
+                    uint32_t lb;
+                    if (!wait_slot(unit, lb)) return false;
                     fence_proxy_async();
                     fence_after();
-                    for (int kk = 0; kk < 4; kk++) {
-                        const uint32_t koff = (uint32_t)(kk * 16 * 128);
-                        const uint32_t prow = (uint32_t)((64 * hh + 16 * kk) * 128);
-                        const uint64_t ah = make_desc(xh + koff, SLOT, 1024, 2);
-                        const uint64_t bh = make_desc(phi + prow, 8192, 1024, 2);
-                        const uint64_t bl = make_desc(plo + prow, 8192, 1024, 2);
-                        const uint32_t acc = (first && hh == 0 && kk == 0) ? 0u : 1u;
-                        mma(d_o, ah, bh, ID_PV, acc);
-                        mma(d_o, ah, bl, ID_PV, 1u);
-                        if (has_lo) mma(d_o, make_desc(xl + koff, SLOT, 1024, 2), bh, ID_PV, 1u);
+#pragma unroll
+                    for (int kk = 0; kk < 8; kk++) {
+                        const uint32_t aoff = (uint32_t)((kk >> 2) * PAIR + (kk & 3) * 2048);
+                        mma(d_o, DA + ((lb + aoff) >> 4), DP + ((phi + kk * 2048) >> 4), ID_PV, 1u);
                     }
-                    free_unit(unit++);
-                    if (has_lo) free_unit(unit++);
+                    free_slot(unit++);
                 }
             }
             mma_commit(bar(B_PVDONE));
@@ -726,11 +845,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             if (itm.tb >= itm.te) continue;
             int good = 1;
             if (lane == 0) {
-                good = mbar_wait(bar(B_QREADY), tok & 1, abort) ? 1 : 0;
-                if (good) {
-                    fence_after();
-                    good = do_qk(g, itm.tb, itm.tb == itm.te - 1) ? 1 : 0;
-                }
+                good = do_qk(g, itm.tb, itm.tb == itm.te - 1) ? 1 : 0;
                 for (int i = itm.tb; i < itm.te && good; i++) {
                     const uint32_t gi = g + (i - itm.tb);
                     if (i + 1 < itm.te && !do_qk(gi + 1, i + 1, i + 1 == itm.te - 1)) { good = 0; break; }
@@ -912,63 +1027,53 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         const int r = q4 * 32 + lane;            // d within a 128-wide block
         const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
         const int tid = threadIdx.x - 256;       // 0..127
-        uint32_t aphase = 0, qph = 0, nq = 0, tok = 0, g = 0;
+        uint32_t tok = 0, g = 0;
         bool ok = true;
-        auto aux_bar = [&]() -> bool {
-            mbar_arrive(bar(B_ABAR));
-            const bool r_ = mbar_wait(bar(B_ABAR), aphase, abort);
-            aphase ^= 1;
-            return r_;
-        };
-        // fp32 Q of the item's query by TMA into the Q chunks, then each 64-d chunk [H][64]
-        // rewritten in place as its bf16 hi (K-major, 128-byte swizzle) and lo halves, one
-        // chunk per round (all reads of a round before its writes)
-        auto load_split = [&](int item) -> bool {
-            nq++;
-            if (tid == 0) {
-                mbar_expect_tx(bar(B_QLOAD), Lay::DC * Lay::QCH);
-                for (int c = 0; c < Lay::DC; c++)
-                    tma_box(smem_u32(sm + Lay::OFF_Q + c * Lay::QCH), &qMap, 64 * c, (item / p.parts) * H, bar(B_QLOAD));
-            }
-            if (!mbar_wait(bar(B_QLOAD), qph, abort)) return false;
-            qph ^= 1;
-            constexpr int PER = H * 64 / 4 / 128;          // float4 per thread per chunk
-            for (int c = 0; c < Lay::DC; c++) {
-                uint8_t *qc = sm + Lay::OFF_Q + c * Lay::QCH;
-                float4 v[PER];
+        // fp32 Q [H][D] of the item's query, split into bf16 hi / lo, into this CTA's buffer
+        // `buf` as D/64 query chunks [2H][64] (rows 0 .. H-1 hi, H .. 2H-1 lo), which the
+        // producer loads by TMA into the 128-byte-swizzled K-major operand layout
+        auto prepare = [&](int item, int buf) {
+            const float4 *src = reinterpret_cast<const float4 *>(p.q + (size_t)(item / p.parts) * H * D);
+            uint16_t *qd = p.qsplit + ((size_t)blockIdx.x * 2 + buf) * Lay::DC * 2 * H * 64;
+            constexpr int NF = H * D / 4 / 128;           // float4 per thread
+            static_assert(NF % 8 == 0, "whole batches of eight loads");
+            for (int j0 = 0; j0 < NF; j0 += 8) {
+                float4 v[8];
 #pragma unroll
-                for (int j = 0; j < PER; j++) v[j] = *reinterpret_cast<const float4 *>(qc + (j * 128 + tid) * 16);
-                if (!aux_bar()) return false;
+                for (int u = 0; u < 8; u++) v[u] = __ldcs(src + tid + 128 * (j0 + u));
 #pragma unroll
-                for (int j = 0; j < PER; j++) {
-                    const int f = j * 128 + tid;
-                    const int h = f / 16, d = (f % 16) * 4;
-                    const int off = h * 128 + (((d / 8) ^ (h & 7)) * 16) + (d % 8) * 2;
+                for (int u = 0; u < 8; u++) {
+                    const int f = tid + 128 * (j0 + u);
+                    const int h = f / (D / 4), d = (f % (D / 4)) * 4;
+                    uint16_t *row = qd + ((size_t)(d / 64) * 2 * H + h) * 64 + (d % 64);
                     float h0, l0, h1, l1, h2, l2, h3, l3;
-                    split_bf16(v[j].x, h0, l0);
-                    split_bf16(v[j].y, h1, l1);
-                    split_bf16(v[j].z, h2, l2);
-                    split_bf16(v[j].w, h3, l3);
-                    *reinterpret_cast<uint2 *>(qc + off) = make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3));
-                    *reinterpret_cast<uint2 *>(qc + off + Lay::QCH / 2) = make_uint2(pack_bf16x2(l0, l1), pack_bf16x2(l2, l3));
+                    split_bf16(v[u].x, h0, l0);
+                    split_bf16(v[u].y, h1, l1);
+                    split_bf16(v[u].z, h2, l2);
+                    split_bf16(v[u].w, h3, l3);
+                    *reinterpret_cast<uint2 *>(row) = make_uint2(pack_bf16x2(h0, h1), pack_bf16x2(h2, h3));
+                    *reinterpret_cast<uint2 *>(row + H * 64) = make_uint2(pack_bf16x2(l0, l1), pack_bf16x2(l2, l3));
                 }
             }
-            fence_proxy_async();
-            mbar_arrive(bar(B_QREADY));
-            return true;
+            // the producer's TMA (async proxy) reads what these stores wrote
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            mbar_arrive(bar(B_QREADY0 + buf));
         };
         const int n_items = p.n_q * p.parts;
         int it = next_item(p, blockIdx.x, n_items);
-        if (it < n_items && !load_split(it)) ok = false;
+        if (it < n_items) prepare(it, 0);
         while (ok && it < n_items) {
             const int nx = next_item(p, it + gridDim.x, n_items);
             const Tok k = token_geom(p, it / p.parts);
             const int nc = comp_rows(p, k, nullptr);
             const Item itm = item_tiles(p, it, 1 + (nc + ROWS - 1) / ROWS);
             const uint32_t nt = (uint32_t)(itm.te - itm.tb);
-            // the next query's Q as soon as this item's last S has been computed
+            // the next query into the other buffer, once the item that last used it (the
+            // previous one) has had all its query chunks read
             if (nx < n_items) {
-                if (!mbar_wait(bar(B_QFREE), tok & 1, abort) || !load_split(nx)) { ok = false; break; }
+                const int nb = (tok + 1) & 1;
+                if (tok >= 1 && !mbar_wait(bar(B_QFREE0 + nb), ((tok - 1) >> 1) & 1, abort)) { ok = false; break; }
+                prepare(nx, nb);
             }
             // this item's output once its last O and its denominators are complete
             if (!mbar_wait(bar(B_LREADY), tok & 1, abort)) { ok = false; break; }
@@ -992,8 +1097,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             tok++;
             it = nx;
         }
-        // the last Q load has landed before the CTA exits (bounded, given up or not)
-        if (nq > 0) mbar_drain(bar(B_QLOAD), (nq - 1) & 1);
     }
     __syncthreads();
     if (warp == 1) {
@@ -1107,19 +1210,6 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, int D, uint64_t p
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D fp32 map over a dense [rows][D] array, boxes of 64 x box_rows, no swizzle.
-bool make_map_f32(CUtensorMap *m, const float *base, uint64_t rows, int D, uint32_t box_rows) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 4};
-    cuuint32_t box[2] = {64, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int sm_count() {
     static int n = 0;
     if (n == 0) {
@@ -1139,10 +1229,11 @@ cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, cudaStream_t s
     const uint64_t pitch = (uint64_t)2 * D * 2;
     if (!make_map(&rh, a.raw_mirror, raw_rows, D, pitch, 64) || !make_map(&rl, a.raw_mirror + D, raw_rows, D, pitch, 64))
         return cudaErrorNotSupported;
-    // Q [n_q * H][D] fp32, one 64 x H box per 64-d chunk
-    const uint64_t qrows = (uint64_t)a.n_seq * a.n_tok * H;
+    const int items = a.n_seq * a.n_tok * p.parts;
+    const int grid = items < sm_count() ? items : sm_count();
+    // the split queries: per CTA two buffers of D/64 chunks [2H][64] bf16, one 128-row box each
     CUtensorMap qm;
-    if (!make_map_f32(&qm, a.q, qrows, D, H)) return cudaErrorNotSupported;
+    if (!make_map(&qm, a.qsplit, (uint64_t)grid * 2 * Lay::DC * 2 * H, 64, 128, 2 * H)) return cudaErrorNotSupported;
     cudaError_t e = ensure_dyn_smem(attn_tc_kernel<H, D>, Lay::SMEM);
     if (e != cudaSuccess) return e;
     // the register reallocation at entry needs the launch allocation to cover both shares
@@ -1155,8 +1246,6 @@ cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, cudaStream_t s
         regs = fa.numRegs;
     }
     if (4 * 32 * (REG_LOW + REG_SOFT + REG_AUX) > THREADS * regs) return cudaErrorNotSupported;
-    const int items = a.n_seq * a.n_tok * p.parts;
-    const int grid = items < sm_count() ? items : sm_count();
     e = launch_pdl(attn_tc_kernel<H, D>, dim3(grid), dim3(THREADS), Lay::SMEM, s, rh, rl, qm, p);
     if (e != cudaSuccess || p.parts == 1) return e;
     return launch_pdl(attn_combine_kernel, dim3(a.n_seq * a.n_tok * H), dim3(128), 0, s, a.out,
@@ -1165,6 +1254,8 @@ cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, cudaStream_t s
 }
 
 }  // namespace
+
+size_t attn_tc_qsplit_bytes(int H, int D) { return (size_t)sm_count() * 2 * 2 * H * D * sizeof(uint16_t); }
 
 int attn_tc_decode_parts(int ratio, int k, int comp_cap) {
     // about two tiles per work item: each item loads its query's Q and writes one
@@ -1194,6 +1285,7 @@ cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *dp, cudaSt
     TcAttnParams p{};
     p.out = a.out;
     p.q = a.q;
+    p.qsplit = a.qsplit;
     p.topk = a.topk;
     p.comp_split = a.comp_split;
     p.nope_chunks = (a.D - a.n_rot) / 64;
