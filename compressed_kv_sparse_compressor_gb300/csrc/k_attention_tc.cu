@@ -66,7 +66,7 @@ constexpr int ROWS = 128;
 constexpr int SLOT = 8192;            // [64 rows][64 d] bf16
 constexpr int PAIR = 2 * SLOT;
 constexpr int USLOT = 2 * PAIR;      // one ring slot
-constexpr int RING = 5;
+constexpr int RING = 6;
 // three warpgroups: {producer, MMA, two idle warps}, the softmax, the Q loader / epilogue
 constexpr int THREADS = 384;
 // registers per thread after the reallocation at entry (setmaxnreg): the first warpgroup gives
@@ -95,9 +95,9 @@ struct L {
     static constexpr int OFF_MREF = OFF_TMAX + 4 * H;
     static constexpr int OFF_FLAG = OFF_MREF + 4 * H;
     // per head: the softmax denominator of the item the epilogue writes
-    static constexpr int OFF_LFIN = OFF_FLAG + 32;
+    static constexpr int OFF_LFIN = OFF_FLAG + 8;
     static constexpr int OFF_BAR = OFF_LFIN + 4 * H;
-    static constexpr int N_BAR = 2 * RING + 18;
+    static constexpr int N_BAR = 2 * RING + 16;
     static_assert(2 * H * 64 * 2 == PAIR, "a query chunk fills half a ring slot");
     // the dynamic shared memory starts 1024-byte aligned (checked at entry), as
     // the 128-byte swizzle atoms of Q, the ring and P need
@@ -108,12 +108,12 @@ struct L {
     static constexpr int T_COLS = 512;
     static_assert(T_O + DB * H <= T_COLS, "tensor memory");
     static_assert(SMEM <= 232448, "shared memory");
-    static_assert(DB <= 4, "one output-free barrier per d-block");
+    static_assert(DB <= 4, "one output-free barrier per pair of d-blocks");
 };
 
 // barrier indices
 enum { B_FULL = 0, B_EMPTY = RING, B_QREADY0 = 2 * RING, B_QREADY1, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1, B_PFULL,
-       B_PVDONE, B_OFREE0, B_OFREE1, B_OFREE2, B_OFREE3, B_SOFT, B_DRAIN, B_QFREE0, B_QFREE1, B_LREADY, B_PBAR };
+       B_PVDONE, B_OFREE0, B_OFREE1, B_SOFT, B_DRAIN, B_QFREE0, B_QFREE1, B_LREADY, B_PBAR };
 
 struct TcAttnParams {
     float *out;
@@ -471,7 +471,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
     uint32_t *tmax = reinterpret_cast<uint32_t *>(sm + Lay::OFF_TMAX);
     float *alpha_s = reinterpret_cast<float *>(sm + Lay::OFF_TMAX);
     float *mref_s = reinterpret_cast<float *>(sm + Lay::OFF_MREF);
-    volatile int *flags = reinterpret_cast<volatile int *>(sm + Lay::OFF_FLAG);
+    volatile uint8_t *flags = reinterpret_cast<volatile uint8_t *>(sm + Lay::OFF_FLAG);
     float *lfin = reinterpret_cast<float *>(sm + Lay::OFF_LFIN);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
@@ -489,7 +489,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         mbar_init(bar(B_SFREE1), 128);
         mbar_init(bar(B_PFULL), 128);
         mbar_init(bar(B_PVDONE), 1);
-        for (int j = 0; j < 4; j++) mbar_init(bar(B_OFREE0 + j), 128);
+        for (int j = 0; j < 2; j++) mbar_init(bar(B_OFREE0 + j), 128);
         mbar_init(bar(B_SOFT), 128);
         mbar_init(bar(B_DRAIN), 1);
         mbar_init(bar(B_QFREE0), 1);
@@ -800,8 +800,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         // waits per d-block until the epilogue has read the previous item's block
         auto do_pv = [&](int i, bool first) -> bool {
             for (int j = 0; j < Lay::DB; j++) {
-                if (first && tok > 0) {
-                    if (!mbar_wait(bar(B_OFREE0 + j), (tok - 1) & 1, abort)) return false;
+                if (first && tok > 0 && (j & 1) == 0) {
+                    if (!mbar_wait(bar(B_OFREE0 + (j >> 1)), (tok - 1) & 1, abort)) return false;
                     fence_after();
                 }
                 const uint32_t d_o = tmem + Lay::T_O + j * H;
@@ -1089,7 +1089,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                 float v[H];
                 tmem_load<H>(lane_base + Lay::T_O + j * H, v);
                 fence_before();
-                mbar_arrive(bar(B_OFREE0 + j));
+                if ((j & 1) || j == Lay::DB - 1) mbar_arrive(bar(B_OFREE0 + (j >> 1)));
 #pragma unroll
                 for (int h = 0; h < H; h++) __stcs(dst + (size_t)h * D + 128 * j, v[h] * inv[h]);
             }
