@@ -1109,30 +1109,44 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
 // Prefill: row u <-> position pos0 - 128 + u (zeros before position 0), rows
 // 0 .. 127 from the ring, the rest from raw_new.  Decode: sequence b owns rows
 // 128b .. 128b+127 = its ring slots, with slot pos_b % 128 replaced by raw_new[b].
+constexpr int SPLIT_ROWS = 4;             // mirror rows per block of raw_split_kernel
+
 __global__ void raw_split_kernel(uint16_t *__restrict__ mirror, const float *__restrict__ ring,
                                  const float *__restrict__ raw_new, int D, int n_seq, int n_tok, uint64_t pos0,
-                                 DecodePos dp) {
+                                 DecodePos dp, int n_rows) {
     pdl_wait();
     pdl_launch_dependents();
-    const int u = blockIdx.x;
-    const float *src = nullptr;
-    if (n_seq == 1) {
-        const int64_t pos = (int64_t)pos0 - ROWS + u;
-        if (pos >= 0) src = (pos < (int64_t)pos0) ? ring + (size_t)(pos % ROWS) * D : raw_new + (size_t)(pos - (int64_t)pos0) * D;
-    } else {
+    // the source row of mirror row u (null: zeros)
+    auto source = [&](int u) -> const float * {
+        if (n_seq == 1) {
+            const int64_t pos = (int64_t)pos0 - ROWS + u;
+            if (pos < 0) return nullptr;
+            return (pos < (int64_t)pos0) ? ring + (size_t)(pos % ROWS) * D : raw_new + (size_t)(pos - (int64_t)pos0) * D;
+        }
         const int b = u / ROWS, slot = u % ROWS;
         const uint64_t pos = dp.pos[b];
-        src = ((uint64_t)slot == pos % ROWS) ? raw_new + (size_t)b * D : ring + ((size_t)b * ROWS + slot) * D;
-        if (pos < ROWS && (uint64_t)slot > pos) src = nullptr;      // slot not written yet
-    }
-    uint16_t *hi = mirror + (size_t)u * 2 * D;
-    uint16_t *lo = hi + D;
+        if (pos < ROWS && (uint64_t)slot > pos) return nullptr;      // slot not written yet
+        return ((uint64_t)slot == pos % ROWS) ? raw_new + (size_t)b * D : ring + ((size_t)b * ROWS + slot) * D;
+    };
+    const int u0 = blockIdx.x * SPLIT_ROWS;
     for (int j = threadIdx.x * 4; j < D; j += blockDim.x * 4) {
-        float4 v = src ? *reinterpret_cast<const float4 *>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-        float a[4] = {v.x, v.y, v.z, v.w}, h[4], l[4];
-        for (int e = 0; e < 4; e++) split_bf16(a[e], h[e], l[e]);
-        *reinterpret_cast<uint2 *>(hi + j) = make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
-        *reinterpret_cast<uint2 *>(lo + j) = make_uint2(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]));
+        float4 v[SPLIT_ROWS];
+#pragma unroll
+        for (int r = 0; r < SPLIT_ROWS; r++) {           // every row's load before the first store
+            const float *src = (u0 + r < n_rows) ? source(u0 + r) : nullptr;
+            v[r] = src ? *reinterpret_cast<const float4 *>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int r = 0; r < SPLIT_ROWS; r++) {
+            if (u0 + r >= n_rows) break;
+            uint16_t *hi = mirror + (size_t)(u0 + r) * 2 * D;
+            uint16_t *lo = hi + D;
+            const float a4[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+            float h[4], l[4];
+            for (int e = 0; e < 4; e++) split_bf16(a4[e], h[e], l[e]);
+            *reinterpret_cast<uint2 *>(hi + j) = make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
+            *reinterpret_cast<uint2 *>(lo + j) = make_uint2(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]));
+        }
     }
 }
 
@@ -1279,8 +1293,8 @@ cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *dp, cudaSt
     DecodePos dd{};
     if (a.n_seq > 1) dd = *dp;
     const int raw_rows = (a.n_seq == 1) ? ROWS + a.n_tok : a.n_seq * ROWS;
-    cudaError_t e = launch_pdl(raw_split_kernel, dim3(raw_rows), dim3(128), 0, s, a.raw_mirror, a.ring, a.raw_new, a.D,
-                               a.n_seq, a.n_tok, a.pos0, dd);
+    cudaError_t e = launch_pdl(raw_split_kernel, dim3((raw_rows + SPLIT_ROWS - 1) / SPLIT_ROWS), dim3(128), 0, s,
+                               a.raw_mirror, a.ring, a.raw_new, a.D, a.n_seq, a.n_tok, a.pos0, dd, raw_rows);
     if (e != cudaSuccess) return e;
     TcAttnParams p{};
     p.out = a.out;
