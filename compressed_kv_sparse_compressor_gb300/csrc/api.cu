@@ -69,6 +69,8 @@ int proj_width(const ds4c_layer_cfg &c, bool attn) { return coff_of(c) * lane_wi
 //           over `parts` work items: [n_seq*parts][H][D] + [n_seq*parts][2][H] float
 //   gemm:   decode steps of bf16 layers with at most 128 sequences: split-K
 //           partials of the projections, [kSplitK][rows][P] float
+//   tail:   prefill of bf16 layers: the projection's last-round tiles split
+//           along K, one 128 x 256 float partial per SM
 //   qheads: ratio-4 layers with indexer heads and the round trip: the heads'
 //           query vectors after it, [rows][idx_heads][idx_head_dim] float
 constexpr int kSplitK = 16;
@@ -79,6 +81,7 @@ struct WsLayout {
     size_t qsplit_off;
     size_t part_o_off, part_ml_off;
     size_t gemm_part_off;            // 0: no split-K region
+    size_t gemm_tail_off;            // 0: no tail region
     size_t qheads_off;               // 0: no region
     int parts;
     size_t total;
@@ -116,6 +119,10 @@ WsLayout ws_layout(const ds4c_layer_cfg &c, uint32_t rows, uint64_t mirror_rows,
     if (decode && c.dtype == DS4C_BF16 && P > 0 && rows <= 128) {
         L.gemm_part_off = o;
         o += align_up(sizeof(float) * (size_t)kSplitK * rows * P, 256);
+    }
+    if (!decode && c.dtype == DS4C_BF16 && P > 0) {
+        L.gemm_tail_off = o;
+        o += align_up(sizeof(float) * gemm_tail_floats(), 256);
     }
     if (c.ratio == 4 && c.idx_heads > 0 && c.idx_qat) {
         L.qheads_off = o;
@@ -176,6 +183,7 @@ ds4c_status run_compress(const ds4c_layer_cfg *cfg, const ds4c_lane_weights *aw,
         g.part_ld = (int64_t)L.proj_ld;
         g.max_ksplit = kSplitK;
     }
+    if (L.gemm_tail_off != 0) g.tail_buf = reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + L.gemm_tail_off);
     cudaError_t e = cudaErrorNotSupported;
     if (c.dtype == DS4C_BF16) e = launch_gemm_tc(g, stream);
     if (e == cudaErrorNotSupported) e = launch_gemm_simt(g, stream);

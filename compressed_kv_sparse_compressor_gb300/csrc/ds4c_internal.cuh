@@ -167,7 +167,12 @@ struct GemmArgs {
     float *part = nullptr;
     int64_t part_ld = 0;
     int max_ksplit = 1;
+    // Optional (tensor-core path, no split-K): room for gemm_tail_floats() floats, where the
+    // output tiles of a last, partly filled round over the SMs are computed split along K
+    float *tail_buf = nullptr;
 };
+// Floats of the GEMM's tail buffer (one 128 x 256 fp32 tile per SM).
+size_t gemm_tail_floats();
 cudaError_t launch_gemm_simt(const GemmArgs &a, cudaStream_t s);
 // tcgen05 path for bf16 operands; returns cudaErrorNotSupported when the
 // shape is outside what it handles (the caller then uses the SIMT kernel).

@@ -60,6 +60,11 @@ struct TcParams {
     int m_tiles;
     int n_groups;
     int ksplit;            // K ranges per output tile (1: whole K)
+    // the last partial round's output tiles split along K (ksplit == 1 only): work units
+    // past full_units are (tail tile t, part ks) partials of output tile full_units + t,
+    // written densely [BM][BN] to tail_buf + (t * tail_split + ks) * BM * BN
+    int full_units, tail_split;
+    float *tail_buf;
     int a_rows;            // rows of the A box (BM, or fewer when M is small: the MMA rows past them are unused)
     int tile_start[5];     // prefix sums of tiles per group (ksplit tiles per output tile)
     int n_tiles[4];
@@ -187,10 +192,23 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void tile_coords(const TcParams &p, int tile, int &g, int &mt, int &nt, int &ks) {
+// Work unit -> group, m-tile, n-tile, K-split index and K-split count of its range.
+__device__ __forceinline__ void tile_coords(const TcParams &p, int unit, int &g, int &mt, int &nt, int &ks, int &nsplit) {
+    int tile = unit;
+    nsplit = p.ksplit;
+    if (p.tail_split > 1 && unit >= p.full_units) {
+        tile = p.full_units + (unit - p.full_units) / p.tail_split;
+        nsplit = p.tail_split;
+    }
     g = 0;
     while (g + 1 < p.n_groups && tile >= p.tile_start[g + 1]) g++;
     const int local = tile - p.tile_start[g];
+    if (nsplit == p.tail_split && p.tail_split > 1) {
+        ks = (unit - p.full_units) % p.tail_split;
+        nt = local / p.m_tiles;
+        mt = local % p.m_tiles;
+        return;
+    }
     ks = local % p.ksplit;
     const int o = local / p.ksplit;
     nt = o / p.m_tiles;
@@ -213,9 +231,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int total = p.tile_start[p.n_groups];
+    const int total = p.tail_split > 1 ? p.full_units + (p.tile_start[p.n_groups] - p.full_units) * p.tail_split
+                                       : p.tile_start[p.n_groups];
     const int kb_count = (p.K + BK - 1) / BK;
-    const int kb_per = (kb_count + p.ksplit - 1) / p.ksplit;
+    auto k_range = [&](int ks, int nsplit, int &kb0, int &kb1) {
+        const int per = (kb_count + nsplit - 1) / nsplit;
+        kb0 = ks * per;
+        kb1 = min(kb_count, kb0 + per);
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; s++) {
@@ -250,10 +273,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
             uint32_t it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                int g, mt, nt, ks;
-                tile_coords(p, tile, g, mt, nt, ks);
+                int g, mt, nt, ks, nsplit, kb0, kb1;
+                tile_coords(p, tile, g, mt, nt, ks, nsplit);
+                k_range(ks, nsplit, kb0, kb1);
                 const CUtensorMap *mb = g == 0 ? &mapB0 : g == 1 ? &mapB1 : g == 2 ? &mapB2 : &mapB3;
-                const int kb0 = ks * kb_per, kb1 = min(kb_count, kb0 + kb_per);
                 for (int kb = kb0; kb < kb1; kb++, it++) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
@@ -282,9 +305,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
                 if (!mbar_wait(smem_u32(&acc_empty[acc]), aph ^ 1, abort)) break;
                 fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                int g_, mt_, nt_, ks_;
-                tile_coords(p, tile, g_, mt_, nt_, ks_);
-                const int kb0 = ks_ * kb_per, kb1 = min(kb_count, kb0 + kb_per);
+                int g_, mt_, nt_, ks_, ns_, kb0, kb1;
+                tile_coords(p, tile, g_, mt_, nt_, ks_, ns_);
+                k_range(ks_, ns_, kb0, kb1);
                 for (int kb = kb0; kb < kb1; kb++, it++) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
@@ -311,12 +334,29 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
         const int row = quarter * 32 + lane;
         uint32_t local = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, local++) {
-            int g, mt, nt, ks;
-            tile_coords(p, tile, g, mt, nt, ks);
+            int g, mt, nt, ks, nsplit;
+            tile_coords(p, tile, g, mt, nt, ks, nsplit);
             const int acc = local & 1;
             const uint32_t aph = (local >> 1) & 1;
             if (!mbar_wait(smem_u32(&acc_full[acc]), aph, abort)) break;
             fence_after();
+            if (p.tail_split > 1 && tile >= p.full_units) {
+                // a tail partial: the whole dense [BM][BN] block, bounds applied by the reduce
+                float *trow = p.tail_buf + ((size_t)(tile - p.full_units) * BM + row) * BN;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; c++) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c * 32), r);
+#pragma unroll
+                    for (int v = 0; v < 8; v++)
+                        *reinterpret_cast<float4 *>(trow + c * 32 + 4 * v) =
+                            make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                        __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                }
+                fence_before();
+                mbar_arrive(smem_u32(&acc_empty[acc]));
+                continue;
+            }
             const int m = mt * BM + row;
             const int n0 = nt * BN;
             float *crow = p.C[g] + (size_t)ks * p.part_stride + (size_t)m * p.ldc[g];
@@ -385,6 +425,40 @@ int sm_count() {
     return n;
 }
 
+// The tail tiles' outputs: C = sum over the parts of each tile's dense partials, in part
+// order.  One block per (tail tile, group of 8 rows); out-of-range rows and columns are
+// dropped.
+template <int BN>
+__global__ void __launch_bounds__(256) tail_reduce_kernel(const float *__restrict__ tail_buf, TcParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int t = blockIdx.x / (BM / 8);
+    const int r0 = (blockIdx.x % (BM / 8)) * 8;
+    const int tile = p.full_units + t;
+    int g = 0;
+    while (g + 1 < p.n_groups && tile >= p.tile_start[g + 1]) g++;
+    const int local = tile - p.tile_start[g];
+    const int nt = local / p.m_tiles, mt = local % p.m_tiles;
+    for (int e = threadIdx.x; e < 8 * BN / 4; e += blockDim.x) {
+        const int r = r0 + e / (BN / 4), c = (e % (BN / 4)) * 4;
+        const int m = mt * BM + r, n = nt * BN + c;
+        const float *src = tail_buf + ((size_t)t * p.tail_split * BM + r) * BN + c;
+        float4 acc = *reinterpret_cast<const float4 *>(src);
+        for (int k = 1; k < p.tail_split; k++) {
+            const float4 v = *reinterpret_cast<const float4 *>(src + (size_t)k * BM * BN);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        if (m >= p.M || n >= p.N[g]) continue;
+        float *dst = p.C[g] + (size_t)m * p.ldc[g] + n;
+        if (n + 4 <= p.N[g]) {
+            *reinterpret_cast<float4 *>(dst) = acc;
+        } else {
+            const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+            for (int v = 0; v < 4 && n + v < p.N[g]; v++) dst[v] = a4[v];
+        }
+    }
+}
+
 // Sum of the split-K partials, in split order: C[m][n] = sum_k part[k][m][n]
 // over the whole [M][ldc] block the groups write into.
 __global__ void splitk_reduce_kernel(float *__restrict__ C, const float *__restrict__ part, int64_t n4, int64_t stride,
@@ -434,6 +508,7 @@ cudaError_t launch_bn(const GemmArgs &a, cudaStream_t s) {
     }
     p.ksplit = ksplit;
     p.part_stride = (int64_t)a.M * a.part_ld;
+    p.tail_split = 1;
     CUtensorMap mA, mB[4];
     // small M: a box of the rows present (multiple of 8), not of the whole MMA tile
     p.a_rows = a.M >= BM ? BM : ((a.M + 7) / 8) * 8;
@@ -456,11 +531,34 @@ cudaError_t launch_bn(const GemmArgs &a, cudaStream_t s) {
         }
     }
     p.tile_start[a.n_groups] = start;
+    p.full_units = start;
+    // a last round that fills at most half the SMs: its tiles split along K over the SMs
+    // (every part at least 4 k-blocks, none empty), partials summed by tail_reduce_kernel
+    if (ksplit == 1 && a.tail_buf && BN == 256) {
+        const int sms = sm_count();
+        const int rounds = (start + sms - 1) / sms;
+        const int tail = start - (rounds - 1) * sms;
+        const int kb_count = (a.K + BK - 1) / BK;
+        if (rounds >= 2 && 2 * tail <= sms) {
+            int split = sms / tail;
+            if (split > kb_count / 4) split = kb_count / 4;
+            while (split >= 2 && (split - 1) * ((kb_count + split - 1) / split) >= kb_count) split--;
+            if (split >= 2) {
+                p.full_units = start - tail;
+                p.tail_split = split;
+                p.tail_buf = a.tail_buf;
+            }
+        }
+    }
     if (p.a_rows > AR) return cudaErrorInvalidValue;
     cudaError_t e = ensure_dyn_smem(gemm_tc_kernel<BN, AR>, G::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int grid = start < sm_count() ? start : sm_count();
+    const int units = p.tail_split > 1 ? p.full_units + (start - p.full_units) * p.tail_split : start;
+    const int grid = units < sm_count() ? units : sm_count();
     e = launch_pdl(gemm_tc_kernel<BN, AR>, dim3(grid), dim3(THREADS), G::SMEM_BYTES, s, mA, mB[0], mB[1], mB[2], mB[3], p);
+    if (e == cudaSuccess && p.tail_split > 1)
+        return launch_pdl(tail_reduce_kernel<BN>, dim3((unsigned)((start - p.full_units) * (BM / 8))), dim3(256), 0, s,
+                          (const float *)p.tail_buf, p);
     if (e != cudaSuccess || ksplit == 1) return e;
     const int64_t n4 = (int64_t)a.M * a.part_ld / 4;
     return launch_pdl(splitk_reduce_kernel, dim3((unsigned)((n4 + 255) / 256)), dim3(256), 0, s, a.c_base,
@@ -468,6 +566,8 @@ cudaError_t launch_bn(const GemmArgs &a, cudaStream_t s) {
 }
 
 }  // namespace
+
+size_t gemm_tail_floats() { return (size_t)sm_count() * BM * 256; }
 
 cudaError_t launch_gemm_tc(const GemmArgs &a, cudaStream_t s) {
     if (a.dtype != DS4C_BF16 || a.M < 1 || a.K % 8 != 0 || a.n_groups < 1 || a.n_groups > 4)

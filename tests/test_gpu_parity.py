@@ -154,7 +154,8 @@ def test_decode_small(ratio, base):
     lens = [base + b for b in range(B)]
     cap = max(lens) // max(ratio, 1) + 2
     icap = max(lens) // 4 + 2
-    dl, wa, wi = device_layer(shape, comp_cap=cap, idx_cap=icap, n_seq=B, seed=seed, max_rows=128)
+    # the state is built by one prefill per sequence of up to max(lens) tokens
+    dl, wa, wi = device_layer(shape, comp_cap=cap, idx_cap=icap, n_seq=B, seed=seed, max_rows=max(lens))
     for b in range(B):
         view = dl.seq_view(b)
         saved = dl.state
