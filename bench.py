@@ -200,9 +200,10 @@ class Prefill:
             self.events = ev
 
     def launches_per_step(self):
-        # state init: 5 fills; per chunk: GEMM 1, fused compressor 1 (both lanes, pool and frontier),
-        # score 1, top-k 1, raw mirror 1, attention 1, ring 1; then the gather
-        return 5 + 7 * self.n_chunks + 1
+        # state init: 5 fills; per chunk: GEMM 1 and its tail reduce 1 (a 4096-row chunk's 320 output
+        # tiles leave a partly filled last round on the SMs), fused compressor 1 (both lanes, pool and
+        # frontier), score 1, top-k 1, raw mirror 1, attention 1, ring 1; then the gather
+        return 5 + 8 * self.n_chunks + 1
 
     def breakdown(self):
         """Per-call device time (ms) of the last timed step."""
