@@ -617,8 +617,32 @@ __global__ void __launch_bounds__(T) topk_kernel(IndexerArgs a, DecodePos dp, in
     for (int i = tid; i < W; i += T) eqm[i] = 0;
     if (tid == 0) sh_nc = 0;
     __syncthreads();
-    // 1. histogram of the top 12 key bits (resident: the keys land in shared memory)
+    // 1. histogram of the top 12 key bits (resident: the keys land in shared memory).  A row
+    //    of the workspace (16-byte aligned, a multiple of 4 floats long) is read four scores
+    //    per load; its floats past V exist and are skipped.
     constexpr int SH1 = 32 - TK_HBITS;
+    constexpr int U4 = TK_UNR / 4;
+    const bool vec4 = !RESIDENT && (a.lds & 3) == 0 && (reinterpret_cast<uintptr_t>(s) & 15u) == 0;
+    const float4 *s4 = reinterpret_cast<const float4 *>(s);
+    const int V4 = (V + 3) / 4;
+    if (vec4) {
+        for (int base = 0; base < V4; base += T * U4) {
+            float4 v[U4];
+#pragma unroll
+            for (int u = 0; u < U4; u++) {
+                const int i4 = base + u * T + tid;
+                v[u] = (i4 < V4) ? __ldg(s4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < U4; u++) {
+                const int i4 = base + u * T + tid;
+                const float e4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; e++)
+                    if (4 * i4 + e < V) atomicAdd(&bins[order_key(e4[e]) >> SH1], 1u);
+            }
+        }
+    } else
     for (int base = 0; base < V; base += T * TK_UNR) {
         float v[TK_UNR];
 #pragma unroll
@@ -647,7 +671,46 @@ __global__ void __launch_bounds__(T) topk_kernel(IndexerArgs a, DecodePos dp, in
         return;
     }
     // 2. rows above b* are selected, rows in b* become candidates; a warp's 32
-    //    rows are consecutive and 32-aligned, so its ballot is one bitmap word
+    //    rows are consecutive and 32-aligned, so its ballot is one bitmap word (four-score
+    //    loads: a warp covers 128 rows, each lane a nibble of one of four words, which eight
+    //    lanes OR together)
+    if (vec4) {
+        for (int base = 0; base < V4; base += T * U4) {
+            float4 v[U4];
+#pragma unroll
+            for (int u = 0; u < U4; u++) {
+                const int i4 = base + u * T + tid;
+                v[u] = (i4 < V4) ? __ldcs(s4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < U4; u++) {
+                const int g0 = base + u * T + warp * 32;     // the warp's first group of four rows
+                if (4 * g0 >= V) continue;                   // the whole warp is past the end
+                const int i4 = g0 + lane;
+                const float e4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                uint32_t nib = 0;
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const int r = 4 * i4 + e;
+                    if (r >= V) continue;
+                    const uint32_t key = order_key(e4[e]);
+                    const uint32_t b = key >> SH1;
+                    if (b > bstar) nib |= 1u << e;
+                    else if (b == bstar) {
+                        const uint32_t o = atomicAdd(&sh_nc, 1u);
+                        ckey[o] = key;
+                        crow[o] = (uint32_t)r;
+                    }
+                }
+                uint32_t x = nib << (4 * (lane & 7));
+                x |= __shfl_xor_sync(0xffffffffu, x, 1);
+                x |= __shfl_xor_sync(0xffffffffu, x, 2);
+                x |= __shfl_xor_sync(0xffffffffu, x, 4);
+                const int w = g0 / 8 + lane / 8;
+                if ((lane & 7) == 0 && w < W) sel[w] = x;
+            }
+        }
+    } else
     for (int base = 0; base < V; base += T * TK_UNR) {
         uint32_t kv[TK_UNR];
 #pragma unroll
