@@ -19,7 +19,8 @@ def _gpu():
 
 @pytest.mark.parametrize("dtype,d_model,T,D,d", [
     ("bf16", 512, 300, 512, 128),      # ragged M, 2 n-tiles per kv matrix
-    ("bf16", 4096, 4096, 512, 128),    # full chunk of the long-context layer
+    ("bf16", 4096, 4096, 512, 128),    # full chunk of the long-context layer (last 16 tiles split in 8 along K)
+    ("bf16", 4096, 2000, 512, 128),    # 160 tiles: the last 8 split in 16 along K, ragged last m-tile
     ("bf16", 4096, 64, 512, 128),      # narrow-tile tensor-core path
     ("bf16", 4096, 32, 512, 128),      # decode batch of 32 sequences
     ("bf16", 512, 1, 512, 128),        # a single row
