@@ -117,15 +117,16 @@ enum { B_FULL = 0, B_EMPTY = RING, B_QREADY0 = 2 * RING, B_QREADY1, B_SFULL0, B_
 
 struct TcAttnParams {
     float *out;
-    const float *q;
+    const float *q;                  // [n_q][nh][D]
+    int nh;                          // the layer's query heads (<= H: the kernel runs H, the rest padded)
     uint16_t *qsplit;                // per CTA two buffers [D/64][2H][64] bf16 of split queries
     const int32_t *topk;
     const uint16_t *comp_split;      // [rows][2][D]
     int n_q, n_seq, n_tok, k, ratio, comp_cap;
     int nope_chunks, nope_blocks;    // 64-wide chunks / 128-wide blocks inside the FP8 dims
     int parts;                       // work items per query (1: whole query; >1: split rows, partial outputs)
-    float *part_o;                   // [n_q * parts][H][D] unnormalised partial outputs
-    float *part_ml;                  // [n_q * parts][2][H] reference max (log2) and denominator
+    float *part_o;                   // [n_q * parts][nh][D] unnormalised partial outputs
+    float *part_ml;                  // [n_q * parts][2][nh] reference max (log2) and denominator
     float scale_log2;
     uint64_t pos0;
     DecodePos dp;
@@ -892,9 +893,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             const Item itm = item_tiles(p, it, 1 + (nc + ROWS - 1) / ROWS);
             if (itm.tb >= itm.te) {
                 // empty part: no rows, zero weight in the combine
-                if (tid < H) {
-                    p.part_ml[(size_t)it * 2 * H + tid] = -INFINITY;
-                    p.part_ml[(size_t)it * 2 * H + H + tid] = 0.f;
+                if (tid < p.nh) {
+                    p.part_ml[(size_t)it * 2 * p.nh + tid] = -INFINITY;
+                    p.part_ml[(size_t)it * 2 * p.nh + p.nh + tid] = 0.f;
                 }
                 continue;
             }
@@ -1010,9 +1011,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                         const float l = lfin[tid] + lb[tid];
                         lfin[tid] = l;
                         // split rows: this part's reference maximum and denominator
-                        if (p.parts > 1) {
-                            p.part_ml[(size_t)it * 2 * H + tid] = mref_s[tid];
-                            p.part_ml[(size_t)it * 2 * H + H + tid] = l;
+                        if (p.parts > 1 && tid < p.nh) {
+                            p.part_ml[(size_t)it * 2 * p.nh + tid] = mref_s[tid];
+                            p.part_ml[(size_t)it * 2 * p.nh + p.nh + tid] = l;
                         }
                     }
                     mbar_arrive(bar(B_LREADY));
@@ -1033,14 +1034,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         // `buf` as D/64 query chunks [2H][64] (rows 0 .. H-1 hi, H .. 2H-1 lo), which the
         // producer loads by TMA into the 128-byte-swizzled K-major operand layout
         auto prepare = [&](int item, int buf) {
-            const float4 *src = reinterpret_cast<const float4 *>(p.q + (size_t)(item / p.parts) * H * D);
+            // heads past the layer's (nh < H) get zero query rows: their logits are 0 and their
+            // outputs are not stored
+            const float4 *src = reinterpret_cast<const float4 *>(p.q + (size_t)(item / p.parts) * p.nh * D);
+            const int nf_real = p.nh * (D / 4);
             uint16_t *qd = p.qsplit + ((size_t)blockIdx.x * 2 + buf) * Lay::DC * 2 * H * 64;
             constexpr int NF = H * D / 4 / 128;           // float4 per thread
             static_assert(NF % 8 == 0, "whole batches of eight loads");
             for (int j0 = 0; j0 < NF; j0 += 8) {
                 float4 v[8];
 #pragma unroll
-                for (int u = 0; u < 8; u++) v[u] = __ldcs(src + tid + 128 * (j0 + u));
+                for (int u = 0; u < 8; u++) {
+                    const int f = tid + 128 * (j0 + u);
+                    v[u] = f < nf_real ? __ldcs(src + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
 #pragma unroll
                 for (int u = 0; u < 8; u++) {
                     const int f = tid + 128 * (j0 + u);
@@ -1084,14 +1091,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             float inv[H];
 #pragma unroll
             for (int h = 0; h < H; h++) inv[h] = whole ? 1.0f / lfin[h] : 1.0f;
-            float *dst = (whole ? p.out : p.part_o) + (size_t)it * H * D + r;
+            float *dst = (whole ? p.out : p.part_o) + (size_t)it * p.nh * D + r;
             for (int j = 0; j < Lay::DB; j++) {
                 float v[H];
                 tmem_load<H>(lane_base + Lay::T_O + j * H, v);
                 fence_before();
                 if ((j & 1) || j == Lay::DB - 1) mbar_arrive(bar(B_OFREE0 + (j >> 1)));
 #pragma unroll
-                for (int h = 0; h < H; h++) __stcs(dst + (size_t)h * D + 128 * j, v[h] * inv[h]);
+                for (int h = 0; h < H; h++)
+                    if (h < p.nh) __stcs(dst + (size_t)h * D + 128 * j, v[h] * inv[h]);
             }
             g += nt;
             tok++;
@@ -1262,14 +1270,17 @@ cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, cudaStream_t s
     if (4 * 32 * (REG_LOW + REG_SOFT + REG_AUX) > THREADS * regs) return cudaErrorNotSupported;
     e = launch_pdl(attn_tc_kernel<H, D>, dim3(grid), dim3(THREADS), Lay::SMEM, s, rh, rl, qm, p);
     if (e != cudaSuccess || p.parts == 1) return e;
-    return launch_pdl(attn_combine_kernel, dim3(a.n_seq * a.n_tok * H), dim3(128), 0, s, a.out,
-                      (const float *)p.part_o, (const float *)p.part_ml, H, D, p.parts,
+    return launch_pdl(attn_combine_kernel, dim3(a.n_seq * a.n_tok * a.H), dim3(128), 0, s, a.out,
+                      (const float *)p.part_o, (const float *)p.part_ml, a.H, D, p.parts,
                       a.commit_ring ? const_cast<float *>(a.ring) : nullptr, a.raw_new, p.dp);
 }
 
 }  // namespace
 
-size_t attn_tc_qsplit_bytes(int H, int D) { return (size_t)sm_count() * 2 * 2 * H * D * sizeof(uint16_t); }
+size_t attn_tc_qsplit_bytes(int H, int D) {
+    (void)H;                                           // the kernel always runs 64 heads
+    return (size_t)sm_count() * 2 * 2 * 64 * D * sizeof(uint16_t);
+}
 
 int attn_tc_decode_parts(int ratio, int k, int comp_cap) {
     // about two tiles per work item: each item loads its query's Q and writes one
@@ -1282,7 +1293,9 @@ int attn_tc_decode_parts(int ratio, int k, int comp_cap) {
 }
 
 bool attn_tc_supported(int H, int D, int S, int ratio, int k) {
-    const bool hd = H == 64 && (D == 512 || D == 256 || D == 128);
+    // up to 64 query heads (fewer are padded to 64: the S product's N = 2H and the output
+    // accumulator's H columns per d-block fill the 512 TMEM columns at 64)
+    const bool hd = H >= 1 && H <= 64 && (D == 512 || D == 256 || D == 128);
     return hd && S == ROWS && (ratio == 0 || ratio == 4 || ratio == 128) && (ratio != 4 || k <= MAX_LIST);
 }
 
@@ -1299,6 +1312,7 @@ cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *dp, cudaSt
     TcAttnParams p{};
     p.out = a.out;
     p.q = a.q;
+    p.nh = a.H;
     p.qsplit = a.qsplit;
     p.topk = a.topk;
     p.comp_split = a.comp_split;
@@ -1317,7 +1331,7 @@ cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *dp, cudaSt
     p.pos0 = a.pos0;
     p.dp = dd;
 #define DS4C_HD(h, d) \
-    if (a.H == h && a.D == d) return launch_hd<h, d>(a, p, s);
+    if (a.H <= h && a.D == d) return launch_hd<h, d>(a, p, s);
     DS4C_HD(64, 512)
     DS4C_HD(64, 256)
     DS4C_HD(64, 128)

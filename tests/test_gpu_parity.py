@@ -120,11 +120,12 @@ def test_c1_chain_against_oracle_end_to_end():
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("ratio,heads,D", [(0, 64, 512), (4, 64, 512), (128, 64, 512), (4, 32, 512),
-                                           (4, 64, 128), (4, 64, 256), (128, 64, 256)])
+                                           (4, 64, 128), (4, 64, 256), (128, 64, 256), (128, 8, 256),
+                                           (0, 16, 128), (4, 128, 128), (0, 128, 128)])
 def test_ragged_chunks(ratio, heads, D):
-    """heads = 64: tensor-core attention (head_dim 512, 256 or 128: at 128 the one
-    128-wide d-block holds the RoPE dims, so no block is FP8-exact); heads = 32:
-    CUDA-core attention."""
+    """heads <= 64: tensor-core attention (head_dim 512, 256 or 128: at 128 the one
+    128-wide d-block holds the RoPE dims, so no block is FP8-exact; fewer than 64
+    heads run padded to 64 with zero query rows); heads = 128: CUDA-core attention."""
     shape = configs.LayerShape(d_model=512, head_dim=D, n_rot=64, idx_head_dim=128 if D >= 256 else 64,
                                n_heads=heads, ratio=ratio, top_k=16, dtype="bf16", w_std=0.04)
     seed = 21
@@ -144,9 +145,11 @@ def test_ragged_chunks(ratio, heads, D):
 # Decode: B sequences, one token each at staggered positions
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("ratio,base", [(4, 60), (128, 380), (0, 200)])
-def test_decode_small(ratio, base):
-    shape = configs.LayerShape(d_model=512, head_dim=512, n_rot=64, idx_head_dim=128, n_heads=64, ratio=ratio,
+@pytest.mark.parametrize("ratio,base,heads", [(4, 60, 64), (128, 380, 64), (0, 200, 64), (4, 60, 8),
+                                              (128, 380, 24)])
+def test_decode_small(ratio, base, heads):
+    """heads < 64: the padded tensor-core attention, split rows combined over the real heads."""
+    shape = configs.LayerShape(d_model=512, head_dim=512, n_rot=64, idx_head_dim=128, n_heads=heads, ratio=ratio,
                                top_k=16, dtype="bf16", w_std=0.04)
     seed, B = 31, 8
     # every stagger class; ratio 4: some emit this step; ratio 128: 382 + 1 ends a window
