@@ -233,6 +233,26 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uin
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
+// The same two issued by a converged warp: every lane computes the (warp-uniform) operands and
+// only the lane with `leader` set issues, so one thread issues every MMA and every commit.
+__device__ __forceinline__ void mma_w(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc,
+                                      uint32_t leader) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 e, %5, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(id), "r"(acc), "r"(leader)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_w(uint32_t bar, uint32_t leader) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "setp.ne.b32 e, %1, 0;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+        "r"(leader)
+        : "memory");
+}
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -557,48 +577,41 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                 if (i >= nc) return dummy;
                 return p.ratio == 4 ? list[i] : dummy + i;
             };
-            // this lane's rows 16 b + lane / 2 for the four row blocks b = 2 bb + pw of this
-            // warp: every slot of a compressed tile copies from them, so their mirror
-            // addresses are formed once per tile
-            const uint16_t *rp[4];
+            // this lane's rows 8 i + 4 pw + lane / 8 (i = 0 .. 15): every slot of a compressed tile
+            // copies from them, so their mirror rows are looked up once per tile
+            int rix[16];
             int rp_tile = -1;
             auto tile_rows = [&](int tile) {
                 if (tile == rp_tile) return;
                 rp_tile = tile;
 #pragma unroll
-                for (int bb = 0; bb < 4; bb++)
-                    rp[bb] = p.comp_split + (size_t)row_of(tile, 16 * (2 * bb + pw) + (lane >> 1)) * 2 * D;
+                for (int i = 0; i < 16; i++) rix[i] = row_of(tile, 8 * i + 4 * pw + (lane >> 3));
             };
             // this warp's half of 16 KB of gathered compressed rows at dst, in the 128-byte swizzle
             // layout: (pv = false) rows 0 .. 127 of the 64-d chunk at element offset off; (pv =
             // true) rows 64 hh .. 64 hh + 63 of the 128-d block at off, as two [64][64] halves
-            // SLOT apart.  Lane pairs take the two halves of one 32-byte sector, so an
-            // instruction covers 16 rows x 32 bytes.
+            // SLOT apart.  Eight lanes copy one row's 128 bytes, so an instruction reads four
+            // whole lines.
             auto gather16 = [&](uint32_t dst, int tile, bool pv, int off, int hh) {
                 tile_rows(tile);
-                const int sw = (lane >> 1) & 7;              // row & 7 of every row this lane copies
+                const int u = lane & 7;                      // 16-byte unit of the row's 128 bytes
+                const int sw = (4 * pw + (lane >> 3)) & 7;   // row & 7 of every row this lane copies
                 if (!pv) {
 #pragma unroll
-                    for (int bb = 0; bb < 4; bb++) {
-                        const int r = 16 * (2 * bb + pw) + (lane >> 1);
-                        const uint16_t *src = rp[bb] + off;
-                        const uint32_t drow = dst + r * 128;
-#pragma unroll
-                        for (int sct = 0; sct < 4; sct++) {
-                            const int u = 2 * sct + (lane & 1);
-                            cp_async16(drow + ((u ^ sw) << 4), src + 8 * u);
-                        }
+                    for (int i = 0; i < 16; i++) {
+                        const int r = 8 * i + 4 * pw + (lane >> 3);
+                        const uint16_t *src = p.comp_split + (size_t)rix[i] * 2 * D + off + 8 * u;
+                        cp_async16(dst + r * 128 + ((u ^ sw) << 4), src);
                     }
                 } else {
 #pragma unroll
-                    for (int bb = 0; bb < 2; bb++) {
-                        const int rr = 16 * (2 * bb + pw) + (lane >> 1);
-                        const uint16_t *src0 = rp[2 * hh + bb] + off;
+                    for (int i = 0; i < 8; i++) {
+                        const int rr = 8 * i + 4 * pw + (lane >> 3);
+                        const int ri = hh ? rix[8 + i] : rix[i];
+                        const uint16_t *src = p.comp_split + (size_t)ri * 2 * D + off + 8 * u;
 #pragma unroll
-                        for (int sct = 0; sct < 8; sct++) {
-                            const int half = sct >> 2, u = 2 * (sct & 3) + (lane & 1);
-                            cp_async16(dst + half * SLOT + rr * 128 + ((u ^ sw) << 4), src0 + 64 * half + 8 * u);
-                        }
+                        for (int half = 0; half < 2; half++)
+                            cp_async16(dst + half * SLOT + rr * 128 + ((u ^ sw) << 4), src + 64 * half);
                     }
                 }
             };
@@ -736,18 +749,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         const uint32_t phi = smem_u32(sm + Lay::OFF_PHI), plo = smem_u32(sm + Lay::OFF_PLO);
         uint32_t unit = 0, g = 0, tok = 0;
         bool ok = true;
+        // The whole warp runs the issue loop (its operands stay warp-uniform); lane 0 issues.
+        const uint32_t leader = lane == 0;
+        auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(b, parity, abort)) != 0;
+        };
         // slot u of the ring: wait until loaded / hand back once its MMAs finish
         auto wait_slot = [&](uint32_t u, uint32_t &base) -> bool {
             base = smem_u32(sm + Lay::OFF_X + (u % RING) * USLOT);
-            return mbar_wait(bar(B_FULL + u % RING), (u / RING) & 1, abort);
+            return wait_all(bar(B_FULL + u % RING), (u / RING) & 1);
         };
-        auto free_slot = [&](uint32_t u) { mma_commit(bar(B_EMPTY + u % RING)); };
+        auto free_slot = [&](uint32_t u) { mma_commit_w(bar(B_EMPTY + u % RING), leader); };
         // S of global tile gt; `last`: the item's last tile, after which its query chunks are
         // no longer read.  The slots of a lo chunk pair's query chunks stay held until the
         // pair's lo product has been issued.
         auto do_qk = [&](uint32_t gt, int tile, bool last) -> bool {
             const int sb = gt & 1;
-            if (gt >= 2 && !mbar_wait(bar(B_SFREE0 + sb), ((gt >> 1) - 1) & 1, abort)) return false;
+            if (gt >= 2 && !wait_all(bar(B_SFREE0 + sb), ((gt >> 1) - 1) & 1)) return false;
             fence_after();
             const uint32_t d_t = tmem + Lay::T_S + sb * 2 * H;
             const int c0 = tile == 0 ? 0 : p.nope_chunks;
@@ -762,7 +780,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                 // against [Q_hi; Q_lo] (rows 0 .. 2H-1 of the query chunk)
                 const uint64_t q0 = DK + (b >> 4), x0 = DK + ((b + PAIR) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < 4; kk++) mma(d_t, x0 + 2 * kk, q0 + 2 * kk, ID_QK2, (c > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < 4; kk++)
+                    mma_w(d_t, x0 + 2 * kk, q0 + 2 * kk, ID_QK2, (c > 0 || kk > 0) ? 1u : 0u, leader);
                 const uint32_t mu = unit++;
                 if (c < c0) {
                     free_slot(mu);
@@ -779,12 +798,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                     {
                         const uint64_t ql = DK + (hb0 >> 4), xl = DK + (lb >> 4);
 #pragma unroll
-                        for (int kk = 0; kk < 4; kk++) mma(d_t, xl + 2 * kk, ql + 2 * kk, ID_QK, 1u);
+                        for (int kk = 0; kk < 4; kk++) mma_w(d_t, xl + 2 * kk, ql + 2 * kk, ID_QK, 1u, leader);
                     }
                     if (nheld == 2) {
                         const uint64_t ql = DK + (hb1 >> 4), xl = DK + ((lb + PAIR) >> 4);
 #pragma unroll
-                        for (int kk = 0; kk < 4; kk++) mma(d_t, xl + 2 * kk, ql + 2 * kk, ID_QK, 1u);
+                        for (int kk = 0; kk < 4; kk++) mma_w(d_t, xl + 2 * kk, ql + 2 * kk, ID_QK, 1u, leader);
                     }
                     free_slot(hu0);
                     if (nheld == 2) free_slot(hu1);
@@ -792,9 +811,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                     nheld = 0;
                 }
             }
-            mma_commit(bar(B_SFULL0 + sb));
+            mma_commit_w(bar(B_SFULL0 + sb), leader);
             // every query chunk of this item has been read: its split buffer may be refilled
-            if (last) mma_commit(bar(B_QFREE0 + (tok & 1)));
+            if (last) mma_commit_w(bar(B_QFREE0 + (tok & 1)), leader);
             return true;
         };
         // O of tile i; `first`: the item's first tile (overwrites the accumulator), which
@@ -802,7 +821,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         auto do_pv = [&](int i, bool first) -> bool {
             for (int j = 0; j < Lay::DB; j++) {
                 if (first && tok > 0 && (j & 1) == 0) {
-                    if (!mbar_wait(bar(B_OFREE0 + (j >> 1)), (tok - 1) & 1, abort)) return false;
+                    if (!wait_all(bar(B_OFREE0 + (j >> 1)), (tok - 1) & 1)) return false;
                     fence_after();
                 }
                 const uint32_t d_o = tmem + Lay::T_O + j * H;
@@ -818,8 +837,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                     const uint32_t aoff = (uint32_t)((kk >> 2) * PAIR + (kk & 3) * 2048);
                     const uint64_t ah = DA + ((xb + aoff) >> 4);
                     const uint64_t bh = DP + ((phi + kk * 2048) >> 4), bl = DP + ((plo + kk * 2048) >> 4);
-                    mma(d_o, ah, bh, ID_PV, (first && kk == 0) ? 0u : 1u);
-                    mma(d_o, ah, bl, ID_PV, 1u);
+                    mma_w(d_o, ah, bh, ID_PV, (first && kk == 0) ? 0u : 1u, leader);
+                    mma_w(d_o, ah, bl, ID_PV, 1u, leader);
                 }
                 free_slot(unit++);
                 if (has_lo) {
@@ -830,12 +849,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
 #pragma unroll
                     for (int kk = 0; kk < 8; kk++) {
                         const uint32_t aoff = (uint32_t)((kk >> 2) * PAIR + (kk & 3) * 2048);
-                        mma(d_o, DA + ((lb + aoff) >> 4), DP + ((phi + kk * 2048) >> 4), ID_PV, 1u);
+                        mma_w(d_o, DA + ((lb + aoff) >> 4), DP + ((phi + kk * 2048) >> 4), ID_PV, 1u, leader);
                     }
                     free_slot(unit++);
                 }
             }
-            mma_commit(bar(B_PVDONE));
+            mma_commit_w(bar(B_PVDONE), leader);
             return true;
         };
         const int n_items = p.n_q * p.parts;
@@ -844,18 +863,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             const int nc = comp_rows(p, k, nullptr);          // whole warp
             const Item itm = item_tiles(p, it, 1 + (nc + ROWS - 1) / ROWS);
             if (itm.tb >= itm.te) continue;
-            int good = 1;
-            if (lane == 0) {
-                good = do_qk(g, itm.tb, itm.tb == itm.te - 1) ? 1 : 0;
-                for (int i = itm.tb; i < itm.te && good; i++) {
-                    const uint32_t gi = g + (i - itm.tb);
-                    if (i + 1 < itm.te && !do_qk(gi + 1, i + 1, i + 1 == itm.te - 1)) { good = 0; break; }
-                    if (!mbar_wait(bar(B_PFULL), gi & 1, abort)) { good = 0; break; }
-                    fence_after();
-                    if (!do_pv(i, i == itm.tb)) { good = 0; break; }
-                }
+            bool good = do_qk(g, itm.tb, itm.tb == itm.te - 1);
+            for (int i = itm.tb; i < itm.te && good; i++) {
+                const uint32_t gi = g + (i - itm.tb);
+                if (i + 1 < itm.te && !do_qk(gi + 1, i + 1, i + 1 == itm.te - 1)) { good = false; break; }
+                if (!wait_all(bar(B_PFULL), gi & 1)) { good = false; break; }
+                fence_after();
+                if (!do_pv(i, i == itm.tb)) { good = false; break; }
             }
-            ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+            ok = good;
             g += itm.te - itm.tb;
             tok++;
         }
