@@ -32,7 +32,7 @@ from compressed_kv_sparse_compressor_gb300 import configs  # noqa: E402
 METRIC = "prefill tokens/s per layer"
 # dram__bytes_read.sum + dram__bytes_write.sum of one attention launch (4096 queries), from an ncu capture
 # under profiles/; None when the kernel has changed since the counters were taken
-ATTN_TRAFFIC = 556767232 + 574585600   # profiles/attn_tc_kernel_prefill_8192tok_chunk2.md
+ATTN_TRAFFIC = 556817920 + 580525312   # profiles/attn_tc_kernel_prefill_8192tok_chunk2.md
 ATTN_TRAFFIC_SRC = "ncu, one 4096-query launch of the 8192-token case (same units per launch as C5)"
 UNIT = "tokens/s"
 
