@@ -119,7 +119,9 @@ struct TcAttnParams {
     float *out;
     const float *q;                  // [n_q][nh][D]
     int nh;                          // the layer's query heads (<= H: the kernel runs H, the rest padded)
-    uint16_t *qsplit;                // per CTA two buffers [D/64][2H][64] bf16 of split queries
+    uint16_t *qsplit;                // per CTA two buffers [D/64][2H][64] bf16 of split queries, or (qpre)
+                                     // every query's [D/64][2H][64], split before the launch
+    int qpre;
     const int32_t *topk;
     const uint16_t *comp_split;      // [rows][2][D]
     int n_q, n_seq, n_tok, k, ratio, comp_cap;
@@ -222,14 +224,6 @@ __host__ __device__ constexpr uint32_t idesc(int M, int N, int a_mn, int b_mn) {
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(id), "r"(acc)
-        : "memory");
-}
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
@@ -570,7 +564,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                 if (__shfl_sync(0xffffffffu, okq, 0) == 0) { ok = false; break; }
             }
             tok++;
-            const int qrow0 = (blockIdx.x * 2 + qbuf) * Lay::DC * 2 * H;
+            const int qrow0 = (p.qpre ? it / p.parts : blockIdx.x * 2 + qbuf) * Lay::DC * 2 * H;
             const int dummy = k.seq * p.comp_cap;
             auto row_of = [&](int tile, int r) -> int {   // comp mirror row of tile >= 1, row r
                 const int i = (tile - 1) * ROWS + r;
@@ -1050,6 +1044,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         // `buf` as D/64 query chunks [2H][64] (rows 0 .. H-1 hi, H .. 2H-1 lo), which the
         // producer loads by TMA into the 128-byte-swizzled K-major operand layout
         auto prepare = [&](int item, int buf) {
+            if (p.qpre) {                                // split before the launch
+                mbar_arrive(bar(B_QREADY0 + buf));
+                return;
+            }
             // heads past the layer's (nh < H) get zero query rows: their logits are 0 and their
             // outputs are not stored
             const float4 *src = reinterpret_cast<const float4 *>(p.q + (size_t)(item / p.parts) * p.nh * D);
@@ -1137,7 +1135,38 @@ constexpr int SPLIT_ROWS = 4;             // mirror rows per block of raw_split_
 
 __global__ void raw_split_kernel(uint16_t *__restrict__ mirror, const float *__restrict__ ring,
                                  const float *__restrict__ raw_new, int D, int n_seq, int n_tok, uint64_t pos0,
-                                 DecodePos dp, int n_rows) {
+                                 DecodePos dp, int n_rows, const float *__restrict__ q, uint16_t *__restrict__ qsplit,
+                                 int nh) {
+    const int raw_blocks = (n_rows + SPLIT_ROWS - 1) / SPLIT_ROWS;
+    if ((int)blockIdx.x >= raw_blocks) {
+        // the query split (decode): one 64-d chunk c of query n per block, as the attention's
+        // query chunks [2 x 64 heads][64] bf16 (hi rows, then lo rows; heads past nh zero).  Its
+        // inputs are the call's own, so it runs before the wait for the previous kernel, which
+        // it still takes before finishing (the dependent attention waits for this grid).
+        const int DC = D / 64, qb = blockIdx.x - raw_blocks;
+        const int n = qb / DC, c = qb % DC;
+        uint16_t *qd = qsplit + ((size_t)n * DC + c) * 2 * 64 * 64;
+        float4 v[8];
+#pragma unroll
+        for (int k = 0; k < 8; k++) {                  // 64 heads x 16 float4, every load first
+            const int f = threadIdx.x + 128 * k, h = f >> 4, e = (f & 15) * 4;
+            v[k] = h < nh ? *reinterpret_cast<const float4 *>(q + ((size_t)n * nh + h) * D + 64 * c + e)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            const int f = threadIdx.x + 128 * k, h = f >> 4, e = (f & 15) * 4;
+            const float a4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+            float hh[4], ll[4];
+            for (int i = 0; i < 4; i++) split_bf16(a4[i], hh[i], ll[i]);
+            *reinterpret_cast<uint2 *>(qd + (size_t)h * 64 + e) = make_uint2(pack_bf16x2(hh[0], hh[1]), pack_bf16x2(hh[2], hh[3]));
+            *reinterpret_cast<uint2 *>(qd + (size_t)(64 + h) * 64 + e) =
+                make_uint2(pack_bf16x2(ll[0], ll[1]), pack_bf16x2(ll[2], ll[3]));
+        }
+        pdl_launch_dependents();
+        pdl_wait();
+        return;
+    }
     pdl_wait();
     pdl_launch_dependents();
     // the source row of mirror row u (null: zeros)
@@ -1271,7 +1300,8 @@ cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, cudaStream_t s
     const int grid = items < sm_count() ? items : sm_count();
     // the split queries: per CTA two buffers of D/64 chunks [2H][64] bf16, one 128-row box each
     CUtensorMap qm;
-    if (!make_map(&qm, a.qsplit, (uint64_t)grid * 2 * Lay::DC * 2 * H, 64, 128, 2 * H)) return cudaErrorNotSupported;
+    const uint64_t q_bufs = p.qpre ? (uint64_t)a.n_seq * a.n_tok : (uint64_t)grid * 2;
+    if (!make_map(&qm, a.qsplit, q_bufs * Lay::DC * 2 * H, 64, 128, 2 * H)) return cudaErrorNotSupported;
     cudaError_t e = ensure_dyn_smem(attn_tc_kernel<H, D>, Lay::SMEM);
     if (e != cudaSuccess) return e;
     // the register reallocation at entry needs the launch allocation to cover both shares
@@ -1322,19 +1352,26 @@ cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *dp, cudaSt
     DecodePos dd{};
     if (a.n_seq > 1) dd = *dp;
     const int raw_rows = (a.n_seq == 1) ? ROWS + a.n_tok : a.n_seq * ROWS;
-    cudaError_t e = launch_pdl(raw_split_kernel, dim3((raw_rows + SPLIT_ROWS - 1) / SPLIT_ROWS), dim3(128), 0, s,
-                               a.raw_mirror, a.ring, a.raw_new, a.D, a.n_seq, a.n_tok, a.pos0, dd, raw_rows);
+    // split rows (decode): the queries are split here, by many blocks, instead of by each work
+    // item's CTA on its critical path; the per-CTA query buffers hold 2 x sm_count queries
+    const int parts = a.parts > 0 ? a.parts : 1;
+    const bool qpre = parts > 1 && nq <= 2 * sm_count();
+    const int q_blocks = qpre ? nq * (a.D / 64) : 0;
+    cudaError_t e = launch_pdl(raw_split_kernel, dim3((raw_rows + SPLIT_ROWS - 1) / SPLIT_ROWS + q_blocks), dim3(128),
+                               0, s, a.raw_mirror, a.ring, a.raw_new, a.D, a.n_seq, a.n_tok, a.pos0, dd, raw_rows,
+                               a.q, a.qsplit, a.H);
     if (e != cudaSuccess) return e;
     TcAttnParams p{};
     p.out = a.out;
     p.q = a.q;
     p.nh = a.H;
     p.qsplit = a.qsplit;
+    p.qpre = qpre ? 1 : 0;
     p.topk = a.topk;
     p.comp_split = a.comp_split;
     p.nope_chunks = (a.D - a.n_rot) / 64;
     p.nope_blocks = (a.D - a.n_rot) / 128;
-    p.parts = a.parts > 0 ? a.parts : 1;
+    p.parts = parts;
     p.part_o = a.part_o;
     p.part_ml = a.part_ml;
     p.n_q = nq;
