@@ -449,8 +449,20 @@ __device__ __forceinline__ Item item_tiles(const TcAttnParams &p, int it, int n_
     Item r;
     r.n = it / p.parts;
     const int part = it % p.parts;
-    const int w = (n_tiles + p.parts - 1) / p.parts;
-    r.tb = part * w;
+    if (p.parts == 1) {
+        r.tb = 0;
+        r.te = n_tiles;
+        return r;
+    }
+    // split rows: the raw tile alone (its lo halves make it the longest), the compressed
+    // tiles spread evenly over the other parts
+    if (part == 0) {
+        r.tb = 0;
+        r.te = 1;
+        return r;
+    }
+    const int w = (n_tiles - 1 + p.parts - 2) / (p.parts - 1);
+    r.tb = 1 + (part - 1) * w;
     r.te = min(r.tb + w, n_tiles);
     return r;
 }
@@ -1329,12 +1341,12 @@ size_t attn_tc_qsplit_bytes(int H, int D) {
 }
 
 int attn_tc_decode_parts(int ratio, int k, int comp_cap) {
-    // about two tiles per work item: each item loads its query's Q and writes one
-    // partial, so halving the item count against one tile per item saves those
-    // fixed costs while a decode batch still spreads over the SMs
+    // the raw tile alone and about two compressed tiles per further work item: each item
+    // loads its query's Q and writes one partial, so halving the item count against one
+    // tile per item saves those fixed costs while a decode batch still spreads over the SMs
     const int rows = ratio == 4 ? (k < comp_cap ? k : comp_cap) : (ratio == 128 ? comp_cap : 0);
     const int tiles = 1 + (rows + ROWS - 1) / ROWS;
-    const int parts = (tiles + 1) / 2;
+    const int parts = tiles == 1 ? 1 : 1 + tiles / 2;
     return parts < 8 ? parts : 8;
 }
 
