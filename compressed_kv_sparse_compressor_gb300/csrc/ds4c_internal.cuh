@@ -59,10 +59,13 @@ cudaError_t launch_fma_probe(uint32_t blocks, uint32_t iters, float *out, cudaSt
 // Programmatic dependent launch.  Kernels launched by launch_pdl may be
 // scheduled while the previous kernel of the stream is still finishing, so
 // every such kernel calls pdl_wait() in each CTA before its first access to
-// global memory (and before any early return): it returns once the previous
-// kernel has completed and its writes are visible, which also orders every
-// earlier kernel.  pdl_launch_dependents() lets the next kernel be scheduled.
-// Under an ordinary launch both are no-ops.
+// global memory written by the previous kernel, and before it exits: it returns
+// once the previous kernel has completed and its writes are visible, which also
+// orders every earlier kernel.  pdl_launch_dependents() lets the next kernel be
+// scheduled.  Under an ordinary launch both are no-ops.  (The decode indexer
+// score reads rows older than the newest before its wait when the previous
+// kernel is the decode compressor, see PdlPrev; the split query blocks of the
+// attention's raw-row split read only the call's own inputs before theirs.)
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
@@ -130,9 +133,24 @@ __device__ __forceinline__ void indexer_qat_group(float4 &v, float c) {
     v.w = ldexpf(e2m1_rne(ldexpf(v.w, -e)), e);
 }
 
+// The last kernel launch_pdl issued on this thread: set by the decode compressor's launcher,
+// whose kernel writes nothing a decode indexer score reads but the newest compressed row of
+// each sequence; any other launch clears it.  A score launched right after it on the same
+// stream may read the older rows before waiting for it (a kernel of the caller in between
+// is an ordinary launch, which the score waits for in full).
+struct PdlPrev {
+    cudaStream_t s = nullptr;
+    bool newest_only = false;
+};
+inline PdlPrev &pdl_prev() {
+    static thread_local PdlPrev v;
+    return v;
+}
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                               Args &&...args) {
+    pdl_prev().newest_only = false;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = grid;
     cfg.blockDim = block;

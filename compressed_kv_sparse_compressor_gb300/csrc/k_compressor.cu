@@ -380,8 +380,10 @@ __global__ void commit_kernel(CompressArgs a, int lane_id, DecodePos dp, int dec
 template <int GA, int GI>
 __global__ void __launch_bounds__(128) compress_decode_r4_kernel(CompressArgs a, DecodePos dp) {
     __shared__ float red[32];
-    pdl_wait();
+    // the indexer score may start now: it scores the rows of earlier steps first and waits for
+    // this grid before the newest row and before finishing
     pdl_launch_dependents();
+    pdl_wait();
     const int seq = blockIdx.x, lane_id = blockIdx.y;
     if (lane_id == 0) pool_r4<GA>(a, 0, dp, 1, (threadIdx.x / GA == 0) ? seq : a.n_seg, red);
     else pool_r4<GI>(a, 1, dp, 1, (threadIdx.x / GI == 0) ? seq : a.n_seg, red);
@@ -491,7 +493,9 @@ cudaError_t launch_compress_decode(const CompressArgs &a, const DecodePos &p, in
         const dim3 grid((unsigned)n_seq, 2);
 #define DS4C_CDEC(A, I)                                                              \
         if (ga == A && gi == I) {                                                   \
-            return launch_pdl(compress_decode_r4_kernel<A, I>, grid, dim3(128), 0, s, a, p); \
+            const cudaError_t e = launch_pdl(compress_decode_r4_kernel<A, I>, grid, dim3(128), 0, s, a, p); \
+            if (e == cudaSuccess) pdl_prev() = PdlPrev{s, true};                      \
+            return e;                                                               \
         }
         DS4C_CDEC(128, 32)
         DS4C_CDEC(128, 16)

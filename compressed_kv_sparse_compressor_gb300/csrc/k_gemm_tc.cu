@@ -463,8 +463,10 @@ __global__ void __launch_bounds__(256) tail_reduce_kernel(const float *__restric
 // over the whole [M][ldc] block the groups write into.
 __global__ void splitk_reduce_kernel(float *__restrict__ C, const float *__restrict__ part, int64_t n4, int64_t stride,
                                      int ksplit) {
-    pdl_wait();
+    // the dependent kernel may start now (it waits for this grid before reading C); the
+    // partials are read only after the GEMM is complete
     pdl_launch_dependents();
+    pdl_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n4) return;
     float4 acc = reinterpret_cast<const float4 *>(part)[i];

@@ -229,19 +229,29 @@ __global__ void wait_selftest_kernel(unsigned long long limit_ns) {
 
 template <int DD>
 __global__ void __launch_bounds__(128) score_decode_tma_kernel(const __grid_constant__ CUtensorMap rowsMap, IndexerArgs a,
-                                                               DecodePos dp, int idx_cap) {
+                                                               DecodePos dp, int idx_cap, int early) {
     static_assert(DD % 32 == 0 && DD <= 128, "staged rows: d/32 boxes of 16 KB");
     constexpr int SEG = DD / 32;
     extern __shared__ uint8_t sm_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~(uintptr_t)1023);
     __shared__ uint64_t bar;
     __shared__ float qs[DD];
-    pdl_wait();
     pdl_launch_dependents();
     const int b = blockIdx.y;
     const uint64_t vis = (dp.pos[b] + 1) / 4;
     const int c0 = blockIdx.x * 128;
-    if ((uint64_t)c0 >= vis) return;
+    if ((uint64_t)c0 >= vis) {                          // no rows (early: as a block of old rows)
+        if (!early) pdl_wait();
+        return;
+    }
+    // early: the previous kernel is this step's decode compressor, which writes no row but the
+    // newest.  Rows before the newest visible one were then written by earlier steps: a block
+    // of only those scores them while the compressor still runs and exits without waiting.
+    // The block holding a sequence's newest row, which this step may just have emitted, waits
+    // first; every sequence with a visible row has one, so this grid still completes only
+    // after the compressor (and the kernels after it see what the compressor wrote).
+    const bool wait_first = !early || (uint64_t)c0 + 128 >= vis;
+    if (wait_first) pdl_wait();
     const uint32_t bar_a = idx_smem_u32(&bar);
     if (threadIdx.x == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_a) : "memory");
@@ -270,7 +280,7 @@ __global__ void __launch_bounds__(128) score_decode_tma_kernel(const __grid_cons
     }
     const int t = threadIdx.x;
     const int c = c0 + t;
-    if ((uint64_t)c >= vis) return;
+    if ((uint64_t)c >= vis) return;                     // (only in the newest row's block, which has waited)
     float4 v[DD / 4];
 #pragma unroll
     for (int sg = 0; sg < SEG; sg++)
@@ -882,6 +892,7 @@ cudaError_t launch_indexer_prefill(const IndexerArgs &a, cudaStream_t s) {
 cudaError_t launch_indexer_decode(const IndexerArgs &a, const DecodePos &p, cudaStream_t s) {
     uint64_t vis_max = 0;
     for (int b = 0; b < a.n_seq; b++) vis_max = ((p.pos[b] + 1) / 4 > vis_max) ? (p.pos[b] + 1) / 4 : vis_max;
+    const int early = (pdl_prev().newest_only && pdl_prev().s == s) ? 1 : 0;
     cudaError_t e;
     // staged rows by TMA when the row width allows it (d = 32, 64, 96 or 128)
     const int64_t idx_cap = a.d > 0 ? a.seq_stride / a.d : 0;
@@ -905,7 +916,7 @@ cudaError_t launch_indexer_decode(const IndexerArgs &a, const DecodePos &p, cuda
     case dd:                                                                                                 \
         e = ensure_dyn_smem(score_decode_tma_kernel<dd>, smem);                                              \
         if (e != cudaSuccess) return e;                                                                      \
-        e = launch_pdl(score_decode_tma_kernel<dd>, grid, dim3(128), smem, s, rm, a, p, (int)idx_cap);       \
+        e = launch_pdl(score_decode_tma_kernel<dd>, grid, dim3(128), smem, s, rm, a, p, (int)idx_cap, early); \
         if (e != cudaSuccess) return e;                                                                      \
         break;
         switch (a.d) {
