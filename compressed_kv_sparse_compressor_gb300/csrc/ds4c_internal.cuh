@@ -64,8 +64,10 @@ cudaError_t launch_fma_probe(uint32_t blocks, uint32_t iters, float *out, cudaSt
 // orders every earlier kernel.  pdl_launch_dependents() lets the next kernel be
 // scheduled.  Under an ordinary launch both are no-ops.  (The decode indexer
 // score reads rows older than the newest before its wait when the previous
-// kernel is the decode compressor, see PdlPrev; the split query blocks of the
-// attention's raw-row split read only the call's own inputs before theirs.)
+// kernel is the decode compressor, and the attention's raw-row split reads the
+// ring before its wait when the previous kernel is the top-k or the decode
+// compressor, see PdlPrev; its split query blocks read only the call's own
+// inputs before theirs.)
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
@@ -133,24 +135,27 @@ __device__ __forceinline__ void indexer_qat_group(float4 &v, float c) {
     v.w = ldexpf(e2m1_rne(ldexpf(v.w, -e)), e);
 }
 
-// The last kernel launch_pdl issued on this thread: set by the decode compressor's launcher,
-// whose kernel writes nothing a decode indexer score reads but the newest compressed row of
-// each sequence; any other launch clears it.  A score launched right after it on the same
-// stream may read the older rows before waiting for it (a kernel of the caller in between
-// is an ordinary launch, which the score waits for in full).
+// What the kernel launch_pdl issued last on this thread (and its stream) writes, when a kernel
+// launched right after it may read other data before waiting for it: set by the launchers of
+// the decode compressor (which writes no compressed row but the newest of each sequence, and
+// no raw ring, raw mirror or query) and of the top-k (which writes the row lists alone); any
+// other launch clears it.  A caller's kernel in between is an ordinary launch, which the next
+// kernel waits for in full.
+enum PdlKind { PDL_ANY = 0, PDL_DECODE_COMPRESS = 1, PDL_TOPK = 2 };
 struct PdlPrev {
     cudaStream_t s = nullptr;
-    bool newest_only = false;
+    int kind = PDL_ANY;
 };
 inline PdlPrev &pdl_prev() {
     static thread_local PdlPrev v;
     return v;
 }
+inline bool pdl_prev_is(cudaStream_t s, int kind) { return pdl_prev().s == s && pdl_prev().kind == kind; }
 
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                               Args &&...args) {
-    pdl_prev().newest_only = false;
+    pdl_prev().kind = PDL_ANY;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = grid;
     cfg.blockDim = block;

@@ -1148,7 +1148,7 @@ constexpr int SPLIT_ROWS = 4;             // mirror rows per block of raw_split_
 __global__ void raw_split_kernel(uint16_t *__restrict__ mirror, const float *__restrict__ ring,
                                  const float *__restrict__ raw_new, int D, int n_seq, int n_tok, uint64_t pos0,
                                  DecodePos dp, int n_rows, const float *__restrict__ q, uint16_t *__restrict__ qsplit,
-                                 int nh) {
+                                 int nh, int early) {
     const int raw_blocks = (n_rows + SPLIT_ROWS - 1) / SPLIT_ROWS;
     if ((int)blockIdx.x >= raw_blocks) {
         // the query split (decode): one 64-d chunk c of query n per block, as the attention's
@@ -1179,7 +1179,10 @@ __global__ void raw_split_kernel(uint16_t *__restrict__ mirror, const float *__r
         pdl_wait();
         return;
     }
-    pdl_wait();
+    // early: the previous kernel writes neither the ring nor the mirror (the top-k or the decode
+    // compressor), so the rows are split before the wait; the last block (and every query
+    // block) still waits before finishing, so this grid completes only after that kernel
+    if (!early) pdl_wait();
     pdl_launch_dependents();
     // the source row of mirror row u (null: zeros)
     auto source = [&](int u) -> const float * {
@@ -1213,6 +1216,7 @@ __global__ void raw_split_kernel(uint16_t *__restrict__ mirror, const float *__r
             *reinterpret_cast<uint2 *>(lo + j) = make_uint2(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]));
         }
     }
+    if (early && (int)blockIdx.x == raw_blocks - 1) pdl_wait();
 }
 
 // Split rows: out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p over the
@@ -1369,9 +1373,10 @@ cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *dp, cudaSt
     const int parts = a.parts > 0 ? a.parts : 1;
     const bool qpre = parts > 1 && nq <= 2 * sm_count();
     const int q_blocks = qpre ? nq * (a.D / 64) : 0;
+    const int early = (pdl_prev_is(s, PDL_TOPK) || pdl_prev_is(s, PDL_DECODE_COMPRESS)) ? 1 : 0;
     cudaError_t e = launch_pdl(raw_split_kernel, dim3((raw_rows + SPLIT_ROWS - 1) / SPLIT_ROWS + q_blocks), dim3(128),
                                0, s, a.raw_mirror, a.ring, a.raw_new, a.D, a.n_seq, a.n_tok, a.pos0, dd, raw_rows,
-                               a.q, a.qsplit, a.H);
+                               a.q, a.qsplit, a.H, early);
     if (e != cudaSuccess) return e;
     TcAttnParams p{};
     p.out = a.out;

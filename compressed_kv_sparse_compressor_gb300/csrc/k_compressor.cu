@@ -494,7 +494,7 @@ cudaError_t launch_compress_decode(const CompressArgs &a, const DecodePos &p, in
 #define DS4C_CDEC(A, I)                                                              \
         if (ga == A && gi == I) {                                                   \
             const cudaError_t e = launch_pdl(compress_decode_r4_kernel<A, I>, grid, dim3(128), 0, s, a, p); \
-            if (e == cudaSuccess) pdl_prev() = PdlPrev{s, true};                      \
+            if (e == cudaSuccess) pdl_prev() = PdlPrev{s, PDL_DECODE_COMPRESS};       \
             return e;                                                               \
         }
         DS4C_CDEC(128, 32)

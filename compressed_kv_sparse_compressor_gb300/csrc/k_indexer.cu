@@ -777,13 +777,16 @@ cudaError_t launch_topk(const IndexerArgs &a, const DecodePos &dp, int n_q, uint
     if (allow_resident && tk_smem<T>(vmax, true) <= LIMIT) {
         const size_t smem = tk_smem<T>(vmax, true);
         if ((e = ensure_dyn_smem(topk_kernel<T, true>, smem)) != cudaSuccess) return e;
-        return launch_pdl(topk_kernel<T, true>, dim3(n_q), dim3(T), smem, s, a, dp, wcap);
+        e = launch_pdl(topk_kernel<T, true>, dim3(n_q), dim3(T), smem, s, a, dp, wcap);
     } else if (tk_smem<T>(vmax, false) <= LIMIT) {
         const size_t smem = tk_smem<T>(vmax, false);
         if ((e = ensure_dyn_smem(topk_kernel<T, false>, smem)) != cudaSuccess) return e;
-        return launch_pdl(topk_kernel<T, false>, dim3(n_q), dim3(T), smem, s, a, dp, wcap);
+        e = launch_pdl(topk_kernel<T, false>, dim3(n_q), dim3(T), smem, s, a, dp, wcap);
+    } else {
+        return cudaErrorNotSupported;
     }
-    return cudaErrorNotSupported;
+    if (e == cudaSuccess) pdl_prev() = PdlPrev{s, PDL_TOPK};
+    return e;
 }
 
 
@@ -892,7 +895,7 @@ cudaError_t launch_indexer_prefill(const IndexerArgs &a, cudaStream_t s) {
 cudaError_t launch_indexer_decode(const IndexerArgs &a, const DecodePos &p, cudaStream_t s) {
     uint64_t vis_max = 0;
     for (int b = 0; b < a.n_seq; b++) vis_max = ((p.pos[b] + 1) / 4 > vis_max) ? (p.pos[b] + 1) / 4 : vis_max;
-    const int early = (pdl_prev().newest_only && pdl_prev().s == s) ? 1 : 0;
+    const int early = pdl_prev_is(s, PDL_DECODE_COMPRESS) ? 1 : 0;
     cudaError_t e;
     // staged rows by TMA when the row width allows it (d = 32, 64, 96 or 128)
     const int64_t idx_cap = a.d > 0 ? a.seq_stride / a.d : 0;
