@@ -501,6 +501,9 @@ cudaError_t launch_bn(const GemmArgs &a, cudaStream_t s) {
         for (int k = 2; k <= a.max_ksplit; k++) {
             const int kb_per = (kb_count + k - 1) / k;
             if (kb_per < 4 || (k - 1) * kb_per >= kb_count) continue;
+            // at most three quarters of the SMs: in a decode step the indexer score starts
+            // beside this GEMM (its blocks only need SMs the GEMM leaves free)
+            if (out_tiles * k > sms * 3 / 4) continue;
             const long cost = (long)((out_tiles * k + sms - 1) / sms) * (kb_per + UNIT_COST);
             if (cost < best) {
                 best = cost;
