@@ -752,12 +752,37 @@ __global__ void __launch_bounds__(T) topk_kernel(IndexerArgs a, DecodePos dp, in
         }
     }
     __syncthreads();
-    // 3. the low 20 bits among the candidates (all in b*), 10 at a time
-    tk_cand_pass<T>(bins, ckey, nc, 10, 10, true, 0u, rank1, warp_a, res);
-    const uint32_t b1 = res[0], rank2 = res[1];
-    tk_cand_pass<T>(bins, ckey, nc, 10, 0, false, (bstar << 10) | b1, rank2, warp_a, res);
-    const uint32_t kstar = (bstar << 20) | (b1 << 10) | res[0];
-    const uint32_t take_eq = res[1];                     // rows equal to K* to take, lowest first
+    // 3. K*, the rank1-th largest candidate key (all in b*), and how many rows equal to it to
+    //    take: up to 32 candidates by one warp (each lane counts the keys above and equal to its
+    //    own), more by the low 20 bits, 10 at a time
+    uint32_t kstar, take_eq;                             // take_eq: rows equal to K*, lowest first
+    if (nc <= 32) {
+        if (warp == 0) {
+            const uint32_t key = lane < nc ? ckey[lane] : 0u;
+            uint32_t gt = 0, eq = 0;
+            for (int j = 0; j < nc; j++) {
+                const uint32_t o = __shfl_sync(0xffffffffu, key, j);
+                gt += o > key ? 1u : 0u;
+                eq += o == key ? 1u : 0u;
+            }
+            const unsigned m = __ballot_sync(0xffffffffu, lane < nc && gt < rank1 && rank1 <= gt + eq);
+            const int src = __ffs(m) - 1;
+            const uint32_t kk = __shfl_sync(0xffffffffu, key, src), g = __shfl_sync(0xffffffffu, gt, src);
+            if (lane == 0) {
+                res[0] = kk;
+                res[1] = rank1 - g;
+            }
+        }
+        __syncthreads();
+        kstar = res[0];
+        take_eq = res[1];
+    } else {
+        tk_cand_pass<T>(bins, ckey, nc, 10, 10, true, 0u, rank1, warp_a, res);
+        const uint32_t b1 = res[0], rank2 = res[1];
+        tk_cand_pass<T>(bins, ckey, nc, 10, 0, false, (bstar << 10) | b1, rank2, warp_a, res);
+        kstar = (bstar << 20) | (b1 << 10) | res[0];
+        take_eq = res[1];
+    }
     // 4. candidates above K* join the selection, those equal to K* are marked apart
     tk_mark<T>(ckey, crow, nc, kstar, sel, eqm);
     // 5. in row order

@@ -212,6 +212,34 @@ def test_decode_small(ratio, base, heads):
             torch.testing.assert_close(dl.idx_comp[b], ref.idx_comp[0], rtol=RTOL, atol=ATOL)
 
 
+def test_decode_indexer_right_after_prefill_compressor():
+    """A decode indexer call straight after prefill compressor calls (no decode compressor in
+    between): the score may read rows before waiting for its predecessor only after the decode
+    compressor, so here it waits first; scores and lists bit-exact against the oracle."""
+    shape = configs.LayerShape(d_model=512, head_dim=512, n_rot=64, idx_head_dim=128, n_heads=64, ratio=4,
+                               top_k=16, dtype="bf16", w_std=0.04)
+    seed, B = 41, 6
+    lens = [700 + 37 * b for b in range(B)]                # some (pos + 1) % 4 == 0, some not
+    cap = max(lens) // 4 + 2
+    dl, wa, wi = device_layer(shape, comp_cap=cap, idx_cap=cap, n_seq=B, seed=seed, max_rows=max(lens))
+    for b in range(B):
+        view = dl.seq_view(b)
+        saved = dl.state
+        dl.state = view
+        dl.compress_prefill(configs.hidden(shape, seed, lens[b], layer=b).cuda(), 0)
+        dl.state = saved
+    q_idx = torch.cat([configs.queries(shape, seed, 1, offset_tok=lens[b], layer=b)[1] for b in range(B)]).cuda()
+    topk = torch.empty(B, shape.top_k, dtype=torch.int32, device="cuda")
+    vmax = (max(lens) + 1) // 4
+    scores = torch.full((B, vmax), float("nan"), device="cuda")
+    dl.indexer_topk(q_idx, lens, B, 1, topk, scores, vmax)
+    dl.sync()
+    for b in range(B):
+        st = download(dl, b)
+        check_indexer_sampled(st, q_idx[b:b + 1].cpu().numpy(), [lens[b]], topk[b:b + 1].cpu().numpy(),
+                              scores[b:b + 1].cpu().numpy(), [0])
+
+
 # ---------------------------------------------------------------------------
 # "One ratio-128 layer, 8192-token prefill in two 4096-token chunks" (full size)
 # ---------------------------------------------------------------------------
