@@ -19,16 +19,15 @@
 // position-ordered mirror the call builds in the workspace (one 128-row box per
 // query), compressed rows from the comp_split mirror the compressor maintains,
 // gathered by the row list (top-k on ratio-4 layers, every visible row on
-// ratio-128 layers) with 16-byte cp.async by the whole producer warp into the
-// same 128-byte-swizzled layout, lane pairs taking the two halves of one
-// 32-byte sector so that no sector is fetched twice (16 rows per instruction;
-// 32 rows of one 16-byte chunk each fetched every sector twice, and 4 whole
-// rows per instruction was slower still).  A tile is streamed twice through a
-// 4-deep ring of 16 KB slot pairs (the rate is set by the bytes in flight:
-// a 2-deep ring took 1.6 times as long as the 3-deep one): by 64-wide d-chunks
-// for S, by 64-row halves of 128-wide d-blocks for O (the same bytes form the
-// K-major A operand of the first product and the MN-major A operand of the
-// second).  Compressed rows
+// ratio-128 layers) with 16-byte cp.async by the two producer warps into the
+// same 128-byte-swizzled layout, eight lanes copying one row's 128 bytes so
+// that an instruction reads four whole lines (on the six 32 KB slots below
+// this beat lane pairs sharing 32-byte sectors, sixteen rows per instruction,
+// by 9 %; on an earlier ring of 16 KB slots it had been the slower one).  A
+// tile is streamed twice through a ring of six 32 KB slots: by 64-wide
+// d-chunks for S (each slot with the query chunk it meets), by 128-wide
+// d-blocks for O (the same bytes form the K-major A operand of the first
+// product and the MN-major A operand of the second).  Compressed rows
 // went through the E4M3 round trip on their first head_dim - n_rot dims, so
 // those values are exact in bf16 and their lo half is zero: the lo loads and
 // the lo MMAs of those dims are skipped.
