@@ -65,7 +65,7 @@ constexpr int ROWS = 128;
 constexpr int SLOT = 8192;            // [64 rows][64 d] bf16
 constexpr int PAIR = 2 * SLOT;
 constexpr int USLOT = 2 * PAIR;      // one ring slot
-constexpr int RING = 6;
+constexpr int RING = 5;
 // three warpgroups: {producer, MMA, two idle warps}, the softmax, the Q loader / epilogue
 constexpr int THREADS = 384;
 // registers per thread after the reallocation at entry (setmaxnreg): the first warpgroup gives
@@ -85,9 +85,8 @@ struct L {
     // the ring: 16 KB units of gathered rows, raw-row boxes and query chunks (a query
     // chunk [2H][64] bf16 holds Q_hi of 64 d in rows 0 .. H-1 and Q_lo in rows H .. 2H-1)
     static constexpr int OFF_X = 0;
-    static constexpr int OFF_PHI = OFF_X + RING * USLOT;
-    static constexpr int OFF_PLO = OFF_PHI + PB;
-    static constexpr int OFF_LIST = OFF_PLO + PB;
+    static constexpr int OFF_P = OFF_X + RING * USLOT;   // two P buffers (tile parity), each hi then lo
+    static constexpr int OFF_LIST = OFF_P + 4 * PB;
     // per head: the tile maximum as an order-preserving key, then (same word)
     // the rescale factor of the new reference
     static constexpr int OFF_TMAX = OFF_LIST + 4 * MAX_LIST;
@@ -96,7 +95,7 @@ struct L {
     // per head: the softmax denominator of the item the epilogue writes
     static constexpr int OFF_LFIN = OFF_FLAG + 8;
     static constexpr int OFF_BAR = OFF_LFIN + 4 * H;
-    static constexpr int N_BAR = 2 * RING + 16;
+    static constexpr int N_BAR = 2 * RING + 17;
     static_assert(2 * H * 64 * 2 == PAIR, "a query chunk fills half a ring slot");
     // the dynamic shared memory starts 1024-byte aligned (checked at entry), as
     // the 128-byte swizzle atoms of Q, the ring and P need
@@ -111,8 +110,12 @@ struct L {
 };
 
 // barrier indices
-enum { B_FULL = 0, B_EMPTY = RING, B_QREADY0 = 2 * RING, B_QREADY1, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1, B_PFULL,
-       B_PVDONE, B_OFREE0, B_OFREE1, B_SOFT, B_DRAIN, B_QFREE0, B_QFREE1, B_LREADY, B_PBAR };
+enum { B_FULL = 0, B_EMPTY = RING, B_QREADY0 = 2 * RING, B_QREADY1, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1, B_PFULL0,
+       B_PFULL1, B_PVDONE, B_OFREE0, B_OFREE1, B_SOFT, B_DRAIN, B_QFREE0, B_QFREE1, B_LREADY, B_PBAR, B_COUNT };
+static_assert(B_QREADY1 == B_QREADY0 + 1 && B_SFULL1 == B_SFULL0 + 1 && B_SFREE1 == B_SFREE0 + 1 &&
+                  B_PFULL1 == B_PFULL0 + 1 && B_OFREE1 == B_OFREE0 + 1 && B_QFREE1 == B_QFREE0 + 1,
+              "barrier pairs indexed by a parity are adjacent");
+static_assert(B_COUNT == 2 * RING + 17, "the layout's barrier count");
 
 struct TcAttnParams {
     float *out;
@@ -513,7 +516,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         mbar_init(bar(B_SFULL1), 1);
         mbar_init(bar(B_SFREE0), 128);
         mbar_init(bar(B_SFREE1), 128);
-        mbar_init(bar(B_PFULL), 128);
+        mbar_init(bar(B_PFULL0), 128);
+        mbar_init(bar(B_PFULL1), 128);
         mbar_init(bar(B_PVDONE), 1);
         for (int j = 0; j < 2; j++) mbar_init(bar(B_OFREE0 + j), 128);
         mbar_init(bar(B_SOFT), 128);
@@ -751,7 +755,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         constexpr uint64_t DK = desc_template(16, 1024, 2);      // S operands
         constexpr uint64_t DA = desc_template(SLOT, 1024, 2);    // X^T of the O product
         constexpr uint64_t DP = desc_template(8192, 1024, 2);    // P^T
-        const uint32_t phi = smem_u32(sm + Lay::OFF_PHI), plo = smem_u32(sm + Lay::OFF_PLO);
+        const uint32_t p_base = smem_u32(sm + Lay::OFF_P);
         uint32_t unit = 0, g = 0, tok = 0;
         bool ok = true;
         // The whole warp runs the issue loop (its operands stay warp-uniform); lane 0 issues.
@@ -823,7 +827,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         };
         // O of tile i; `first`: the item's first tile (overwrites the accumulator), which
         // waits per d-block until the epilogue has read the previous item's block
-        auto do_pv = [&](int i, bool first) -> bool {
+        auto do_pv = [&](int i, bool first, uint32_t gi) -> bool {
+            const uint32_t phi = p_base + (gi & 1) * 2 * Lay::PB, plo = phi + Lay::PB;
             for (int j = 0; j < Lay::DB; j++) {
                 if (first && tok > 0 && (j & 1) == 0) {
                     if (!wait_all(bar(B_OFREE0 + (j >> 1)), (tok - 1) & 1)) return false;
@@ -872,9 +877,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             for (int i = itm.tb; i < itm.te && good; i++) {
                 const uint32_t gi = g + (i - itm.tb);
                 if (i + 1 < itm.te && !do_qk(gi + 1, i + 1, i + 1 == itm.te - 1)) { good = false; break; }
-                if (!wait_all(bar(B_PFULL), gi & 1)) { good = false; break; }
+                if (!wait_all(bar(B_PFULL0 + (gi & 1)), (gi >> 1) & 1)) { good = false; break; }
                 fence_after();
-                if (!do_pv(i, i == itm.tb)) { good = false; break; }
+                if (!do_pv(i, i == itm.tb, gi)) { good = false; break; }
             }
             ok = good;
             g += itm.te - itm.tb;
@@ -894,8 +899,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         const int q4 = warp & 3;                 // TMEM lane quarter
         const int r = q4 * 32 + lane;            // tile row
         const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
-        uint8_t *phi_p = sm + Lay::OFF_PHI;
-        uint8_t *plo_p = sm + Lay::OFF_PLO;
         const int tid = threadIdx.x - 128;       // 0..127
         uint32_t g = 0, sphase = 0, tok = 0;
         bool ok = true;
@@ -986,11 +989,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                         fence_before();
                     }
                 }
-                // the P buffers are free once the previous tile's O (of this item or the
-                // previous one) has been computed
-                if (g > 0 && !waited) {
+                // P buffer g & 1 was last read by the O of tile g - 2, issued before this tile's S
+                // and so complete by now.  The last tile of an item still waits for the previous
+                // tile's O before its P is handed over: the epilogue tells the item's last O from
+                // the one before by this order.
+                if (i == itm.te - 1 && i > itm.tb && !waited) {
                     if (!mbar_wait(bar(B_PVDONE), (g - 1) & 1, abort)) { ok = false; break; }
                 }
+                uint8_t *phi_p = sm + Lay::OFF_P + (g & 1) * 2 * Lay::PB;
+                uint8_t *plo_p = phi_p + Lay::PB;
                 // P^T row r (MN-major, 128-byte swizzle), hi and lo
 #pragma unroll
                 for (int h = 0; h < H; h++) s[h] = exp2f(s[h] - mref_s[h]);
@@ -1006,7 +1013,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                                                                          pack_bf16x2(lv[4], lv[5]), pack_bf16x2(lv[6], lv[7]));
                 }
                 fence_proxy_async();
-                mbar_arrive(bar(B_PFULL));
+                mbar_arrive(bar(B_PFULL0 + (g & 1)));
                 {
                     float l0, l1;
                     warp_heads_reduce<false>(s, l0, l1);
@@ -1219,49 +1226,50 @@ __global__ void raw_split_kernel(uint16_t *__restrict__ mirror, const float *__r
 }
 
 // Split rows: out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p over the
-// parts of a query (M = the largest reference of a non-empty part).
+// parts of a query (M = the largest reference of a non-empty part).  Every
+// thread reads its head's part maxima and denominators together with its
+// partial outputs and forms the weights itself, so the block has no barrier.
+constexpr int COMBINE_MAX_PARTS = 8;
 __global__ void __launch_bounds__(128) attn_combine_kernel(float *__restrict__ out, const float *__restrict__ part_o,
                                                            const float *__restrict__ part_ml, int H, int D, int parts,
                                                            float *__restrict__ ring, const float *__restrict__ raw_new,
                                                            DecodePos dp) {
-    __shared__ float w[8];
-    __shared__ float inv_den;
     pdl_wait();
     pdl_launch_dependents();
     const int n = blockIdx.x / H, h = blockIdx.x % H;
-    // ring commit of the step (decode: query n is sequence n): the attention read the
-    // ring through the raw mirror, so the slot can take the new row now
+    // ring commit of the step (decode: query n is sequence n): the attention read the ring
+    // through the raw mirror, so the slot can take the new row now
     if (ring && h == 0) {
         float *dst = ring + ((size_t)n * ROWS + (size_t)(dp.pos[n] % ROWS)) * D;
         const float *src = raw_new + (size_t)n * D;
         for (int d = threadIdx.x * 4; d < D; d += blockDim.x * 4)
             *reinterpret_cast<float4 *>(dst + d) = *reinterpret_cast<const float4 *>(src + d);
     }
-    if (threadIdx.x == 0) {
-        float M = -INFINITY;
-        for (int q = 0; q < parts; q++) {
-            const float *ml = part_ml + ((size_t)n * parts + q) * 2 * H;
-            if (ml[H + h] > 0.f) M = fmaxf(M, ml[h]);
-        }
-        float den = 0.f;
-        for (int q = 0; q < parts; q++) {
-            const float *ml = part_ml + ((size_t)n * parts + q) * 2 * H;
-            const float wq = (ml[H + h] > 0.f) ? exp2f(ml[h] - M) : 0.f;
-            w[q] = wq;
-            den += wq * ml[H + h];
-        }
-        inv_den = 1.0f / den;
-    }
-    __syncthreads();
     for (int d = threadIdx.x * 4; d < D; d += blockDim.x * 4) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q = 0; q < parts; q++) {
-            const float wq = w[q];
-            if (wq == 0.f) continue;
-            const float4 o = *reinterpret_cast<const float4 *>(part_o + (((size_t)n * parts + q) * H + h) * D + d);
-            acc.x += wq * o.x; acc.y += wq * o.y; acc.z += wq * o.z; acc.w += wq * o.w;
+        float m[COMBINE_MAX_PARTS], l[COMBINE_MAX_PARTS];
+        float4 o[COMBINE_MAX_PARTS];
+#pragma unroll
+        for (int q = 0; q < COMBINE_MAX_PARTS; q++) {
+            if (q >= parts) break;
+            const float *ml = part_ml + ((size_t)n * parts + q) * 2 * H;
+            m[q] = ml[h];
+            l[q] = ml[H + h];
+            o[q] = *reinterpret_cast<const float4 *>(part_o + (((size_t)n * parts + q) * H + h) * D + d);
         }
-        const float id = inv_den;
+        float M = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < COMBINE_MAX_PARTS; q++)
+            if (q < parts && l[q] > 0.f) M = fmaxf(M, m[q]);
+        float den = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < COMBINE_MAX_PARTS; q++) {
+            if (q >= parts || !(l[q] > 0.f)) continue;
+            const float wq = exp2f(m[q] - M);
+            den += wq * l[q];
+            acc.x += wq * o[q].x; acc.y += wq * o[q].y; acc.z += wq * o[q].z; acc.w += wq * o[q].w;
+        }
+        const float id = 1.0f / den;
         *reinterpret_cast<float4 *>(out + ((size_t)n * H + h) * D + d) = make_float4(acc.x * id, acc.y * id, acc.z * id, acc.w * id);
     }
 }
@@ -1331,6 +1339,7 @@ cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, cudaStream_t s
     if (4 * 32 * (REG_LOW + REG_SOFT + REG_AUX) > THREADS * regs) return cudaErrorNotSupported;
     e = launch_pdl(attn_tc_kernel<H, D>, dim3(grid), dim3(THREADS), Lay::SMEM, s, rh, rl, qm, p);
     if (e != cudaSuccess || p.parts == 1) return e;
+    if (p.parts > COMBINE_MAX_PARTS) return cudaErrorNotSupported;
     return launch_pdl(attn_combine_kernel, dim3(a.n_seq * a.n_tok * a.H), dim3(128), 0, s, a.out,
                       (const float *)p.part_o, (const float *)p.part_ml, a.H, D, p.parts,
                       a.commit_ring ? const_cast<float *>(a.ring) : nullptr, a.raw_new, p.dp);
@@ -1350,7 +1359,7 @@ int attn_tc_decode_parts(int ratio, int k, int comp_cap) {
     const int rows = ratio == 4 ? (k < comp_cap ? k : comp_cap) : (ratio == 128 ? comp_cap : 0);
     const int tiles = 1 + (rows + ROWS - 1) / ROWS;
     const int parts = tiles == 1 ? 1 : 1 + tiles / 2;
-    return parts < 8 ? parts : 8;
+    return parts < COMBINE_MAX_PARTS ? parts : COMBINE_MAX_PARTS;
 }
 
 bool attn_tc_supported(int H, int D, int S, int ratio, int k) {
