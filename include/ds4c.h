@@ -20,6 +20,13 @@
  *   - Calls are asynchronous on `stream`.  Arguments are validated on the host
  *     before anything is launched, so a call that returns an error has no
  *     side effect.  Calls on one layer state must be ordered on one stream.
+ *   - The kernels are programmatic dependent launches: each may be scheduled
+ *     while the previous kernel on the stream drains, and waits for it before
+ *     reading what it wrote.  Right after this library's decode compressor (or
+ *     top-k) on the same stream and host thread, the decode indexer score (or
+ *     the attention's raw-row split) reads data that kernel does not write
+ *     before that wait; a kernel of the caller in between is an ordinary
+ *     launch, which the next one waits for in full.
  *   - A position `pos` counts tokens already processed by a sequence; token
  *     `pos` is the next one.  Compressed row c of a ratio-r layer pools the
  *     window of tokens c*r .. c*r+r-1 and exists once pos >= (c+1)*r.
