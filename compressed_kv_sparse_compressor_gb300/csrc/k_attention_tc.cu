@@ -65,7 +65,7 @@ constexpr int ROWS = 128;
 constexpr int SLOT = 8192;            // [64 rows][64 d] bf16
 constexpr int PAIR = 2 * SLOT;
 constexpr int USLOT = 2 * PAIR;      // one ring slot
-constexpr int RING = 5;
+constexpr int RING = 6;
 // three warpgroups: {producer, MMA, two idle warps}, the softmax, the Q loader / epilogue
 constexpr int THREADS = 384;
 // registers per thread after the reallocation at entry (setmaxnreg): the first warpgroup gives
@@ -85,8 +85,9 @@ struct L {
     // the ring: 16 KB units of gathered rows, raw-row boxes and query chunks (a query
     // chunk [2H][64] bf16 holds Q_hi of 64 d in rows 0 .. H-1 and Q_lo in rows H .. 2H-1)
     static constexpr int OFF_X = 0;
-    static constexpr int OFF_P = OFF_X + RING * USLOT;   // two P buffers (tile parity), each hi then lo
-    static constexpr int OFF_LIST = OFF_P + 4 * PB;
+    static constexpr int OFF_PHI = OFF_X + RING * USLOT;
+    static constexpr int OFF_PLO = OFF_PHI + PB;
+    static constexpr int OFF_LIST = OFF_PLO + PB;
     // per head: the tile maximum as an order-preserving key, then (same word)
     // the rescale factor of the new reference
     static constexpr int OFF_TMAX = OFF_LIST + 4 * MAX_LIST;
@@ -95,7 +96,7 @@ struct L {
     // per head: the softmax denominator of the item the epilogue writes
     static constexpr int OFF_LFIN = OFF_FLAG + 8;
     static constexpr int OFF_BAR = OFF_LFIN + 4 * H;
-    static constexpr int N_BAR = 2 * RING + 17;
+    static constexpr int N_BAR = 2 * RING + 16;
     static_assert(2 * H * 64 * 2 == PAIR, "a query chunk fills half a ring slot");
     // the dynamic shared memory starts 1024-byte aligned (checked at entry), as
     // the 128-byte swizzle atoms of Q, the ring and P need
@@ -110,12 +111,8 @@ struct L {
 };
 
 // barrier indices
-enum { B_FULL = 0, B_EMPTY = RING, B_QREADY0 = 2 * RING, B_QREADY1, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1, B_PFULL0,
-       B_PFULL1, B_PVDONE, B_OFREE0, B_OFREE1, B_SOFT, B_DRAIN, B_QFREE0, B_QFREE1, B_LREADY, B_PBAR, B_COUNT };
-static_assert(B_QREADY1 == B_QREADY0 + 1 && B_SFULL1 == B_SFULL0 + 1 && B_SFREE1 == B_SFREE0 + 1 &&
-                  B_PFULL1 == B_PFULL0 + 1 && B_OFREE1 == B_OFREE0 + 1 && B_QFREE1 == B_QFREE0 + 1,
-              "barrier pairs indexed by a parity are adjacent");
-static_assert(B_COUNT == 2 * RING + 17, "the layout's barrier count");
+enum { B_FULL = 0, B_EMPTY = RING, B_QREADY0 = 2 * RING, B_QREADY1, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1, B_PFULL,
+       B_PVDONE, B_OFREE0, B_OFREE1, B_SOFT, B_DRAIN, B_QFREE0, B_QFREE1, B_LREADY, B_PBAR };
 
 struct TcAttnParams {
     float *out;
@@ -516,8 +513,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         mbar_init(bar(B_SFULL1), 1);
         mbar_init(bar(B_SFREE0), 128);
         mbar_init(bar(B_SFREE1), 128);
-        mbar_init(bar(B_PFULL0), 128);
-        mbar_init(bar(B_PFULL1), 128);
+        mbar_init(bar(B_PFULL), 128);
         mbar_init(bar(B_PVDONE), 1);
         for (int j = 0; j < 2; j++) mbar_init(bar(B_OFREE0 + j), 128);
         mbar_init(bar(B_SOFT), 128);
@@ -755,7 +751,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         constexpr uint64_t DK = desc_template(16, 1024, 2);      // S operands
         constexpr uint64_t DA = desc_template(SLOT, 1024, 2);    // X^T of the O product
         constexpr uint64_t DP = desc_template(8192, 1024, 2);    // P^T
-        const uint32_t p_base = smem_u32(sm + Lay::OFF_P);
+        const uint32_t phi = smem_u32(sm + Lay::OFF_PHI), plo = smem_u32(sm + Lay::OFF_PLO);
         uint32_t unit = 0, g = 0, tok = 0;
         bool ok = true;
         // The whole warp runs the issue loop (its operands stay warp-uniform); lane 0 issues.
@@ -827,8 +823,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         };
         // O of tile i; `first`: the item's first tile (overwrites the accumulator), which
         // waits per d-block until the epilogue has read the previous item's block
-        auto do_pv = [&](int i, bool first, uint32_t gi) -> bool {
-            const uint32_t phi = p_base + (gi & 1) * 2 * Lay::PB, plo = phi + Lay::PB;
+        auto do_pv = [&](int i, bool first) -> bool {
             for (int j = 0; j < Lay::DB; j++) {
                 if (first && tok > 0 && (j & 1) == 0) {
                     if (!wait_all(bar(B_OFREE0 + (j >> 1)), (tok - 1) & 1)) return false;
@@ -877,9 +872,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             for (int i = itm.tb; i < itm.te && good; i++) {
                 const uint32_t gi = g + (i - itm.tb);
                 if (i + 1 < itm.te && !do_qk(gi + 1, i + 1, i + 1 == itm.te - 1)) { good = false; break; }
-                if (!wait_all(bar(B_PFULL0 + (gi & 1)), (gi >> 1) & 1)) { good = false; break; }
+                if (!wait_all(bar(B_PFULL), gi & 1)) { good = false; break; }
                 fence_after();
-                if (!do_pv(i, i == itm.tb, gi)) { good = false; break; }
+                if (!do_pv(i, i == itm.tb)) { good = false; break; }
             }
             ok = good;
             g += itm.te - itm.tb;
@@ -899,6 +894,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
         const int q4 = warp & 3;                 // TMEM lane quarter
         const int r = q4 * 32 + lane;            // tile row
         const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+        uint8_t *phi_p = sm + Lay::OFF_PHI;
+        uint8_t *plo_p = sm + Lay::OFF_PLO;
         const int tid = threadIdx.x - 128;       // 0..127
         uint32_t g = 0, sphase = 0, tok = 0;
         bool ok = true;
@@ -989,15 +986,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                         fence_before();
                     }
                 }
-                // P buffer g & 1 was last read by the O of tile g - 2, issued before this tile's S
-                // and so complete by now.  The last tile of an item still waits for the previous
-                // tile's O before its P is handed over: the epilogue tells the item's last O from
-                // the one before by this order.
-                if (i == itm.te - 1 && i > itm.tb && !waited) {
+                // the P buffers are free once the previous tile's O (of this item or the
+                // previous one) has been computed
+                if (g > 0 && !waited) {
                     if (!mbar_wait(bar(B_PVDONE), (g - 1) & 1, abort)) { ok = false; break; }
                 }
-                uint8_t *phi_p = sm + Lay::OFF_P + (g & 1) * 2 * Lay::PB;
-                uint8_t *plo_p = phi_p + Lay::PB;
                 // P^T row r (MN-major, 128-byte swizzle), hi and lo
 #pragma unroll
                 for (int h = 0; h < H; h++) s[h] = exp2f(s[h] - mref_s[h]);
@@ -1013,7 +1006,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
                                                                          pack_bf16x2(lv[4], lv[5]), pack_bf16x2(lv[6], lv[7]));
                 }
                 fence_proxy_async();
-                mbar_arrive(bar(B_PFULL0 + (g & 1)));
+                mbar_arrive(bar(B_PFULL));
                 {
                     float l0, l1;
                     warp_heads_reduce<false>(s, l0, l1);
