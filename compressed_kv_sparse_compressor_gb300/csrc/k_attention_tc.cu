@@ -112,7 +112,12 @@ struct L {
 
 // barrier indices
 enum { B_FULL = 0, B_EMPTY = RING, B_QREADY0 = 2 * RING, B_QREADY1, B_SFULL0, B_SFULL1, B_SFREE0, B_SFREE1, B_PFULL,
-       B_PVDONE, B_OFREE0, B_OFREE1, B_SOFT, B_DRAIN, B_QFREE0, B_QFREE1, B_LREADY, B_PBAR };
+       B_PVDONE, B_OFREE0, B_OFREE1, B_SOFT, B_DRAIN, B_QFREE0, B_QFREE1, B_LREADY, B_PBAR, B_COUNT };
+// barriers indexed as X0 + parity must be adjacent
+static_assert(B_QREADY1 == B_QREADY0 + 1 && B_SFULL1 == B_SFULL0 + 1 && B_SFREE1 == B_SFREE0 + 1 &&
+                  B_OFREE1 == B_OFREE0 + 1 && B_QFREE1 == B_QFREE0 + 1,
+              "barrier pairs indexed by a parity are adjacent");
+static_assert(B_COUNT == 2 * RING + 16, "the layout's barrier count");
 
 struct TcAttnParams {
     float *out;
