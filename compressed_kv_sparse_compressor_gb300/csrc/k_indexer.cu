@@ -753,34 +753,56 @@ __global__ void __launch_bounds__(T) topk_kernel(IndexerArgs a, DecodePos dp, in
     }
     __syncthreads();
     // 3. K*, the rank1-th largest candidate key (all in b*), and how many rows equal to it to
-    //    take: up to 32 candidates by one warp (each lane counts the keys above and equal to its
-    //    own), more by the low 20 bits, 10 at a time
+    //    take: bits 10..19 by a 1024-bin pass unless the candidates are few; then one warp
+    //    ranks the (at most 32) candidates left, each lane counting the keys above and equal
+    //    to its own; more than 32 left take the pass over bits 0..9
     uint32_t kstar, take_eq;                             // take_eq: rows equal to K*, lowest first
-    if (nc <= 32) {
+    uint32_t match = 0, need = rank1;                    // candidates whose key >> mshift == match
+    int mshift = 32;                                     // (32: every candidate)
+    if (nc > 32) {
+        tk_cand_pass<T>(bins, ckey, nc, 10, 10, true, 0u, rank1, warp_a, res);
+        const uint32_t b1 = res[0];
+        need = res[1];
+        match = (bstar << 10) | b1;
+        mshift = 10;
+    }
+    if (mshift == 32 || bins[match & 1023u] <= 32) {
         if (warp == 0) {
-            const uint32_t key = lane < nc ? ckey[lane] : 0u;
+            // gather the matching candidates, one per lane, in candidate order
+            uint32_t key = 0u;
+            int cnt = 0;
+            for (int j0 = 0; j0 < nc; j0 += 32) {
+                const int j = j0 + lane;
+                const uint32_t kj = j < nc ? ckey[j] : 0u;
+                const bool mt = j < nc && (mshift == 32 || (kj >> mshift) == match);
+                unsigned bm = __ballot_sync(0xffffffffu, mt);
+                while (bm) {                             // at most 32 matches in all
+                    const uint32_t v = __shfl_sync(0xffffffffu, kj, __ffs(bm) - 1);
+                    if (lane == cnt) key = v;
+                    cnt++;
+                    bm &= bm - 1u;
+                }
+            }
             uint32_t gt = 0, eq = 0;
-            for (int j = 0; j < nc; j++) {
+            for (int j = 0; j < cnt; j++) {
                 const uint32_t o = __shfl_sync(0xffffffffu, key, j);
                 gt += o > key ? 1u : 0u;
                 eq += o == key ? 1u : 0u;
             }
-            const unsigned m = __ballot_sync(0xffffffffu, lane < nc && gt < rank1 && rank1 <= gt + eq);
+            const unsigned m = __ballot_sync(0xffffffffu, lane < cnt && gt < need && need <= gt + eq);
             const int src = __ffs(m) - 1;
             const uint32_t kk = __shfl_sync(0xffffffffu, key, src), g = __shfl_sync(0xffffffffu, gt, src);
-            if (lane == 0) {
-                res[0] = kk;
-                res[1] = rank1 - g;
+            if (lane == 0) {                             // (res may still be read: the pass's b1)
+                warp_b[0] = kk;
+                warp_b[1] = need - g;
             }
         }
         __syncthreads();
-        kstar = res[0];
-        take_eq = res[1];
+        kstar = warp_b[0];
+        take_eq = warp_b[1];
     } else {
-        tk_cand_pass<T>(bins, ckey, nc, 10, 10, true, 0u, rank1, warp_a, res);
-        const uint32_t b1 = res[0], rank2 = res[1];
-        tk_cand_pass<T>(bins, ckey, nc, 10, 0, false, (bstar << 10) | b1, rank2, warp_a, res);
-        kstar = (bstar << 20) | (b1 << 10) | res[0];
+        tk_cand_pass<T>(bins, ckey, nc, 10, 0, false, match, need, warp_a, res);
+        kstar = (match << 10) | res[0];
         take_eq = res[1];
     }
     // 4. candidates above K* join the selection, those equal to K* are marked apart
