@@ -145,12 +145,13 @@ def test_ragged_chunks(ratio, heads, D):
 # Decode: B sequences, one token each at staggered positions
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("ratio,base,heads", [(4, 60, 64), (128, 380, 64), (0, 200, 64), (4, 60, 8),
-                                              (128, 380, 24)])
-def test_decode_small(ratio, base, heads):
-    """heads < 64: the padded tensor-core attention, split rows combined over the real heads."""
+@pytest.mark.parametrize("ratio,base,heads,top_k", [(4, 60, 64, 16), (128, 380, 64, 16), (0, 200, 64, 16),
+                                                    (4, 60, 8, 16), (128, 380, 24, 16), (4, 1600, 64, 384)])
+def test_decode_small(ratio, base, heads, top_k):
+    """heads < 64: the padded tensor-core attention, split rows combined over the real heads.
+    top_k 384: four row tiles, split as the raw tile, two compressed tiles and one."""
     shape = configs.LayerShape(d_model=512, head_dim=512, n_rot=64, idx_head_dim=128, n_heads=heads, ratio=ratio,
-                               top_k=16, dtype="bf16", w_std=0.04)
+                               top_k=top_k, dtype="bf16", w_std=0.04)
     seed, B = 31, 8
     # every stagger class; ratio 4: some emit this step; ratio 128: 382 + 1 ends a window
     # (383 = 3*128 - 1), the others sit mid-window over 2 visible rows; ratio 0: a wrapped ring
