@@ -507,7 +507,7 @@ __device__ void tk_radix(int V, int k, int32_t *out, KeyAt key_at, uint32_t *cnt
         const int eq_rank = eq_run + __popc(eqm & lt);
         const bool sel = gt || (eq && eq_rank < remaining);
         const unsigned selm = __ballot_sync(0xffffffffu, sel);
-        if (sel) out[sel_run + __popc(selm & lt)] = c;
+        if (sel && sel_run + __popc(selm & lt) < k) out[sel_run + __popc(selm & lt)] = c;
         eq_run += __popc(eqm);
         sel_run += __popc(selm);
     }
@@ -546,10 +546,11 @@ __device__ __forceinline__ void tk_mark(const uint32_t *ckey, const uint32_t *cr
 
 // The list in row order: the selected rows plus the first take_eq rows equal
 // to K*.  Each thread owns a run of bitmap words; an exclusive scan of the
-// per-thread counts gives its output offset and the equal-key rank.
+// per-thread counts gives its output offset and the equal-key rank.  No write
+// lands past the k entries of the list, whatever the bitmaps hold.
 template <int T>
 __device__ __forceinline__ void tk_emit(const uint32_t *sel, const uint32_t *eqm, int W, uint32_t take_eq, int32_t *out,
-                                        uint32_t *warp_a, uint32_t *warp_b) {
+                                        int k, uint32_t *warp_a, uint32_t *warp_b) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int per = (W + T - 1) / T;
     const int w0 = min(W, tid * per), w1 = min(W, w0 + per);
@@ -585,7 +586,8 @@ __device__ __forceinline__ void tk_emit(const uint32_t *sel, const uint32_t *eqm
         eq_before += __popc(e_all);
         uint32_t m = sel[w] | e;
         while (m) {
-            out[dst++] = w * 32 + (__ffs(m) - 1);
+            if (dst < (uint32_t)k) out[dst] = w * 32 + (__ffs(m) - 1);
+            dst++;
             m &= m - 1u;
         }
     }
@@ -766,7 +768,9 @@ __global__ void __launch_bounds__(T) topk_kernel(IndexerArgs a, DecodePos dp, in
         match = (bstar << 10) | b1;
         mshift = 10;
     }
-    if (mshift == 32 || bins[match & 1023u] <= 32) {
+    const bool few = mshift == 32 || bins[match & 1023u] <= 32;
+    __syncthreads();                                     // every thread has read the count before bins is reused
+    if (few) {
         if (warp == 0) {
             // gather the matching candidates, one per lane, in candidate order
             uint32_t key = 0u;
@@ -808,7 +812,7 @@ __global__ void __launch_bounds__(T) topk_kernel(IndexerArgs a, DecodePos dp, in
     // 4. candidates above K* join the selection, those equal to K* are marked apart
     tk_mark<T>(ckey, crow, nc, kstar, sel, eqm);
     // 5. in row order
-    tk_emit<T>(sel, eqm, W, take_eq, out, warp_a, warp_b);
+    tk_emit<T>(sel, eqm, W, take_eq, out, k, warp_a, warp_b);
 }
 
 // Launch the top-k over n_q queries: the keys resident in shared memory when
