@@ -82,29 +82,48 @@ __device__ __forceinline__ float e4m3_roundtrip(float y) {
     return __half2float(__half(h));
 }
 
+// What a row's finish needs besides the pooled values: the RMSNorm gain of the
+// thread's columns and, in the rotated tail, the sine and cosine of its two
+// pairs' angles (both depend only on the row position and the columns, so they
+// are fetched and computed before the pool, while its loads are in flight).
+struct RowPrep {
+    float4 g;
+    float s0, c0, s1, c1;
+};
+
+__device__ __forceinline__ RowPrep row_prep(const CompressArgs &a, const LaneArgs &L, uint64_t c, int j) {
+    RowPrep r;
+    r.g = L.gain ? ld4(L.gain + j) : make_float4(1.f, 1.f, 1.f, 1.f);
+    r.s0 = r.s1 = 0.f;
+    r.c0 = r.c1 = 1.f;
+    const int nope = L.Dl - a.n_rot;
+    if (j >= nope) {
+        const int i0 = (j - nope) / 2;
+        const float pc = (float)(c * (uint64_t)a.ratio);
+        sincosf(__fmul_rn(pc, a.rope.inv_freq[i0]), &r.s0, &r.c0);
+        sincosf(__fmul_rn(pc, a.rope.inv_freq[i0 + 1]), &r.s1, &r.c1);
+    }
+    return r;
+}
+
 // RMSNorm -> tail RoPE -> (attention lane) FP8, then append.  x is this
 // thread's float4 of the pooled row; all G threads of the group call this.
 template <int G>
 __device__ __forceinline__ void finish_row(const CompressArgs &a, const LaneArgs &L, bool active, int seq,
-                                           uint64_t c, int j, float4 x, float *red) {
+                                           uint64_t c, int j, float4 x, float *red, const RowPrep &rp) {
     const int Dl = L.Dl;
     float ss = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
     ss = group_sum<G>(active ? ss : 0.f, red);
     const float inv = 1.0f / sqrtf(ss / (float)Dl + a.eps);
-    float4 g = L.gain ? ld4(L.gain + j) : make_float4(1.f, 1.f, 1.f, 1.f);
+    const float4 g = rp.g;
     float4 y = make_float4(x.x * inv * g.x, x.y * inv * g.y, x.z * inv * g.z, x.w * inv * g.w);
     const int nope = Dl - a.n_rot;
     if (j >= nope) {
-        const int i0 = (j - nope) / 2;
-        const float pc = (float)(c * (uint64_t)a.ratio);
-        float s0, c0, s1, c1;
-        sincosf(__fmul_rn(pc, a.rope.inv_freq[i0]), &s0, &c0);
-        sincosf(__fmul_rn(pc, a.rope.inv_freq[i0 + 1]), &s1, &c1);
         float4 r;
-        r.x = y.x * c0 - y.y * s0;
-        r.y = y.x * s0 + y.y * c0;
-        r.z = y.z * c1 - y.w * s1;
-        r.w = y.z * s1 + y.w * c1;
+        r.x = y.x * rp.c0 - y.y * rp.s0;
+        r.y = y.x * rp.s0 + y.y * rp.c0;
+        r.z = y.z * rp.c1 - y.w * rp.s1;
+        r.w = y.z * rp.s1 + y.w * rp.c1;
         y = r;
     }
     const size_t off = ((size_t)seq * L.cap + (size_t)c) * Dl + j;
@@ -145,6 +164,27 @@ __device__ __forceinline__ void finish_row(const CompressArgs &a, const LaneArgs
     }
 }
 
+// Softmax pool of a ratio-4 window's eight candidates, per column: the weights
+// exp(s - max) over the eight, their sum as the denominator.
+__device__ __forceinline__ float4 pool8(const float4 (&kv)[8], const float4 (&s)[8]) {
+    float4 m = s[0];
+#pragma unroll
+    for (int q = 1; q < 8; q++) m = max4(m, s[q]);
+    float4 den = make_float4(0.f, 0.f, 0.f, 0.f), sum = den;
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+        float4 w = make_float4(expf(s[q].x - m.x), expf(s[q].y - m.y), expf(s[q].z - m.z), expf(s[q].w - m.w));
+        den = add4(den, w);
+        sum.x += w.x * kv[q].x; sum.y += w.y * kv[q].y; sum.z += w.z * kv[q].z; sum.w += w.w * kv[q].w;
+    }
+    float4 x;
+    x.x = den.x > 0.f ? sum.x / den.x : 0.f;
+    x.y = den.y > 0.f ? sum.y / den.y : 0.f;
+    x.z = den.z > 0.f ? sum.z / den.z : 0.f;
+    x.w = den.w > 0.f ? sum.w / den.w : 0.f;
+    return x;
+}
+
 // Ratio 4: window c pools, per column j, rows 0..3 (previous window, columns
 // [0, Dl)) and rows 4..7 (current window, columns [Dl, 2Dl)).
 // One pooling task per G threads of a 128-thread block (decode: task = the
@@ -178,6 +218,7 @@ __device__ __forceinline__ void pool_r4(const CompressArgs &a, int lane_id, cons
     const float *skv = L.skv + (size_t)seq * 8 * W;
     const float *ssc = L.ssc + (size_t)seq * 8 * W;
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    RowPrep rp{};
     if (active) {
         float4 kv[8], s[8];
         const uint64_t cur = pos0 / 4;
@@ -192,22 +233,10 @@ __device__ __forceinline__ void pool_r4(const CompressArgs &a, int lane_id, cons
             const int64_t p = 4 * (int64_t)c + q;
             fetch(L, skv, ssc, W, 4, p, 4 + q, L.Dl + j, pos0, ws_row0, kv[4 + q], s[4 + q]);
         }
-        float4 m = s[0];
-#pragma unroll
-        for (int q = 1; q < 8; q++) m = max4(m, s[q]);
-        float4 den = make_float4(0.f, 0.f, 0.f, 0.f), sum = den;
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            float4 w = make_float4(expf(s[q].x - m.x), expf(s[q].y - m.y), expf(s[q].z - m.z), expf(s[q].w - m.w));
-            den = add4(den, w);
-            sum.x += w.x * kv[q].x; sum.y += w.y * kv[q].y; sum.z += w.z * kv[q].z; sum.w += w.w * kv[q].w;
-        }
-        x.x = den.x > 0.f ? sum.x / den.x : 0.f;
-        x.y = den.y > 0.f ? sum.y / den.y : 0.f;
-        x.z = den.z > 0.f ? sum.z / den.z : 0.f;
-        x.w = den.w > 0.f ? sum.w / den.w : 0.f;
+        rp = row_prep(a, L, c, j);
+        x = pool8(kv, s);
     }
-    finish_row<G>(a, L, active, seq, c, j, x, red);
+    finish_row<G>(a, L, active, seq, c, j, x, red, rp);
 }
 
 template <int G>
@@ -254,6 +283,7 @@ __global__ void __launch_bounds__(G * 4) compress_r128_kernel(CompressArgs a, in
     (void)T;
     const float *skv = L.skv + (size_t)seq * 128 * W;
     const float *ssc = L.ssc + (size_t)seq * 128 * W;
+    const RowPrep rp = row_prep(a, L, c, j);
     float4 m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     float4 den = make_float4(0.f, 0.f, 0.f, 0.f), sum = den;
     if (active) {
@@ -301,7 +331,7 @@ __global__ void __launch_bounds__(G * 4) compress_r128_kernel(CompressArgs a, in
     }
     // Every thread enters (the reductions use full-warp shuffles and, for
     // G > 32, block barriers); only split 0 owns the row and stores it.
-    finish_row<G>(a, L, active && split == 0, seq, c, j, x, red);
+    finish_row<G>(a, L, active && split == 0, seq, c, j, x, red, rp);
 }
 
 // Frontier commit (K2b): after the pools of a segment (tokens pos0 .. end-1),
@@ -325,30 +355,40 @@ __device__ __forceinline__ void commit_col(const CompressArgs &a, int lane_id, c
         return add4(ld4(L.sc + (ws_row0 + (int64_t)(p - pos0)) * L.sc_ld + col), ld4(L.ape + (size_t)(p % ratio) * W + col));
     };
     if (ratio == 4) {
+        // Every load first, then every store: the loads of the four row pairs go out
+        // together (one memory round trip), and no store can overtake a load of the
+        // frontier row it replaces.
+        const bool have = ce > c0;                        // a window completed in the segment
+        float4 nk[4], ns[4], mk[4], ms[4];
+        bool wr4[4];
 #pragma unroll
         for (int q = 0; q < 4; q++) {
-            // row q: token (ce-1)*4+q when a window completed in the segment
-            bool have = ce > c0;
-            float4 k0 = ld4(skv + (size_t)q * W + col), s0 = ld4(ssc + (size_t)q * W + col);
+            // new row q: token (ce-1)*4+q, from the segment or from the old row 4+q
+            nk[q] = ns[q] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (have) {
                 const uint64_t p = (ce - 1) * 4 + q;
-                if (p >= pos0) { k0 = ws_kv(p); s0 = ws_sc(p); }
-                else { k0 = ld4(skv + (size_t)(4 + q) * W + col); s0 = ld4(ssc + (size_t)(4 + q) * W + col); }
+                if (p >= pos0) { nk[q] = ws_kv(p); ns[q] = ws_sc(p); }
+                else { nk[q] = ld4(skv + (size_t)(4 + q) * W + col); ns[q] = ld4(ssc + (size_t)(4 + q) * W + col); }
             }
-            // row 4+q
+            // new row 4+q: token ce*4+q of the open window when the segment reached it,
+            // else (a window completed) the same token as row q
+            mk[q] = nk[q]; ms[q] = ns[q];
+            wr4[q] = have;
             if (q < me) {
                 const uint64_t p = ce * 4 + q;
-                if (p >= pos0) {
-                    st4(skv + (size_t)(4 + q) * W + col, ws_kv(p));
-                    st4(ssc + (size_t)(4 + q) * W + col, ws_sc(p));
-                }
-            } else if (have) {
-                st4(skv + (size_t)(4 + q) * W + col, k0);
-                st4(ssc + (size_t)(4 + q) * W + col, s0);
+                wr4[q] = p >= pos0;
+                if (wr4[q]) { mk[q] = ws_kv(p); ms[q] = ws_sc(p); }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            if (wr4[q]) {
+                st4(skv + (size_t)(4 + q) * W + col, mk[q]);
+                st4(ssc + (size_t)(4 + q) * W + col, ms[q]);
             }
             if (have) {
-                st4(skv + (size_t)q * W + col, k0);
-                st4(ssc + (size_t)q * W + col, s0);
+                st4(skv + (size_t)q * W + col, nk[q]);
+                st4(ssc + (size_t)q * W + col, ns[q]);
             }
         }
     } else {
