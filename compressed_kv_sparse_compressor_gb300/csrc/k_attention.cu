@@ -5,7 +5,8 @@
 // CTA handles one query token for all heads and streams its rows once.
 //
 // This is the CUDA-core formulation: Q [H][D] and a 32-row tile of K/V live
-// in shared memory; each thread owns H*D/256 output accumulators.
+// in shared memory; each thread owns up to ACC output accumulators (ACC the
+// power of two at or above H*D/256; the slots past H*D stay idle).
 #include "ds4c_internal.cuh"
 
 namespace ds4c {
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(AT_THREADS) attn_simt_kernel(AttnArgs a, Decod
 #pragma unroll
         for (int m = 0; m < ACC; m++) {
             const int e = threadIdx.x + AT_THREADS * m;
+            if (e >= H * D) break;
             const int h = e / D, dd = e % D;
             float v = acc[m] * alpha[h];
             const float *ph = Ps + h * AT_ROWS;
@@ -148,6 +150,7 @@ __global__ void __launch_bounds__(AT_THREADS) attn_simt_kernel(AttnArgs a, Decod
 #pragma unroll
     for (int m = 0; m < ACC; m++) {
         const int e = threadIdx.x + AT_THREADS * m;
+        if (e >= H * D) break;
         const int h = e / D;
         o[e] = acc[m] / l_run[h];
     }
@@ -170,7 +173,8 @@ cudaError_t launch_attention(const AttnArgs &a, const DecodePos *p, cudaStream_t
     if (n_q <= 0) return cudaSuccess;
     DecodePos dp{};
     if (a.n_seq > 1) dp = *p;
-    const int acc = a.H * a.D / AT_THREADS;
+    int acc = 2;                                         // accumulators per thread: a power of two
+    while (acc * AT_THREADS < a.H * a.D) acc *= 2;
     switch (acc) {
         case 2: return launch_acc<2>(a, dp, n_q, s);
         case 4: return launch_acc<4>(a, dp, n_q, s);
