@@ -62,7 +62,7 @@ class DeviceLayer:
             attn=abi.LaneState(_ptr(self.attn_comp), _ptr(self.attn_kv), _ptr(self.attn_score), _ptr(self.attn_pre),
                                _ptr(self.attn_split)),
             idx=abi.LaneState(_ptr(self.idx_comp), _ptr(self.idx_kv), _ptr(self.idx_score), _ptr(self.idx_pre), None))
-        self.ws_bytes = abi.ds4c_workspace_bytes(self.cfg, max_rows, n_seq if n_seq > 1 else 0)
+        self.ws_bytes = abi.ds4c_workspace_bytes(self.cfg, max_rows, n_seq)
         if self.ws_bytes == 0:
             raise abi.Ds4cError(abi.DS4C_ERR_SHAPE, "ds4c_workspace_bytes")
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)

@@ -259,6 +259,36 @@ def test_c2_full():
     _gather_check(dl, w.n_tok)
 
 
+def test_decode_one_sequence_short_prefix():
+    """A one-sequence layer whose workspace was sized for 4-token prefill chunks
+    takes a decode step: the workspace size covers decode steps of the layer's
+    sequence count (the decode layout's split partials exceed such a prefill's)."""
+    shape = configs.LayerShape(d_model=520, head_dim=128, n_rot=32, idx_head_dim=128, n_heads=16, ratio=4,
+                               top_k=512, dtype="f32", w_std=0.04)
+    seed = 61
+    dl, wa, wi = device_layer(shape, comp_cap=8, idx_cap=8, n_seq=1, seed=seed, max_rows=4)
+    h = configs.hidden(shape, seed, 7).cuda()
+    q, q_idx, raw = (x.cuda() for x in configs.queries(shape, seed, 7))
+    dl.compress_prefill(h[:3], 0)
+    dl.compress_prefill(h[3:6], 3)
+    dl.raw[0, :6] = raw[:6]
+    torch.cuda.synchronize()
+    before = download(dl)
+    dl.compress_decode(h[6:7], [6])
+    topk = torch.empty(1, shape.top_k, dtype=torch.int32, device="cuda")
+    scores = torch.full((1, 4), float("nan"), device="cuda")
+    dl.indexer_topk(q_idx[6:7], [6], 1, 1, topk, scores, 4)
+    out = torch.empty(1, shape.n_heads, shape.head_dim, device="cuda")
+    torch.cuda.synchronize()
+    after = download(dl)
+    dl.attention(q[6:7], raw[6:7], topk, [6], 1, 1, out, commit_ring=True)
+    dl.sync()
+    check_compress(before, after, wa, wi, h[6:7].cpu(), 6)
+    check_indexer_sampled(after, q_idx[6:7].cpu().numpy(), [6], topk.cpu().numpy(), scores.cpu().numpy(), [0])
+    check_attention_sampled(after, q[6:7].cpu().numpy(), raw[6:7].cpu().numpy(), topk.cpu().numpy(),
+                            out.cpu().numpy(), 6, [0])
+
+
 # ---------------------------------------------------------------------------
 # Checkpoint restore: gather -> scatter into a fresh state -> continue
 # ---------------------------------------------------------------------------

@@ -9,6 +9,9 @@ prefill of one to three chunks of ragged lengths or a decode step of up to 33
 sequences at staggered positions.  Every call is checked stage-wise on sampled
 outputs, as in the parity tests: compressed rows and frontier, indexer scores
 and lists (bit-exact), attention (tolerance), ring commit, checkpoint gather.
+Two more sweeps draw the multi-head indexer (1 to 64 heads, QAT on or off;
+scores and lists bit-exact) and the checkpoint restore (gather, scatter into a
+fresh state, continue: bit for bit the uninterrupted run).
 """
 
 import random
@@ -18,7 +21,7 @@ import pytest
 import torch
 
 import oracle as orc
-from compressed_kv_sparse_compressor_gb300 import configs
+from compressed_kv_sparse_compressor_gb300 import configs, synth
 from gpu_util import (check_attention_sampled, check_compress, check_indexer_sampled, device_layer, download,
                       require_gpu)
 from test_gpu_parity import _gather_check, _run_chunk
@@ -26,6 +29,7 @@ from test_gpu_parity import _gather_check, _run_chunk
 pytestmark = pytest.mark.gpu
 
 N_CASES = 40
+N_EXTRA = 12
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -120,3 +124,62 @@ def test_shape_sweep(case):
         _prefill(shape, plan, seed, rng)
     else:
         _decode(shape, plan, seed, rng)
+
+
+@pytest.mark.parametrize("case", range(N_EXTRA))
+def test_indexer_heads_sweep(case):
+    kind, shape0, _, seed, rng = _draw(2000 + case)
+    d = rng.choice([64, 128])
+    heads = rng.choice([1, 2, 4, 8, 16, 33, 64])
+    shape = configs.LayerShape(d_model=shape0.d_model, head_dim=shape0.head_dim, n_rot=min(shape0.n_rot, d),
+                               idx_head_dim=d, n_heads=shape0.n_heads, ratio=4, swa=shape0.swa, top_k=shape0.top_k,
+                               dtype=shape0.dtype, w_std=0.04, idx_heads=heads, idx_qat=rng.choice([0, 1]))
+    Ts = [rng.choice([3, 64, 129, 300, 513]) for _ in range(rng.randint(1, 3))]
+    T = rng.choice([1, 5, 64, 200])
+    cap = (sum(Ts) + T) // 4 + 2
+    dl, _, _ = device_layer(shape, comp_cap=cap, idx_cap=cap, seed=seed, max_rows=max(Ts + [T]))
+    pos = 0
+    for n in Ts:
+        dl.compress_prefill(configs.hidden(shape, seed, n, offset_tok=pos, device="cuda"), pos)
+        pos += n
+    st = download(dl)
+    q = synth.normal(seed, 700, (T, heads, d), offset=pos * heads * d)
+    w = synth.normal(seed, 701, (T, heads), offset=pos * heads).abs() * 0.25
+    V = max(1, (pos + T) // 4)
+    topk = torch.full((T, shape.top_k), -7, dtype=torch.int32, device="cuda")
+    scores = torch.full((T, V), float("nan"), device="cuda")
+    dl.indexer_topk_heads(q.cuda(), w.cuda(), [pos], 1, T, topk, scores, V)
+    dl.sync()
+    tkg, scg = topk.cpu().numpy(), scores.cpu().numpy()
+    for j in sorted(set([0, T - 1] + rng.sample(range(T), min(T, 4)))):
+        tk, sc = orc.indexer_topk_heads(st, q[j:j + 1].numpy(), w[j:j + 1].numpy(), [pos + j], want_scores=True)
+        Vj = (pos + j + 1) // 4
+        np.testing.assert_array_equal(scg[j, :Vj], sc[0, :Vj], err_msg=f"scores query {j}")
+        np.testing.assert_array_equal(tkg[j], tk[0], err_msg=f"top-k query {j}")
+
+
+@pytest.mark.parametrize("case", range(N_EXTRA))
+def test_restore_sweep(case):
+    _, shape, _, seed, rng = _draw(3000 + case)
+    T1, T2 = rng.choice([1, 5, 127, 301, 700]), rng.choice([1, 31, 170, 513])
+    cap = (T1 + T2) // max(shape.ratio, 1) + 2
+    icap = (T1 + T2) // 4 + 2
+    dl, wa, wi = device_layer(shape, comp_cap=cap, idx_cap=icap, seed=seed, max_rows=max(T1, T2))
+    _run_chunk(dl, wa, wi, shape, seed, 0, T1, {}, check=False)
+    n = dl.checkpoint_floats(T1)
+    body = torch.empty(n, device="cuda")
+    dl.checkpoint_gather(0, T1, body)
+    dl.sync()
+    fresh, _, _ = device_layer(shape, comp_cap=cap, idx_cap=icap, seed=seed, max_rows=max(T1, T2))
+    fresh.checkpoint_scatter(0, T1, body)
+    fresh.sync()
+    again = torch.empty(n, device="cuda")
+    fresh.checkpoint_gather(0, T1, again)
+    fresh.sync()
+    assert torch.equal(again, body)
+    tk_a, out_a = _run_chunk(dl, wa, wi, shape, seed, T1, T2, {}, check=False)
+    tk_b, out_b = _run_chunk(fresh, wa, wi, shape, seed, T1, T2, {}, check=False)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b)
+    if tk_a is not None:
+        assert torch.equal(tk_a, tk_b)
