@@ -120,9 +120,10 @@ static_assert(B_QREADY1 == B_QREADY0 + 1 && B_SFULL1 == B_SFULL0 + 1 && B_SFREE1
 static_assert(B_COUNT == 2 * RING + 16, "the layout's barrier count");
 
 struct TcAttnParams {
-    float *out;
-    const float *q;                  // [n_q][nh][D]
-    int nh;                          // the layer's query heads (<= H: the kernel runs H, the rest padded)
+    float *out;                      // this launch's first head of out[n_q][..][D], o_ld floats per query
+    const float *q;                  // this launch's first head of q[n_q][..][D], q_ld floats per query
+    int64_t q_ld, o_ld;
+    int nh;                          // heads of this launch (<= H: the kernel runs H, the rest padded)
     uint16_t *qsplit;                // per CTA two buffers [D/64][2H][64] bf16 of split queries, or (qpre)
                                      // every query's [D/64][2H][64], split before the launch
     int qpre;
@@ -1066,7 +1067,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             }
             // heads past the layer's (nh < H) get zero query rows: their logits are 0 and their
             // outputs are not stored
-            const float4 *src = reinterpret_cast<const float4 *>(p.q + (size_t)(item / p.parts) * p.nh * D);
+            const float4 *src = reinterpret_cast<const float4 *>(p.q + (size_t)(item / p.parts) * p.q_ld);
             const int nf_real = p.nh * (D / 4);
             uint16_t *qd = p.qsplit + ((size_t)blockIdx.x * 2 + buf) * Lay::DC * 2 * H * 64;
             constexpr int NF = H * D / 4 / 128;           // float4 per thread
@@ -1121,7 +1122,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap rawHi, const __grid_constant_
             float inv[H];
 #pragma unroll
             for (int h = 0; h < H; h++) inv[h] = whole ? 1.0f / lfin[h] : 1.0f;
-            float *dst = (whole ? p.out : p.part_o) + (size_t)it * p.nh * D + r;
+            float *dst = (whole ? p.out + (size_t)it * p.o_ld : p.part_o + (size_t)it * p.nh * D) + r;
             for (int j = 0; j < Lay::DB; j++) {
                 float v[H];
                 tmem_load<H>(lane_base + Lay::T_O + j * H, v);
@@ -1152,7 +1153,7 @@ constexpr int SPLIT_ROWS = 4;             // mirror rows per block of raw_split_
 __global__ void raw_split_kernel(uint16_t *__restrict__ mirror, const float *__restrict__ ring,
                                  const float *__restrict__ raw_new, int D, int n_seq, int n_tok, uint64_t pos0,
                                  DecodePos dp, int n_rows, const float *__restrict__ q, uint16_t *__restrict__ qsplit,
-                                 int nh, int early) {
+                                 int nh, int64_t q_ld, int early) {
     const int raw_blocks = (n_rows + SPLIT_ROWS - 1) / SPLIT_ROWS;
     if ((int)blockIdx.x >= raw_blocks) {
         // the query split (decode): one 64-d chunk c of query n per block, as the attention's
@@ -1166,7 +1167,7 @@ __global__ void raw_split_kernel(uint16_t *__restrict__ mirror, const float *__r
 #pragma unroll
         for (int k = 0; k < 8; k++) {                  // 64 heads x 16 float4, every load first
             const int f = threadIdx.x + 128 * k, h = f >> 4, e = (f & 15) * 4;
-            v[k] = h < nh ? *reinterpret_cast<const float4 *>(q + ((size_t)n * nh + h) * D + 64 * c + e)
+            v[k] = h < nh ? *reinterpret_cast<const float4 *>(q + (size_t)n * q_ld + (size_t)h * D + 64 * c + e)
                           : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
@@ -1228,7 +1229,8 @@ __global__ void raw_split_kernel(uint16_t *__restrict__ mirror, const float *__r
 // thread reads its head's part maxima and denominators together with its
 // partial outputs and forms the weights itself, so the block has no barrier.
 constexpr int COMBINE_MAX_PARTS = 8;
-__global__ void __launch_bounds__(128) attn_combine_kernel(float *__restrict__ out, const float *__restrict__ part_o,
+__global__ void __launch_bounds__(128) attn_combine_kernel(float *__restrict__ out, int64_t o_ld,
+                                                           const float *__restrict__ part_o,
                                                            const float *__restrict__ part_ml, int H, int D, int parts,
                                                            float *__restrict__ ring, const float *__restrict__ raw_new,
                                                            DecodePos dp) {
@@ -1268,7 +1270,8 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(float *__restrict__ o
             acc.x += wq * o[q].x; acc.y += wq * o[q].y; acc.z += wq * o[q].z; acc.w += wq * o[q].w;
         }
         const float id = 1.0f / den;
-        *reinterpret_cast<float4 *>(out + ((size_t)n * H + h) * D + d) = make_float4(acc.x * id, acc.y * id, acc.z * id, acc.w * id);
+        *reinterpret_cast<float4 *>(out + (size_t)n * o_ld + (size_t)h * D + d) =
+            make_float4(acc.x * id, acc.y * id, acc.z * id, acc.w * id);
     }
 }
 
@@ -1310,7 +1313,7 @@ int sm_count() {
 }
 
 template <int H, int D>
-cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, cudaStream_t s) {
+cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, bool commit, cudaStream_t s) {
     using Lay = L<H, D>;
     const uint64_t raw_rows = (a.n_seq == 1) ? (uint64_t)(ROWS + a.n_tok) : (uint64_t)a.n_seq * ROWS;
     CUtensorMap rh, rl;
@@ -1338,9 +1341,9 @@ cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, cudaStream_t s
     e = launch_pdl(attn_tc_kernel<H, D>, dim3(grid), dim3(THREADS), Lay::SMEM, s, rh, rl, qm, p);
     if (e != cudaSuccess || p.parts == 1) return e;
     if (p.parts > COMBINE_MAX_PARTS) return cudaErrorNotSupported;
-    return launch_pdl(attn_combine_kernel, dim3(a.n_seq * a.n_tok * a.H), dim3(128), 0, s, a.out,
-                      (const float *)p.part_o, (const float *)p.part_ml, a.H, D, p.parts,
-                      a.commit_ring ? const_cast<float *>(a.ring) : nullptr, a.raw_new, p.dp);
+    return launch_pdl(attn_combine_kernel, dim3(a.n_seq * a.n_tok * p.nh), dim3(128), 0, s, p.out, p.o_ld,
+                      (const float *)p.part_o, (const float *)p.part_ml, p.nh, D, p.parts,
+                      commit ? const_cast<float *>(a.ring) : nullptr, a.raw_new, p.dp);
 }
 
 }  // namespace
@@ -1361,16 +1364,16 @@ int attn_tc_decode_parts(int ratio, int k, int comp_cap) {
 }
 
 bool attn_tc_supported(int H, int D, int S, int ratio, int k) {
-    // up to 64 query heads (fewer are padded to 64: the S product's N = 2H and the output
-    // accumulator's H columns per d-block fill the 512 TMEM columns at 64)
-    const bool hd = H >= 1 && H <= 64 && (D == 512 || D == 256 || D == 128);
+    // 64 query heads per launch (fewer are padded to 64: the S product's N = 2H and the output
+    // accumulator's H columns per d-block fill the 512 TMEM columns at 64); more than 64 run
+    // as groups of 64
+    const bool hd = H >= 1 && H <= 128 && (D == 512 || D == 256 || D == 128);
     return hd && S == ROWS && (ratio == 0 || ratio == 4 || ratio == 128) && (ratio != 4 || k <= MAX_LIST);
 }
 
 cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *dp, cudaStream_t s) {
     const int nq = a.n_seq * a.n_tok;
     if (nq <= 0) return cudaSuccess;
-    // raw mirror
     DecodePos dd{};
     if (a.n_seq > 1) dd = *dp;
     const int raw_rows = (a.n_seq == 1) ? ROWS + a.n_tok : a.n_seq * ROWS;
@@ -1379,40 +1382,50 @@ cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *dp, cudaSt
     const int parts = a.parts > 0 ? a.parts : 1;
     const bool qpre = parts > 1 && nq <= 2 * sm_count();
     const int q_blocks = qpre ? nq * (a.D / 64) : 0;
-    const int early = (pdl_prev_is(s, PDL_TOPK) || pdl_prev_is(s, PDL_DECODE_COMPRESS)) ? 1 : 0;
-    cudaError_t e = launch_pdl(raw_split_kernel, dim3((raw_rows + SPLIT_ROWS - 1) / SPLIT_ROWS + q_blocks), dim3(128),
-                               0, s, a.raw_mirror, a.ring, a.raw_new, a.D, a.n_seq, a.n_tok, a.pos0, dd, raw_rows,
-                               a.q, a.qsplit, a.H, early);
-    if (e != cudaSuccess) return e;
-    TcAttnParams p{};
-    p.out = a.out;
-    p.q = a.q;
-    p.nh = a.H;
-    p.qsplit = a.qsplit;
-    p.qpre = qpre ? 1 : 0;
-    p.topk = a.topk;
-    p.comp_split = a.comp_split;
-    p.nope_chunks = (a.D - a.n_rot) / 64;
-    p.nope_blocks = (a.D - a.n_rot) / 128;
-    p.parts = parts;
-    p.part_o = a.part_o;
-    p.part_ml = a.part_ml;
-    p.n_q = nq;
-    p.n_seq = a.n_seq;
-    p.n_tok = a.n_tok;
-    p.k = a.k;
-    p.ratio = a.ratio;
-    p.comp_cap = a.comp_cap;
-    p.scale_log2 = a.scale * 1.4426950408889634f;
-    p.pos0 = a.pos0;
-    p.dp = dd;
-#define DS4C_HD(h, d) \
-    if (a.H <= h && a.D == d) return launch_hd<h, d>(a, p, s);
-    DS4C_HD(64, 512)
-    DS4C_HD(64, 256)
-    DS4C_HD(64, 128)
-#undef DS4C_HD
-    return cudaErrorNotSupported;
+    // More than 64 heads run as groups of 64 (the last one padded), one raw split, attention
+    // and (split rows) combine per group, each over the same rows; the ring takes the step's
+    // row after the last group (the combine) or after the call (ring commit)
+    const int groups = (a.H + 63) / 64;
+    for (int g = 0; g < groups; g++) {
+        const int h0 = 64 * g, nh = a.H - h0 < 64 ? a.H - h0 : 64;
+        const float *q = a.q + (size_t)h0 * a.D;
+        // raw mirror (and, split rows, the queries of this group)
+        const int early = (pdl_prev_is(s, PDL_TOPK) || pdl_prev_is(s, PDL_DECODE_COMPRESS)) ? 1 : 0;
+        cudaError_t e = launch_pdl(raw_split_kernel, dim3((raw_rows + SPLIT_ROWS - 1) / SPLIT_ROWS + q_blocks),
+                                   dim3(128), 0, s, a.raw_mirror, a.ring, a.raw_new, a.D, a.n_seq, a.n_tok, a.pos0, dd,
+                                   raw_rows, q, a.qsplit, nh, (int64_t)a.H * a.D, early);
+        if (e != cudaSuccess) return e;
+        TcAttnParams p{};
+        p.out = a.out + (size_t)h0 * a.D;
+        p.q = q;
+        p.q_ld = p.o_ld = (int64_t)a.H * a.D;
+        p.nh = nh;
+        p.qsplit = a.qsplit;
+        p.qpre = qpre ? 1 : 0;
+        p.topk = a.topk;
+        p.comp_split = a.comp_split;
+        p.nope_chunks = (a.D - a.n_rot) / 64;
+        p.nope_blocks = (a.D - a.n_rot) / 128;
+        p.parts = parts;
+        p.part_o = a.part_o;
+        p.part_ml = a.part_ml;
+        p.n_q = nq;
+        p.n_seq = a.n_seq;
+        p.n_tok = a.n_tok;
+        p.k = a.k;
+        p.ratio = a.ratio;
+        p.comp_cap = a.comp_cap;
+        p.scale_log2 = a.scale * 1.4426950408889634f;
+        p.pos0 = a.pos0;
+        p.dp = dd;
+        const bool commit = a.commit_ring && g == groups - 1;
+        e = cudaErrorNotSupported;
+        if (a.D == 512) e = launch_hd<64, 512>(a, p, commit, s);
+        else if (a.D == 256) e = launch_hd<64, 256>(a, p, commit, s);
+        else if (a.D == 128) e = launch_hd<64, 128>(a, p, commit, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t attn_tc_set_wait_ns(unsigned long long ns) { return cudaMemcpyToSymbol(g_attn_wait_ns, &ns, sizeof ns); }

@@ -57,10 +57,13 @@ def test_invalid_configs_are_rejected(L):
     assert abi.ds4c_workspace_bytes(_cfg(base), 64) > 0
     big = _cfg(configs.C5.layer, 32768, 32768)
     assert abi.ds4c_attn_uses_tensor_cores(big) == 1
-    # fewer than 64 heads are padded to the MMA tile; more than 64 run on the CUDA cores
+    # fewer than 64 heads are padded to the MMA tile; more than 64 run as groups of 64
     assert abi.ds4c_attn_uses_tensor_cores(_cfg(base)) == (1 if base.head_dim in (128, 256, 512) else 0)
-    many = _cfg(configs.LayerShape(**{**configs.C5.layer.__dict__, "n_heads": 128}), 32768, 32768)
-    assert abi.ds4c_attn_uses_tensor_cores(many) == 0
+    many = _cfg(configs.LayerShape(**{**configs.C5.layer.__dict__, "n_heads": 128, "head_dim": 256}), 32768, 32768)
+    assert abi.ds4c_attn_uses_tensor_cores(many) == 1
+    # (128 heads of 512 exceed the configuration's 32768-float query row)
+    too_many = _cfg(configs.LayerShape(**{**configs.C5.layer.__dict__, "n_heads": 128}), 32768, 32768)
+    assert abi.ds4c_attn_uses_tensor_cores(too_many) == 0
     # the tensor-core path holds a row list of at most 512 entries; larger top-k runs on the CUDA cores
     wide = _cfg(configs.LayerShape(**{**configs.C5.layer.__dict__, "top_k": 1024}), 32768, 32768)
     assert abi.ds4c_attn_uses_tensor_cores(wide) == 0
