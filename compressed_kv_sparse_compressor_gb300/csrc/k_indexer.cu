@@ -349,15 +349,17 @@ constexpr int TK_PREFILL = 256, TK_DECODE = 1024;
 
 // Dynamic shared memory in u32 words:
 //   bins [max(4096, 16 T)] | candidate keys [2048] | candidate rows [2048] |
-//   selected bitmap [wcap] | equal-key bitmap [wcap] | resident keys [vmax]
+//   selected bitmap [wcap] | equal-key bitmap [wcap] | resident keys [vmax rounded up to 4]
+// (wcap even, so that the resident keys start on 16 bytes and are stored four at a time)
 // The radix path reuses the bins as its per-thread counters and the candidate
 // lists as its 4096-key survivor buffer.
 template <int T>
 __host__ __device__ constexpr int tk_bin_words() { return TK_HBINS > TK_BINS * T ? TK_HBINS : TK_BINS * T; }
+inline uint64_t tk_wcap(uint64_t vmax) { return ((vmax + 31) / 32 + 1) & ~(uint64_t)1; }
 template <int T>
 size_t tk_smem(uint64_t vmax, bool resident) {
-    const uint64_t wcap = (vmax + 31) / 32;
-    return sizeof(uint32_t) * ((size_t)tk_bin_words<T>() + 2 * TK_CAND + 2 * wcap + (resident ? vmax : 0));
+    return sizeof(uint32_t) * ((size_t)tk_bin_words<T>() + 2 * TK_CAND + 2 * tk_wcap(vmax) +
+                               (resident ? (vmax + 3) / 4 * 4 : 0));
 }
 static_assert(2 * TK_CAND >= TK_RCAND, "radix survivors fit the candidate lists");
 
@@ -631,10 +633,10 @@ __global__ void __launch_bounds__(T) topk_kernel(IndexerArgs a, DecodePos dp, in
     __syncthreads();
     // 1. histogram of the top 12 key bits (resident: the keys land in shared memory).  A row
     //    of the workspace (16-byte aligned, a multiple of 4 floats long) is read four scores
-    //    per load; its floats past V exist and are skipped.
+    //    per load; its floats past V exist and are skipped (resident: stored as keys 0, never read).
     constexpr int SH1 = 32 - TK_HBITS;
     constexpr int U4 = TK_UNR / 4;
-    const bool vec4 = !RESIDENT && (a.lds & 3) == 0 && (reinterpret_cast<uintptr_t>(s) & 15u) == 0;
+    const bool vec4 = (a.lds & 3) == 0 && (reinterpret_cast<uintptr_t>(s) & 15u) == 0;
     const float4 *s4 = reinterpret_cast<const float4 *>(s);
     const int V4 = (V + 3) / 4;
     if (vec4) {
@@ -643,15 +645,20 @@ __global__ void __launch_bounds__(T) topk_kernel(IndexerArgs a, DecodePos dp, in
 #pragma unroll
             for (int u = 0; u < U4; u++) {
                 const int i4 = base + u * T + tid;
-                v[u] = (i4 < V4) ? __ldg(s4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[u] = (i4 < V4) ? (RESIDENT ? __ldcs(s4 + i4) : __ldg(s4 + i4)) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int u = 0; u < U4; u++) {
                 const int i4 = base + u * T + tid;
                 const float e4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                uint32_t k4[4];
 #pragma unroll
-                for (int e = 0; e < 4; e++)
-                    if (4 * i4 + e < V) atomicAdd(&bins[order_key(e4[e]) >> SH1], 1u);
+                for (int e = 0; e < 4; e++) {
+                    k4[e] = 4 * i4 + e < V ? order_key(e4[e]) : 0u;
+                    if (4 * i4 + e < V) atomicAdd(&bins[k4[e] >> SH1], 1u);
+                }
+                if (RESIDENT && i4 < V4)
+                    *reinterpret_cast<uint4 *>(keys + 4 * i4) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
             }
         }
     } else
@@ -689,23 +696,31 @@ __global__ void __launch_bounds__(T) topk_kernel(IndexerArgs a, DecodePos dp, in
     if (vec4) {
         for (int base = 0; base < V4; base += T * U4) {
             float4 v[U4];
+            uint4 kr[U4];
 #pragma unroll
             for (int u = 0; u < U4; u++) {
                 const int i4 = base + u * T + tid;
-                v[u] = (i4 < V4) ? __ldcs(s4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                if (RESIDENT) kr[u] = (i4 < V4) ? *reinterpret_cast<const uint4 *>(keys + 4 * i4) : make_uint4(0u, 0u, 0u, 0u);
+                else v[u] = (i4 < V4) ? __ldcs(s4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int u = 0; u < U4; u++) {
                 const int g0 = base + u * T + warp * 32;     // the warp's first group of four rows
                 if (4 * g0 >= V) continue;                   // the whole warp is past the end
                 const int i4 = g0 + lane;
-                const float e4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                uint32_t k4[4];
+                if (RESIDENT) {
+                    k4[0] = kr[u].x; k4[1] = kr[u].y; k4[2] = kr[u].z; k4[3] = kr[u].w;
+                } else {
+                    k4[0] = order_key(v[u].x); k4[1] = order_key(v[u].y); k4[2] = order_key(v[u].z);
+                    k4[3] = order_key(v[u].w);
+                }
                 uint32_t nib = 0;
 #pragma unroll
                 for (int e = 0; e < 4; e++) {
                     const int r = 4 * i4 + e;
                     if (r >= V) continue;
-                    const uint32_t key = order_key(e4[e]);
+                    const uint32_t key = k4[e];
                     const uint32_t b = key >> SH1;
                     if (b > bstar) nib |= 1u << e;
                     else if (b == bstar) {
@@ -823,7 +838,7 @@ cudaError_t launch_topk(const IndexerArgs &a, const DecodePos &dp, int n_q, uint
                         cudaStream_t s) {
     constexpr size_t LIMIT = 200 * 1024;
     if (vmax == 0) vmax = 1;
-    const int wcap = (int)((vmax + 31) / 32);
+    const int wcap = (int)tk_wcap(vmax);
     cudaError_t e;
     if (allow_resident && tk_smem<T>(vmax, true) <= LIMIT) {
         const size_t smem = tk_smem<T>(vmax, true);
