@@ -536,6 +536,7 @@ ds4c_status ds4c_sparse_swa_attn(const ds4c_layer_cfg *cfg, const ds4c_layer_sta
         a.k = (int)c.top_k;
         a.comp_cap = (int)c.comp_cap;
         a.n_rot = (int)c.n_rot;
+        a.S = (int)c.swa;
         a.scale = c.attn_scale;
         a.n_seq = (int)n_seq;
         a.n_tok = (int)n_tok;

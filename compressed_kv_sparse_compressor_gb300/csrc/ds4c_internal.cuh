@@ -290,6 +290,7 @@ struct AttnTcArgs {
     const int32_t *topk;
     float *out;
     int D, H, ratio, k, comp_cap, n_rot;
+    int S;                        // raw window = ring rows (at most 128)
     float scale;
     int n_seq, n_tok, n_seq_state;
     uint64_t pos0;

@@ -130,6 +130,7 @@ struct TcAttnParams {
     const int32_t *topk;
     const uint16_t *comp_split;      // [rows][2][D]
     int n_q, n_seq, n_tok, k, ratio, comp_cap;
+    int swa;                         // raw window (ring rows), at most 128: the raw tile's valid rows
     int nope_chunks, nope_blocks;    // 64-wide chunks / 128-wide blocks inside the FP8 dims
     int parts;                       // work items per query (1: whole query; >1: split rows, partial outputs)
     float *part_o;                   // [n_q * parts][nh][D] unnormalised partial outputs
@@ -382,15 +383,15 @@ __device__ __forceinline__ Tok token_geom(const TcAttnParams &p, int n) {
         k.seq = 0;
         k.t = p.pos0 + (uint64_t)n;
         k.raw_row0 = n + 1;                               // mirror row u <-> position pos0 - 128 + u
-        const int lo = (k.t >= 127) ? 0 : (int)(127 - k.t);
-        k.raw_lo = lo;
+        // the window's positions t - swa + 1 .. t (from 0 on) are the tile's last rows
+        k.raw_lo = ROWS - 1 - (int)(k.t < (uint64_t)(p.swa - 1) ? k.t : (uint64_t)(p.swa - 1));
         k.raw_hi = ROWS - 1;
     } else {
         k.seq = n;
         k.t = p.dp.pos[n];
-        k.raw_row0 = n * ROWS;                            // mirror rows = the sequence's 128 ring slots
+        k.raw_row0 = n * ROWS;                            // mirror rows = the sequence's swa ring slots, then zeros
         k.raw_lo = 0;
-        k.raw_hi = (k.t >= 127) ? ROWS - 1 : (int)k.t;    // slot s holds position s while t < 128
+        k.raw_hi = k.t < (uint64_t)(p.swa - 1) ? (int)k.t : p.swa - 1;   // slot s holds position s while t < swa
     }
     return k;
 }
@@ -1153,7 +1154,7 @@ constexpr int SPLIT_ROWS = 4;             // mirror rows per block of raw_split_
 __global__ void raw_split_kernel(uint16_t *__restrict__ mirror, const float *__restrict__ ring,
                                  const float *__restrict__ raw_new, int D, int n_seq, int n_tok, uint64_t pos0,
                                  DecodePos dp, int n_rows, const float *__restrict__ q, uint16_t *__restrict__ qsplit,
-                                 int nh, int64_t q_ld, int early) {
+                                 int nh, int64_t q_ld, int S, int early) {
     const int raw_blocks = (n_rows + SPLIT_ROWS - 1) / SPLIT_ROWS;
     if ((int)blockIdx.x >= raw_blocks) {
         // the query split (decode): one 64-d chunk c of query n per block, as the attention's
@@ -1193,13 +1194,14 @@ __global__ void raw_split_kernel(uint16_t *__restrict__ mirror, const float *__r
     auto source = [&](int u) -> const float * {
         if (n_seq == 1) {
             const int64_t pos = (int64_t)pos0 - ROWS + u;
-            if (pos < 0) return nullptr;
-            return (pos < (int64_t)pos0) ? ring + (size_t)(pos % ROWS) * D : raw_new + (size_t)(pos - (int64_t)pos0) * D;
+            if (pos < 0 || pos < (int64_t)pos0 - S) return nullptr;  // before 0, or older than the ring holds
+            return (pos < (int64_t)pos0) ? ring + (size_t)(pos % S) * D : raw_new + (size_t)(pos - (int64_t)pos0) * D;
         }
         const int b = u / ROWS, slot = u % ROWS;
         const uint64_t pos = dp.pos[b];
-        if (pos < ROWS && (uint64_t)slot > pos) return nullptr;      // slot not written yet
-        return ((uint64_t)slot == pos % ROWS) ? raw_new + (size_t)b * D : ring + ((size_t)b * ROWS + slot) * D;
+        if (slot >= S) return nullptr;                                // past the ring
+        if (pos < (uint64_t)S && (uint64_t)slot > pos) return nullptr;  // slot not written yet
+        return ((uint64_t)slot == pos % S) ? raw_new + (size_t)b * D : ring + ((size_t)b * S + slot) * D;
     };
     const int u0 = blockIdx.x * SPLIT_ROWS;
     for (int j = threadIdx.x * 4; j < D; j += blockDim.x * 4) {
@@ -1233,14 +1235,14 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(float *__restrict__ o
                                                            const float *__restrict__ part_o,
                                                            const float *__restrict__ part_ml, int H, int D, int parts,
                                                            float *__restrict__ ring, const float *__restrict__ raw_new,
-                                                           DecodePos dp) {
+                                                           int S, DecodePos dp) {
     pdl_wait();
     pdl_launch_dependents();
     const int n = blockIdx.x / H, h = blockIdx.x % H;
     // ring commit of the step (decode: query n is sequence n): the attention read the ring
     // through the raw mirror, so the slot can take the new row now
     if (ring && h == 0) {
-        float *dst = ring + ((size_t)n * ROWS + (size_t)(dp.pos[n] % ROWS)) * D;
+        float *dst = ring + ((size_t)n * S + (size_t)(dp.pos[n] % (uint64_t)S)) * D;
         const float *src = raw_new + (size_t)n * D;
         for (int d = threadIdx.x * 4; d < D; d += blockDim.x * 4)
             *reinterpret_cast<float4 *>(dst + d) = *reinterpret_cast<const float4 *>(src + d);
@@ -1343,7 +1345,7 @@ cudaError_t launch_hd(const AttnTcArgs &a, const TcAttnParams &p, bool commit, c
     if (p.parts > COMBINE_MAX_PARTS) return cudaErrorNotSupported;
     return launch_pdl(attn_combine_kernel, dim3(a.n_seq * a.n_tok * p.nh), dim3(128), 0, s, p.out, p.o_ld,
                       (const float *)p.part_o, (const float *)p.part_ml, p.nh, D, p.parts,
-                      commit ? const_cast<float *>(a.ring) : nullptr, a.raw_new, p.dp);
+                      commit ? const_cast<float *>(a.ring) : nullptr, a.raw_new, a.S, p.dp);
 }
 
 }  // namespace
@@ -1368,7 +1370,8 @@ bool attn_tc_supported(int H, int D, int S, int ratio, int k) {
     // accumulator's H columns per d-block fill the 512 TMEM columns at 64); more than 64 run
     // as groups of 64
     const bool hd = H >= 1 && H <= 128 && (D == 512 || D == 256 || D == 128);
-    return hd && S == ROWS && (ratio == 0 || ratio == 4 || ratio == 128) && (ratio != 4 || k <= MAX_LIST);
+    // a raw window of at most one 128-row tile (a shorter one masks the tile's older rows)
+    return hd && S >= 1 && S <= ROWS && (ratio == 0 || ratio == 4 || ratio == 128) && (ratio != 4 || k <= MAX_LIST);
 }
 
 cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *dp, cudaStream_t s) {
@@ -1393,7 +1396,7 @@ cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *dp, cudaSt
         const int early = (pdl_prev_is(s, PDL_TOPK) || pdl_prev_is(s, PDL_DECODE_COMPRESS)) ? 1 : 0;
         cudaError_t e = launch_pdl(raw_split_kernel, dim3((raw_rows + SPLIT_ROWS - 1) / SPLIT_ROWS + q_blocks),
                                    dim3(128), 0, s, a.raw_mirror, a.ring, a.raw_new, a.D, a.n_seq, a.n_tok, a.pos0, dd,
-                                   raw_rows, q, a.qsplit, nh, (int64_t)a.H * a.D, early);
+                                   raw_rows, q, a.qsplit, nh, (int64_t)a.H * a.D, a.S, early);
         if (e != cudaSuccess) return e;
         TcAttnParams p{};
         p.out = a.out + (size_t)h0 * a.D;
@@ -1415,6 +1418,7 @@ cudaError_t launch_attention_tc(const AttnTcArgs &a, const DecodePos *dp, cudaSt
         p.k = a.k;
         p.ratio = a.ratio;
         p.comp_cap = a.comp_cap;
+        p.swa = a.S;
         p.scale_log2 = a.scale * 1.4426950408889634f;
         p.pos0 = a.pos0;
         p.dp = dd;

@@ -140,7 +140,8 @@ typedef struct {
 /* 1 when ds4c_sparse_swa_attn runs on the tensor cores for this shape
  * (ratio 0/4/128 with any n_heads: 64 per launch, fewer padded to 64 rows of
  * the MMA tile, more than 64 as groups of 64 that each read the rows again),
- * head_dim in {128, 256, 512}, swa == 128,
+ * head_dim in {128, 256, 512}, swa <= 128 (a shorter window masks the older rows
+ * of the 128-row raw tile),
  * and top_k <= 512 on ratio-4 layers), 0 when it runs on the CUDA cores.  On
  * the tensor-core path the attention lane's comp_split mirror must be
  * allocated. */

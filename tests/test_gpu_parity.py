@@ -119,16 +119,18 @@ def test_c1_chain_against_oracle_end_to_end():
 # Multi-tile shapes with ragged tails (D=512, d=128, 64 heads)
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("ratio,heads,D", [(0, 64, 512), (4, 64, 512), (128, 64, 512), (4, 32, 512),
-                                           (4, 64, 128), (4, 64, 256), (128, 64, 256), (128, 8, 256),
-                                           (0, 16, 128), (4, 128, 128), (0, 128, 128), (4, 96, 128)])
-def test_ragged_chunks(ratio, heads, D):
+@pytest.mark.parametrize("ratio,heads,D,swa", [(0, 64, 512, 128), (4, 64, 512, 128), (128, 64, 512, 128),
+                                               (4, 32, 512, 128), (4, 64, 128, 128), (4, 64, 256, 128),
+                                               (128, 64, 256, 128), (128, 8, 256, 128), (0, 16, 128, 128),
+                                               (4, 128, 128, 128), (0, 128, 128, 128), (4, 96, 128, 128),
+                                               (4, 64, 512, 64), (0, 64, 256, 32), (128, 32, 512, 100)])
+def test_ragged_chunks(ratio, heads, D, swa):
     """heads <= 64: tensor-core attention (head_dim 512, 256 or 128: at 128 the one
     128-wide d-block holds the RoPE dims, so no block is FP8-exact; fewer than 64
-    heads run padded to 64 with zero query rows); heads = 128 or 96: CUDA-core
-    attention (96 x 128: each thread's accumulator slots are not all used)."""
+    heads run padded to 64 with zero query rows); heads = 128 or 96: groups of 64
+    heads.  Rings shorter than 128 rows (swa 64, 32, 100) mask the raw tile's older rows."""
     shape = configs.LayerShape(d_model=512, head_dim=D, n_rot=64, idx_head_dim=128 if D >= 256 else 64,
-                               n_heads=heads, ratio=ratio, top_k=16, dtype="bf16", w_std=0.04)
+                               n_heads=heads, ratio=ratio, swa=swa, top_k=16, dtype="bf16", w_std=0.04)
     seed = 21
     T_total = 300 if ratio != 128 else 700
     cap = T_total // max(ratio, 1) + 1
@@ -146,15 +148,18 @@ def test_ragged_chunks(ratio, heads, D):
 # Decode: B sequences, one token each at staggered positions
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("ratio,base,heads,top_k", [(4, 60, 64, 16), (128, 380, 64, 16), (0, 200, 64, 16),
-                                                    (4, 60, 8, 16), (128, 380, 24, 16), (4, 1600, 64, 384),
-                                                    (4, 1600, 24, 1024)])
-def test_decode_small(ratio, base, heads, top_k):
+@pytest.mark.parametrize("ratio,base,heads,top_k,swa", [(4, 60, 64, 16, 128), (128, 380, 64, 16, 128),
+                                                        (0, 200, 64, 16, 128), (4, 60, 8, 16, 128),
+                                                        (128, 380, 24, 16, 128), (4, 1600, 64, 384, 128),
+                                                        (4, 1600, 24, 1024, 128), (4, 60, 64, 16, 32),
+                                                        (0, 28, 64, 16, 32)])
+def test_decode_small(ratio, base, heads, top_k, swa):
     """heads < 64: the padded tensor-core attention, split rows combined over the real heads.
     top_k 384: four row tiles, split as the raw tile, two compressed tiles and one.
-    top_k 1024: the CUDA-core attention (lists longer than the tensor-core path takes), 24 heads."""
+    top_k 1024: the CUDA-core attention (lists longer than the tensor-core path takes), 24 heads.
+    swa 32: a ring shorter than the raw tile (positions 60..67 wrap it; 28..35 fill it)."""
     shape = configs.LayerShape(d_model=512, head_dim=512, n_rot=64, idx_head_dim=128, n_heads=heads, ratio=ratio,
-                               top_k=top_k, dtype="bf16", w_std=0.04)
+                               swa=swa, top_k=top_k, dtype="bf16", w_std=0.04)
     seed, B = 31, 8
     # every stagger class; ratio 4: some emit this step; ratio 128: 382 + 1 ends a window
     # (383 = 3*128 - 1), the others sit mid-window over 2 visible rows; ratio 0: a wrapped ring
