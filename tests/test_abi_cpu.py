@@ -64,6 +64,11 @@ def test_invalid_configs_are_rejected(L):
     # (128 heads of 512 exceed the configuration's 32768-float query row)
     too_many = _cfg(configs.LayerShape(**{**configs.C5.layer.__dict__, "n_heads": 128}), 32768, 32768)
     assert abi.ds4c_attn_uses_tensor_cores(too_many) == 0
+    # a raw window of at most one 128-row tile runs on the tensor cores (shorter ones masked); longer on
+    # the CUDA cores
+    for swa, tc in ((32, 1), (100, 1), (128, 1), (256, 0)):
+        ring = _cfg(configs.LayerShape(**{**configs.C5.layer.__dict__, "swa": swa}), 32768, 32768)
+        assert abi.ds4c_attn_uses_tensor_cores(ring) == tc, swa
     # the tensor-core path holds a row list of at most 512 entries; larger top-k runs on the CUDA cores
     wide = _cfg(configs.LayerShape(**{**configs.C5.layer.__dict__, "top_k": 1024}), 32768, 32768)
     assert abi.ds4c_attn_uses_tensor_cores(wide) == 0
