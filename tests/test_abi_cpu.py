@@ -208,3 +208,13 @@ def test_payload_bytes_and_host_validation(L, orc):
     assert abi.ds4c_payload_read(info, cfgs, st, 0, None, need, tok, lg, None)[0] == abi.DS4C_ERR_NULL
     assert abi.ds4c_payload_read(info, cfgs, st, 0, FAKE + 4, need, tok, lg, None)[0] == abi.DS4C_ERR_SHAPE
     assert abi.ds4c_payload_read(info, cfgs, st, 0, FAKE, 10, tok, lg, None)[0] == abi.DS4C_ERR_CAPACITY
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    """No fallback: with the shared library absent, the binding raises instead of computing."""
+    monkeypatch.setattr(abi, "_lib", None)
+    monkeypatch.setattr(abi, "LIB_PATH", "/nonexistent/libds4c.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        abi.lib()
+    with pytest.raises(RuntimeError):
+        abi.ds4c_workspace_bytes(abi.LayerCfg(), 64)
