@@ -11,7 +11,8 @@
  * through RMSNorm, a RoPE on its last n_rot dims and (attention lane) an FP8
  * E4M3 round trip before it is appended to the compressed KV.  Ratio-4 layers
  * run a second (indexer) lane; a top-k over the indexer rows selects which
- * compressed rows the attention sees next to a 128-row raw sliding window.
+ * compressed rows the attention sees next to a raw sliding window (swa rows,
+ * 128 in the pages' model).
  *
  * Conventions shared by every call
  *   - Tensor pointers are DEVICE pointers owned by the caller, unless a name
